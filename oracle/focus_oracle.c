@@ -1,0 +1,294 @@
+/*
+ * Focus centroid-gated sparse attention, forward pass: plain fp64 CPU oracle.
+ *
+ * TEST INFRASTRUCTURE ONLY. This file is the slow, obviously correct statement of
+ * what the CUDA path computes. Only the tests, the smoke check and the benchmark's
+ * CPU-baseline leg may build, load or call it. It shares no code, header, table or
+ * helper with the CUDA library, and the CUDA library never calls it.
+ *
+ * Source: "Why Attend to Everything? Focus is the Key" (Yao, Chen et al.).
+ *   [GS-CA]  gist.science technical summary, section 2 "Core Architecture":
+ *            K learnable centroids C in R^{K x d_g}; each token's hidden state is
+ *            projected into centroid space; local window w attends with exact
+ *            softmax; distant tokens attend only within a shared group.
+ *   [GS-TK]  same section, "Inference Efficiency (Top-k)": each token joins its
+ *            top-k highest-scoring groups; distant tokens interact only if they
+ *            share at least one group; cost O(n^2/K + n w).
+ *   [GS-SH]  same summary, "Key Technical Innovation: Sinkhorn Normalization":
+ *            Sinkhorn replaces softmax and enforces balanced group sizes
+ *            (doubly-stochastic assignment).
+ *   [JB-M]   jindou-blog deep read, method bullets: K centroids per layer,
+ *            routing dimension 16, tokens scored against centroids by dot product;
+ *            window part is full-precision softmax, long-range part is an exact
+ *            softmax restricted to same-group pairs.
+ *
+ * Readings taken where the pages are silent (each one is listed in the design notes):
+ *   - score s_ig = r_i . c_g (dot product, [JB-M]);
+ *   - Sinkhorn is the log-domain SwAV-style iteration: column step gives each group
+ *     mass N/K, row step gives each token mass 1; eps scales the scores; run over
+ *     the whole sequence of one (batch, routing head); top-k ranks by the final
+ *     column-normalised log-score kappa_ig = s_ig/eps + beta_g (the row potential
+ *     cannot reorder a row);
+ *   - top-k ties go to the lower group index;
+ *   - window pairs are j <= i with i - j < w (diagonal included); long-range pairs
+ *     are j <= i - w whose masks intersect; the attended set is the union, each key
+ *     once, and one softmax runs over it;
+ *   - logits are scale * q_i . k_j (scale = 1/sqrt(d) by default); LSE is the
+ *     natural log of the sum of exp of those scaled logits.
+ *
+ * Numbers: Q/K/V arrive as bf16 bit patterns and are widened exactly to double;
+ * r and C are fp32 and widened exactly. All arithmetic below is double, except the
+ * optional fp32 score mode (score_fp32 = 1), which forms each score as the same
+ * fixed-order fused multiply-add chain over t = 0..15 that a single-precision
+ * implementation would use, so that argmax decisions can be compared in the
+ * kernel's precision.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define DG 16
+
+static double bf16_to_double(uint16_t h) {
+  uint32_t u = ((uint32_t)h) << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return (double)f;
+}
+
+/* ---------------------------------------------------------------- routing -- */
+
+/* s_ig = sum_t r_it c_gt  ([JB-M]: dot-product score of token i against centroid g). */
+static double score(const float* ri, const float* cg, int score_fp32) {
+  if (score_fp32) {
+    float s = 0.0f;
+    for (int t = 0; t < DG; ++t) s = fmaf(ri[t], cg[t], s);
+    return (double)s;
+  }
+  double s = 0.0;
+  for (int t = 0; t < DG; ++t) s += (double)ri[t] * (double)cg[t];
+  return s;
+}
+
+/* log sum_j exp(x_j) with the maximum shifted out. */
+static double logsumexp(const double* x, int64_t n, int64_t stride) {
+  double m = -INFINITY;
+  for (int64_t j = 0; j < n; ++j) if (x[j * stride] > m) m = x[j * stride];
+  if (m == -INFINITY) return -INFINITY;
+  double s = 0.0;
+  for (int64_t j = 0; j < n; ++j) s += exp(x[j * stride] - m);
+  return m + log(s);
+}
+
+/*
+ * Routing for every (b, routing head rho): scores, optional Sinkhorn, top-k.
+ *   r      [B, N, R, 16] fp32      C [K, 16] fp32
+ *   mask   [B, R, N] uint32 out: bit g set iff g is among the token's top_k groups
+ *   margin [B, R, N] double out (nullable): kappa_(k) - kappa_(k+1), +inf if k == K
+ *   kappa  [B, R, N, K] double out (nullable): the ranking keys
+ *   beta   [B, R, K] double out (nullable): final column potentials (0 if T == 0)
+ * Returns 0, or -1 on bad arguments.
+ */
+int oracle_route(int B, int N, int R, int K, int top_k, int T, double eps, int score_fp32,
+                 const float* r, const float* C, uint32_t* mask, double* margin,
+                 double* kappa_out, double* beta_out) {
+  if (B < 1 || N < 1 || R < 1 || K < 1 || K > 32 || top_k < 1 || top_k > K || T < 0 ||
+      !(eps > 0.0))
+    return -1;
+  double* L = (double*)malloc(sizeof(double) * (size_t)N * K);
+  double* alpha = (double*)malloc(sizeof(double) * (size_t)N);
+  double* col = (double*)malloc(sizeof(double) * (size_t)N);
+  double beta[32];
+  if (!L || !alpha || !col) { free(L); free(alpha); free(col); return -1; }
+
+  for (int b = 0; b < B; ++b) {
+    for (int rho = 0; rho < R; ++rho) {
+      /* 1. scores ([JB-M]); divided by eps when Sinkhorn runs. */
+      for (int64_t i = 0; i < N; ++i) {
+        const float* ri = r + (((int64_t)b * N + i) * R + rho) * DG;
+        for (int g = 0; g < K; ++g) {
+          double s = score(ri, C + (int64_t)g * DG, score_fp32);
+          L[i * K + g] = (T > 0) ? s / eps : s;
+        }
+      }
+      /* 2. Sinkhorn ([GS-SH]), log domain: potentials alpha (rows), beta (columns). */
+      for (int g = 0; g < K; ++g) beta[g] = 0.0;
+      for (int64_t i = 0; i < N; ++i) alpha[i] = 0.0;
+      for (int it = 0; it < T; ++it) {
+        /* column step: sum_i P_ig = N / K */
+        for (int g = 0; g < K; ++g) {
+          for (int64_t i = 0; i < N; ++i) col[i] = L[i * K + g] + alpha[i];
+          beta[g] = log((double)N / (double)K) - logsumexp(col, N, 1);
+        }
+        /* row step: sum_g P_ig = 1 */
+        for (int64_t i = 0; i < N; ++i) {
+          double row[32];
+          for (int g = 0; g < K; ++g) row[g] = L[i * K + g] + beta[g];
+          alpha[i] = -logsumexp(row, K, 1);
+        }
+      }
+      if (beta_out)
+        for (int g = 0; g < K; ++g) beta_out[((int64_t)b * R + rho) * K + g] = beta[g];
+      /* 3. hard top-k membership ([GS-TK]); ties go to the lower group index. */
+      for (int64_t i = 0; i < N; ++i) {
+        double key[32];
+        int taken[32] = {0};
+        for (int g = 0; g < K; ++g) key[g] = L[i * K + g] + beta[g];
+        uint32_t bits = 0;
+        double kth = 0.0;
+        for (int sel = 0; sel < top_k; ++sel) {
+          int best = -1;
+          for (int g = 0; g < K; ++g)
+            if (!taken[g] && (best < 0 || key[g] > key[best])) best = g;
+          taken[best] = 1;
+          bits |= 1u << best;
+          kth = key[best];
+        }
+        double next = -INFINITY;
+        int any_left = 0;
+        for (int g = 0; g < K; ++g)
+          if (!taken[g]) { if (!any_left || key[g] > next) next = key[g]; any_left = 1; }
+        int64_t o = ((int64_t)b * R + rho) * N + i;
+        mask[o] = bits;
+        if (margin) margin[o] = any_left ? kth - next : INFINITY;
+        if (kappa_out)
+          for (int g = 0; g < K; ++g) kappa_out[o * K + g] = key[g];
+      }
+    }
+  }
+  free(L); free(alpha); free(col);
+  return 0;
+}
+
+/* ---------------------------------------------------------------- pairs ----- */
+
+/* Is key j in query i's attended set?  ([GS-CA], [GS-TK], [JB-M]) */
+static int allowed(int64_t i, int64_t j, int w, uint32_t mi, uint32_t mj) {
+  if (j > i) return 0;                 /* causal */
+  if (i - j < w) return 1;             /* local window, every pair */
+  return (mi & mj) != 0;               /* distant: must share a group */
+}
+
+/* Number of allowed (i, j) pairs for every (b, routing head): out [B, R] int64.
+ * Brute force over all pairs; meant for small N. */
+int oracle_allowed_pairs(int B, int N, int R, int w, const uint32_t* mask, int64_t* out) {
+  if (B < 1 || N < 1 || R < 1 || w < 1) return -1;
+  for (int b = 0; b < B; ++b)
+    for (int rho = 0; rho < R; ++rho) {
+      const uint32_t* m = mask + ((int64_t)b * R + rho) * N;
+      int64_t c = 0;
+      for (int64_t i = 0; i < N; ++i)
+        for (int64_t j = 0; j <= i; ++j) c += allowed(i, j, w, m[i], m[j]);
+      out[(int64_t)b * R + rho] = c;
+    }
+  return 0;
+}
+
+/* ------------------------------------------------------------- attention ---- */
+
+typedef struct {
+  int B, N, H, H_kv, R, d, w;
+  double scale;
+  const uint16_t *q, *k, *v;
+  const uint32_t* mask;
+  const int64_t* rows; /* flattened (b * N + i) query rows, or NULL for all */
+  int64_t n_rows;
+  double *o, *lse;
+  int64_t next;        /* work counter */
+  pthread_mutex_t mu;
+} attn_job;
+
+/* One query row of one head: two-pass softmax over the union set A_i. */
+static void attn_row(const attn_job* J, int64_t out_row, int64_t bi, int h, double* s_buf,
+                     int64_t* j_buf, double* qv) {
+  const int b = (int)(bi / J->N);
+  const int64_t i = bi % J->N;
+  const int kvh = h / (J->H / J->H_kv);
+  const int rho = kvh / (J->H_kv / J->R);
+  const int d = J->d;
+  const uint32_t* m = J->mask + ((int64_t)b * J->R + rho) * J->N;
+  const uint16_t* qi = J->q + (((int64_t)b * J->N + i) * J->H + h) * d;
+  for (int t = 0; t < d; ++t) qv[t] = bf16_to_double(qi[t]);
+
+  /* logits over the attended set */
+  int64_t n = 0;
+  double mx = -INFINITY;
+  for (int64_t j = 0; j <= i; ++j) {
+    if (!allowed(i, j, J->w, m[i], m[j])) continue;
+    const uint16_t* kj = J->k + (((int64_t)b * J->N + j) * J->H_kv + kvh) * d;
+    double s = 0.0;
+    for (int t = 0; t < d; ++t) s += qv[t] * bf16_to_double(kj[t]);
+    s *= J->scale;
+    s_buf[n] = s;
+    j_buf[n] = j;
+    if (s > mx) mx = s;
+    ++n;
+  }
+  /* the diagonal is always in the window, so n >= 1 */
+  double sum = 0.0;
+  for (int64_t a = 0; a < n; ++a) sum += exp(s_buf[a] - mx);
+  const double lse = mx + log(sum);
+  double* o = J->o + (out_row * J->H + h) * d;
+  for (int t = 0; t < d; ++t) o[t] = 0.0;
+  for (int64_t a = 0; a < n; ++a) {
+    const double p = exp(s_buf[a] - lse);
+    const uint16_t* vj = J->v + (((int64_t)b * J->N + j_buf[a]) * J->H_kv + kvh) * d;
+    for (int t = 0; t < d; ++t) o[t] += p * bf16_to_double(vj[t]);
+  }
+  J->lse[out_row * J->H + h] = lse;
+}
+
+static void* attn_worker(void* arg) {
+  attn_job* J = (attn_job*)arg;
+  double* s_buf = (double*)malloc(sizeof(double) * (size_t)J->N);
+  int64_t* j_buf = (int64_t*)malloc(sizeof(int64_t) * (size_t)J->N);
+  double* qv = (double*)malloc(sizeof(double) * (size_t)J->d);
+  const int64_t total = J->n_rows * J->H;
+  const int64_t chunk = 4;
+  for (;;) {
+    pthread_mutex_lock(&J->mu);
+    int64_t start = J->next;
+    J->next += chunk;
+    pthread_mutex_unlock(&J->mu);
+    if (start >= total) break;
+    int64_t end = start + chunk < total ? start + chunk : total;
+    for (int64_t u = start; u < end; ++u) {
+      int64_t out_row = u / J->H;
+      int h = (int)(u % J->H);
+      int64_t bi = J->rows ? J->rows[out_row] : out_row;
+      attn_row(J, out_row, bi, h, s_buf, j_buf, qv);
+    }
+  }
+  free(s_buf); free(j_buf); free(qv);
+  return NULL;
+}
+
+/*
+ * Attention forward over the union set, every head, for the requested query rows.
+ *   q [B, N, H, d], k/v [B, N, H_kv, d]: bf16 bit patterns
+ *   mask [B, R, N] uint32 (from oracle_route or from the kernel under test)
+ *   rows (nullable) flattened query rows b*N + i, n_rows of them; NULL = all B*N rows
+ *   o   [n_rows, H, d] double out;  lse [n_rows, H] double out (natural log)
+ * Head h reads KV head h / (H / H_kv) and routing head (h / (H / H_kv)) / (H_kv / R).
+ */
+int oracle_attn(int B, int N, int H, int H_kv, int R, int d, int w, double scale,
+                const uint16_t* q, const uint16_t* k, const uint16_t* v, const uint32_t* mask,
+                const int64_t* rows, int64_t n_rows, double* o, double* lse, int n_threads) {
+  if (B < 1 || N < 1 || H < 1 || H_kv < 1 || R < 1 || d < 1 || w < 1 || H % H_kv ||
+      H_kv % R || n_rows < 0)
+    return -1;
+  if (!rows) n_rows = (int64_t)B * N;
+  for (int64_t a = 0; rows && a < n_rows; ++a)
+    if (rows[a] < 0 || rows[a] >= (int64_t)B * N) return -1;
+  attn_job J = {B, N, H, H_kv, R, d, w, scale, q, k, v, mask, rows, n_rows, o, lse, 0};
+  pthread_mutex_init(&J.mu, NULL);
+  if (n_threads < 1) n_threads = 1;
+  if (n_threads > 256) n_threads = 256;
+  pthread_t th[256];
+  for (int t = 0; t < n_threads; ++t) pthread_create(&th[t], NULL, attn_worker, &J);
+  for (int t = 0; t < n_threads; ++t) pthread_join(th[t], NULL);
+  pthread_mutex_destroy(&J.mu);
+  return 0;
+}
