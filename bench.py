@@ -1,0 +1,373 @@
+#!/usr/bin/env python
+"""Benchmark of the Focus attention forward pass on GB300; prints ONE JSON line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl focus|reference]
+
+A step is one full forward pass (routing, bucketing, permuted copies, long-range
+and window attention with the union merge) over one synthetic batch whose inputs
+are already resident in HBM.  Timing: W untimed warm-up steps, then K steps
+between CUDA events on the launching stream, bracketed by barrier + synchronize,
+max over ranks.  Each rank processes its own independent problem (weak scaling,
+no collective on the data path).  The inputs (Q/K/V) are larger than L2, so no
+flush is needed between steps.
+
+--impl reference times the CPU oracle (the only comparison implementation: the
+pages ship no code) on the host cores, on a bounded sample of query rows.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "Focus attn fwd tokens/s and allowed-pair TFLOP/s vs GB300 BF16 peak"
+UNIT = "tokens/s"
+DEFAULT_WORKLOAD = "mha7b_32k"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_BYTES = 129 * 2**20
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(synth.WORKLOADS))
+    ap.add_argument("--impl", default="focus", choices=["focus", "reference"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0,
+                    help="target CPU time of the oracle sample")
+    return ap.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            d = json.load(open(path))
+            flat = {}
+            for k, v in d.items():
+                if isinstance(v, (int, float)):
+                    flat[k] = float(v)
+                elif isinstance(v, dict) and isinstance(v.get("value"), (int, float)):
+                    flat[k] = float(v["value"])
+            if "bf16_tflops" in flat:
+                for k, v in FALLBACK_PEAKS.items():
+                    flat.setdefault(k, v)
+                return flat, "measured"
+        except Exception:
+            pass
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ------------------------------------------------------------------ clocks --
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        sel = []
+        try:
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            sel = ["-i", uuid if uuid.startswith("GPU-") else "GPU-" + uuid]
+        except Exception:
+            pass
+        self.cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                    "-lms", "200"] + sel
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(self.cmd, stdout=self.out, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        self.out.flush()
+        rows = []
+        try:
+            for line in open(self.out.name):
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9 and parts[1].replace(".", "").isdigit():
+                    rows.append(parts)
+        except Exception:
+            pass
+        os.unlink(self.out.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sm = [float(r[1]) for r in rows]
+        reasons = sorted({n for r in rows for n, v in zip(self.NAMES, r[5:9]) if v == "Active"})
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": float(rows[0][2]),
+                "reasons": reasons, "samples": len(rows),
+                "power_w_median": statistics.median(float(r[3]) for r in rows
+                                                    if r[3].replace(".", "").isdigit())}
+
+
+# ------------------------------------------------------------- oracle legs --
+def uniform_rows(N: int, n: int, seed: int) -> np.ndarray:
+    g = np.random.default_rng(seed)
+    return np.sort(g.choice(N, size=min(n, N), replace=False)).astype(np.int64)
+
+
+def oracle_time_tokens(wl, inputs_cpu, target_s: float, seed: int = 11):
+    """Time the CPU oracle on a bounded sample: routing for all N tokens plus the
+    attention of a uniform sample of query rows (all heads).  Returns
+    (tokens/s, cores, sample description)."""
+    import oracle
+    cores = oracle.n_cores()
+    t0 = time.perf_counter()
+    mask, _, _, _ = oracle.route(inputs_cpu["r"], inputs_cpu["C"], K=wl.K, top_k=wl.top_k,
+                                 sinkhorn_iters=wl.sinkhorn_iters, sinkhorn_eps=wl.sinkhorn_eps)
+    t_route = time.perf_counter() - t0
+    q, k, v = inputs_cpu["q"], inputs_cpu["k"], inputs_cpu["v"]
+    cal = uniform_rows(wl.N, 8, seed)
+    t0 = time.perf_counter()
+    oracle.attn(q, k, v, mask, w=wl.w, rows=cal)
+    per_row = (time.perf_counter() - t0) / len(cal)
+    n = int(max(8, min(wl.N, (target_s - t_route) / max(per_row, 1e-9))))
+    rows = uniform_rows(wl.N, n, seed + 1)
+    t0 = time.perf_counter()
+    oracle.attn(q, k, v, mask, w=wl.w, rows=rows)
+    t_attn = time.perf_counter() - t0
+    sec_per_token = t_route / wl.N + t_attn / len(rows)
+    desc = (f"routing of all {wl.N} tokens ({t_route:.2f} s) + attention of {len(rows)} uniformly "
+            f"sampled query rows x {wl.H} heads ({t_attn:.2f} s); tokens/s = 1 / (route s/token + "
+            f"attention s/row), batch b=0")
+    return 1.0 / sec_per_token, cores, desc, t_route + t_attn
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    wl = synth.WORKLOADS[args.workload]
+    x = synth.make_inputs(wl, seed=args.seed, device="cpu")
+    import oracle
+    total = max(1, args.steps + args.warmup)
+    per_step = max(2.0, min(10.0, 150.0 / total))
+    vals = []
+    desc = cores = None
+    for i in range(args.warmup + args.steps):
+        v, cores, desc, _ = oracle_time_tokens(wl, x, per_step, seed=100 + i)
+        if i >= args.warmup:
+            vals.append(v)
+    value = statistics.mean(vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1000.0 * wl.B * wl.N / value, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_of(wl),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"each step: {desc}"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_of(wl):
+    return {"workload": wl.name, "B": wl.B, "N": wl.N, "H": wl.H, "H_kv": wl.H_kv,
+            "d_head": wl.d_head, "R": wl.R, "K": wl.K, "top_k": wl.top_k, "w": wl.w,
+            "sinkhorn_iters": wl.sinkhorn_iters, "softmax_scale": 1.0 / math.sqrt(wl.d_head)}
+
+
+def traffic_of(kernel_src: str):
+    """Per-launch DRAM bytes of the dominant kernel from a committed ncu summary, if it
+    was taken on the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", "attn_long_traffic.json")
+    if not os.path.exists(path):
+        return None
+    try:
+        d = json.load(open(path))
+        h = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()
+        if d.get("source_sha256") == h and d.get("workload") == DEFAULT_WORKLOAD:
+            return d.get("traffic_bytes_per_launch")
+    except Exception:
+        pass
+    return None
+
+
+# ---------------------------------------------------------------- GPU arm --
+def run_focus(args):
+    import learned_centroid_gated_gb300 as focus
+    from learned_centroid_gated_gb300 import pairs
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    wl = synth.WORKLOADS[args.workload]
+    p = focus.Params.from_workload(wl)
+    x = synth.make_inputs(wl, seed=args.seed + rank, device=dev)
+    ws = focus.Workspace(dev).get(p)
+    o = torch.empty_like(x["q"])
+    lse = torch.empty(p.B, p.H, p.N, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(evs=None):
+        focus.attn_fwd(p, x["q"], x["k"], x["v"], x["r"], x["C"], out=o, lse=lse, ws=ws,
+                       stream=stream, stage_events=evs)
+
+    W, K = max(args.warmup, 3), args.steps
+    for _ in range(W):
+        step()
+    torch.cuda.synchronize()
+    status = focus.get_status(ws)
+    if status != 0:
+        raise RuntimeError(f"device status {status}: {focus.strerror(status)}")
+
+    # exact allowed-pair accounting from the membership the kernels used
+    mask, _ = focus.route(p, x["r"], x["C"])
+    mask_np = mask.cpu().numpy().view(np.uint32)
+    cnt = pairs.allowed_pairs(mask_np, wl.w)  # [B, R]
+    heads_per_rho = wl.H // wl.R
+    allowed = int(cnt.sum()) * heads_per_rho
+    window = pairs.window_pairs(wl.N, wl.w) * wl.B * wl.H
+    longrange = allowed - window
+    flops = 4.0 * wl.d_head * allowed
+    flops_long = 4.0 * wl.d_head * longrange
+    causal = wl.B * wl.H * wl.N * (wl.N + 1) // 2
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(focus.N_STAGE_EVENTS)]
+           for _ in range(K)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        time.sleep(0.3)
+        for _ in range(W):
+            step()
+        barrier()
+        t_start.record(stream)
+        for i in range(K):
+            step(evs[i])
+        t_end.record(stream)
+        barrier()
+        time.sleep(0.1)
+    clocks = clk.summary()
+    ms = t_start.elapsed_time(t_end)
+    if dist is not None:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_step = ms / K
+    stage_ms = {}
+    for si, name in enumerate(focus.STAGES):
+        stage_ms[name] = statistics.mean(e[si].elapsed_time(e[si + 1]) for e in evs)
+
+    value = world * wl.B * wl.N / (ms_step / 1e3)
+    tflops = flops / (ms_step / 1e3) / 1e12
+
+    # end-to-end through the public host-buffer API (pinned host inputs)
+    host = {n: t.cpu().pin_memory() for n, t in x.items()}
+    sess = focus.HostSession(p, dev, stream)
+    for _ in range(2):
+        sess(host["q"], host["k"], host["v"], host["r"], host["C"])
+    barrier()
+    e0 = time.perf_counter()
+    ke = max(3, min(K, 10))
+    for _ in range(ke):
+        sess(host["q"], host["k"], host["v"], host["r"], host["C"])
+    barrier()
+    e_s = (time.perf_counter() - e0) / ke
+    if dist is not None:
+        t = torch.tensor([e_s], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e_s = float(t.item())
+    e2e = {"value": world * wl.B * wl.N / e_s, "unit": UNIT,
+           "h2d_bytes_per_step": sess.h2d_bytes(*host.values()),
+           "d2h_bytes_per_step": sess.d2h_bytes(), "ms_per_step": 1e3 * e_s}
+
+    peaks, peak_src = load_peaks()
+    t_long = stage_ms["attn_long"] / 1e3
+    achieved = flops_long / t_long / 1e12
+    roofline = {
+        "kernel": "attn_long (long-range block-sparse attention)",
+        "bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+        "frac": achieved / peaks["bf16_tflops"],
+        "peak_source": f"{peak_src} bf16 dense burst",
+        "peak_sustained": peaks["bf16_tflops_sustained"],
+        "frac_sustained": achieved / peaks["bf16_tflops_sustained"],
+        "traffic": traffic_of(os.path.join(ROOT, "learned_centroid_gated_gb300", "csrc", "attn.cu")),
+        "algorithmic_flops_per_launch": flops_long,
+        "launch_ms": stage_ms["attn_long"],
+    }
+    launches_per_step = (1 + 2 * wl.sinkhorn_iters) + 3 + 1 + 1 + 1 + 1
+    qkv_bytes = sum(x[n].numel() * x[n].element_size() for n in ("q", "k", "v"))
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
+        "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": dict(config_of(wl), l2=f"inputs larger than L2 (Q/K/V {qkv_bytes / 2**20:.0f} MiB "
+                                          f"> {L2_BYTES / 2**20:.0f} MiB), no flush",
+                       parallelism=f"independent problem per GPU x{world}"),
+        "allowed_pair_tflops": tflops,
+        "allowed_pair_frac_of_peak": tflops / peaks["bf16_tflops"],
+        "allowed_pairs": allowed, "allowed_fraction_of_causal": allowed / causal,
+        "stages_ms": stage_ms,
+        "roofline": roofline,
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * K,
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        xc = {n: t.cpu() for n, t in x.items()}
+        v, cores, desc, secs = oracle_time_tokens(wl, xc, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
+                                "sample": desc, "seconds": secs}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_focus(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,162 @@
+/*
+ * focus.h - C ABI of the Focus centroid-gated sparse attention forward pass
+ *           (libfocus.so, sm_103a).
+ *
+ * The method: "Why Attend to Everything? Focus is the Key" (Yao, Chen et al.).
+ *   - gist.science technical summary, section 2 "Core Architecture": K learnable
+ *     centroids C in R^{K x d_g}; tokens are projected into centroid space and
+ *     grouped; a local window of w tokens attends with exact softmax; distant
+ *     tokens attend only within a shared group.
+ *   - same section, "Inference Efficiency (Top-k)": at inference each token joins
+ *     its top-k highest-scoring groups and distant tokens interact only when they
+ *     share at least one group.
+ *   - same summary, "Key Technical Innovation: Sinkhorn Normalization": Sinkhorn
+ *     balancing of the token-to-group assignment.
+ *   - jindou-blog deep read, method bullets: routing dimension d_g = 16, scoring by
+ *     dot product, exact softmax inside the window and inside each group.
+ *
+ * What is computed, per batch b and query head h (readings where the pages are
+ * silent: logits scale * q.k with scale 1/sqrt(d) by default; window pairs are
+ * j <= i with i - j < w; long-range pairs are j <= i - w whose group bitmasks
+ * intersect; ONE softmax runs over the union, each key counted once):
+ *
+ *   A_i   = { j <= i : i - j < w } U { j <= i - w : mask_i & mask_j != 0 }
+ *   LSE_i = log sum_{j in A_i} exp(scale q_i.k_j)          (natural log)
+ *   O_i   = sum_{j in A_i} exp(scale q_i.k_j - LSE_i) v_j
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers on the current CUDA device, caller
+ *     owned, contiguous, row-major in the stated layout, 16-byte aligned (the
+ *     workspace 256-byte aligned). bf16 tensors are passed as uint16_t bit patterns.
+ *   - The library allocates no device memory and keeps no state between calls;
+ *     scratch lives in the caller's workspace (focus_workspace_size bytes).
+ *   - Work is enqueued asynchronously on `stream` (a cudaStream_t, NULL = legacy
+ *     default stream). Nothing is synchronised except by focus_get_status.
+ *   - Return value: FOCUS_OK (0) or a negative FOCUS_ERR_* code. Argument errors
+ *     are detected on the host before anything is launched. Nothing is thrown
+ *     across the ABI.
+ *
+ * Index conventions: B batch, N tokens, H query heads, H_kv key/value heads
+ * (H % H_kv == 0), R routing heads (R divides H_kv; R = 1 is one routing vector
+ * per token per layer, R = H_kv one per KV-head group), K groups (centroids),
+ * top_k groups per token, w window. Query head h reads KV head
+ * kvh = h / (H / H_kv) and routing head rho = kvh / (H_kv / R).
+ */
+#ifndef FOCUS_H_
+#define FOCUS_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define FOCUS_D_G 16            /* routing dimension */
+#define FOCUS_MAX_K 32          /* groups representable in a uint32 bitmask */
+#define FOCUS_MAX_SEGMENTS 1024 /* C(K, top_k) limit of the mask-value bucketing */
+
+enum focus_status {
+  FOCUS_OK = 0,
+  FOCUS_ERR_INVALID_ARG = -1, /* null pointer, bad size or inconsistent shape */
+  FOCUS_ERR_UNSUPPORTED = -2, /* valid but not implemented (d_head, C(K,top_k)) */
+  FOCUS_ERR_WORKSPACE = -3,   /* ws_bytes < focus_workspace_size() */
+  FOCUS_ERR_CUDA = -4,        /* a CUDA runtime call or launch failed */
+  FOCUS_ERR_TIMEOUT = -5,     /* a bounded device-side wait ran out */
+  FOCUS_ERR_BOUNDS = -6,      /* device-side index check failed (bad mask_in) */
+  FOCUS_ERR_ALIGNMENT = -7    /* a pointer is not suitably aligned */
+};
+
+typedef struct focus_params {
+  int32_t B, N, H, H_kv, d_head; /* d_head in {64, 128} */
+  int32_t R;                     /* routing heads, divides H_kv */
+  int32_t K, top_k;              /* 1 <= top_k <= K <= 32, C(K, top_k) <= 1024 */
+  int32_t w;                     /* window, >= 1 */
+  int32_t sinkhorn_iters;        /* 0 = plain top-k on the scores */
+  float sinkhorn_eps;            /* score temperature for Sinkhorn, > 0 (1.0 typical) */
+  float softmax_scale;           /* <= 0 selects 1 / sqrt(d_head) */
+} focus_params;
+
+/* Bytes of device workspace needed by focus_route, focus_bucket and
+ * focus_attn_fwd for these parameters; 0 if the parameters are invalid. */
+size_t focus_workspace_size(const focus_params* p);
+
+/*
+ * Group membership: scoring, optional Sinkhorn balancing, hard top-k.
+ *   r          [B, N, R, 16] fp32  routing vectors
+ *   C          [K, 16] fp32        centroids
+ *   mask_out   [B, R, N] uint32    bit g set iff group g is among the token's
+ *                                  top_k; ties go to the lower group index
+ *   margin_out [B, R, N] fp32 or NULL: kappa_(top_k) - kappa_(top_k+1)
+ *                                  (+inf when top_k == K)
+ * Score s_ig = r_i . c_g as a fused multiply-add chain over t = 0..15 in fp32.
+ * With sinkhorn_iters = T > 0 the log-domain iteration runs T times over all N
+ * tokens of each (b, routing head): column step beta_g = log(N/K) -
+ * LSE_i(s_ig/eps + alpha_i), then row step alpha_i = -LSE_g(s_ig/eps + beta_g);
+ * the ranking key is kappa_ig = s_ig/eps + beta_g. With T = 0, kappa = s.
+ */
+int focus_route(const focus_params* p, const float* r, const float* C, uint32_t* mask_out,
+                float* margin_out, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Bucketing of tokens by group bitmask (exposed for inspection and tests).
+ *   mask        [B, R, N] uint32, exactly top_k of the low K bits set per token
+ *   perm_out    [B, R, N] int32: token positions, stably sorted by the colex rank
+ *               of their mask's k-subset (so positions ascend inside a segment)
+ *   seg_off_out [B, R, C(K,top_k)+1] int32: segment start offsets into perm_out
+ * Either output may be NULL (the result then stays in the workspace only).
+ * A mask with the wrong number of bits sets FOCUS_ERR_BOUNDS in the status word.
+ */
+int focus_bucket(const focus_params* p, const uint32_t* mask, int32_t* perm_out,
+                 int32_t* seg_off_out, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Forward pass of Focus attention over the union set A_i defined above.
+ *   q        [B, N, H, d_head] bf16
+ *   k, v     [B, N, H_kv, d_head] bf16
+ *   r, C     routing inputs as in focus_route (may be NULL when mask_in is given)
+ *   mask_in  [B, R, N] uint32 or NULL: precomputed membership; NULL routes
+ *            internally (focus_route's result, kept in the workspace)
+ *   o        [B, N, H, d_head] bf16 out
+ *   lse      [B, H, N] fp32 out (natural log of the scaled logits), may be NULL
+ * Steps on `stream`: route (if mask_in is NULL), bucket, permuted copies of
+ * Q/K/V, long-range attention over compatible segments, window attention with
+ * the union merge.
+ */
+int focus_attn_fwd(const focus_params* p, const uint16_t* q, const uint16_t* k,
+                   const uint16_t* v, const float* r, const float* C, const uint32_t* mask_in,
+                   uint16_t* o, float* lse, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * focus_attn_fwd with stage timing: identical work and results, plus CUDA events
+ * recorded on `stream` at the stage boundaries, so a caller can time each stage
+ * without adding any synchronisation.
+ *   stage_events  array of FOCUS_N_STAGE_EVENTS cudaEvent_t handles (cast to
+ *                 void*) created by the caller, or NULL (then this is exactly
+ *                 focus_attn_fwd). Recorded in order: [0] start, [1] after routing,
+ *                 [2] after bucketing and the long-range schedule, [3] after the
+ *                 permuted Q/K/V copies, [4] after long-range attention, [5] after
+ *                 window attention and the union merge.
+ */
+#define FOCUS_N_STAGE_EVENTS 6
+int focus_attn_fwd_ev(const focus_params* p, const uint16_t* q, const uint16_t* k,
+                      const uint16_t* v, const float* r, const float* C,
+                      const uint32_t* mask_in, uint16_t* o, float* lse, void* ws,
+                      size_t ws_bytes, void* stream, void* const* stage_events);
+
+/* Synchronises `stream` and returns the device status word of the last call
+ * that used this workspace (FOCUS_OK, FOCUS_ERR_TIMEOUT, FOCUS_ERR_BOUNDS), or
+ * FOCUS_ERR_CUDA if the synchronisation itself failed. */
+int focus_get_status(const void* ws, void* stream);
+
+/* Static, human-readable text for a status code. */
+const char* focus_strerror(int code);
+
+/* ABI version, (major << 16) | minor. */
+int focus_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FOCUS_H_ */

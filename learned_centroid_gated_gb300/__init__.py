@@ -1,0 +1,273 @@
+"""Focus centroid-gated sparse attention, forward pass, for GB300 (sm_103a).
+
+Thin ctypes binding over the C ABI in ``include/focus.h`` (``libfocus.so``, built
+in-tree by ``learned_centroid_gated_gb300.build``). This module only marshals
+arguments: every step of the computation runs in the library's CUDA kernels.
+PyTorch supplies device memory and streams. There is no CPU fallback: importing
+this package fails if the library is missing.
+
+Method: "Why Attend to Everything? Focus is the Key" -- gist.science technical
+summary, section 2 "Core Architecture" and "Inference Efficiency (Top-k)".
+"""
+from __future__ import annotations
+
+import ctypes
+import dataclasses
+import math
+import os
+import re
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libfocus.so")
+HEADER = os.path.join(os.path.dirname(_HERE), "include", "focus.h")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"Focus CUDA library not built ({LIB_PATH} missing); run "
+        "`python learned_centroid_gated_gb300/build.py` on a machine with nvcc")
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+FOCUS_OK = 0
+ERRORS = {
+    -1: "FOCUS_ERR_INVALID_ARG", -2: "FOCUS_ERR_UNSUPPORTED", -3: "FOCUS_ERR_WORKSPACE",
+    -4: "FOCUS_ERR_CUDA", -5: "FOCUS_ERR_TIMEOUT", -6: "FOCUS_ERR_BOUNDS", -7: "FOCUS_ERR_ALIGNMENT",
+}
+
+
+class FocusError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__(f"{what}: {ERRORS.get(code, code)} ({strerror(code)})")
+
+
+class _Params(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in
+                ("B", "N", "H", "H_kv", "d_head", "R", "K", "top_k", "w", "sinkhorn_iters")] + \
+               [("sinkhorn_eps", ctypes.c_float), ("softmax_scale", ctypes.c_float)]
+
+
+@dataclasses.dataclass(frozen=True)
+class Params:
+    """Problem description (focus_params).  softmax_scale <= 0 selects 1/sqrt(d_head)."""
+    B: int
+    N: int
+    H: int
+    H_kv: int
+    d_head: int
+    R: int
+    K: int
+    top_k: int
+    w: int
+    sinkhorn_iters: int = 0
+    sinkhorn_eps: float = 1.0
+    softmax_scale: float = 0.0
+
+    @classmethod
+    def from_workload(cls, wl, **kw) -> "Params":
+        return cls(B=wl.B, N=wl.N, H=wl.H, H_kv=wl.H_kv, d_head=wl.d_head, R=wl.R, K=wl.K,
+                   top_k=wl.top_k, w=wl.w, sinkhorn_iters=wl.sinkhorn_iters,
+                   sinkhorn_eps=wl.sinkhorn_eps, **kw)
+
+    def c(self) -> _Params:
+        return _Params(*[getattr(self, f.name) for f in dataclasses.fields(self)])
+
+    @property
+    def nseg(self) -> int:
+        return math.comb(self.K, self.top_k)
+
+    @property
+    def scale(self) -> float:
+        return self.softmax_scale if self.softmax_scale > 0 else 1.0 / math.sqrt(self.d_head)
+
+
+_P = ctypes.c_void_p
+_PP = ctypes.POINTER(_Params)
+_lib.focus_workspace_size.argtypes = [_PP]
+_lib.focus_workspace_size.restype = ctypes.c_size_t
+_lib.focus_route.argtypes = [_PP, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]
+_lib.focus_route.restype = ctypes.c_int
+_lib.focus_bucket.argtypes = [_PP, _P, _P, _P, _P, ctypes.c_size_t, _P]
+_lib.focus_bucket.restype = ctypes.c_int
+_lib.focus_attn_fwd.argtypes = [_PP, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]
+_lib.focus_attn_fwd.restype = ctypes.c_int
+_lib.focus_attn_fwd_ev.argtypes = [_PP, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P,
+                                   ctypes.POINTER(ctypes.c_void_p)]
+_lib.focus_attn_fwd_ev.restype = ctypes.c_int
+N_STAGE_EVENTS = 6
+STAGES = ("route", "bucket", "permute", "attn_long", "attn_window")
+_lib.focus_get_status.argtypes = [_P, _P]
+_lib.focus_get_status.restype = ctypes.c_int
+_lib.focus_strerror.argtypes = [ctypes.c_int]
+_lib.focus_strerror.restype = ctypes.c_char_p
+_lib.focus_version.argtypes = []
+_lib.focus_version.restype = ctypes.c_int
+
+
+def declared_symbols() -> list[str]:
+    """Function names declared in include/focus.h."""
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:[\w\s\*]+?)\b(focus_\w+)\s*\(", text, re.M)))
+
+
+def strerror(code: int) -> str:
+    return _lib.focus_strerror(code).decode()
+
+
+def version() -> int:
+    return _lib.focus_version()
+
+
+def workspace_size(p: Params) -> int:
+    return int(_lib.focus_workspace_size(ctypes.byref(p.c())))
+
+
+def _ptr(t: torch.Tensor | None):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(rc: int, what: str):
+    if rc != FOCUS_OK:
+        raise FocusError(rc, what)
+
+
+class Workspace:
+    """Caller-owned device workspace (a torch uint8 buffer), grown on demand."""
+
+    def __init__(self, device=None):
+        self.device = torch.device(device or "cuda")
+        self.buf: torch.Tensor | None = None
+
+    def get(self, p: Params) -> torch.Tensor:
+        need = workspace_size(p)
+        if need == 0:
+            raise FocusError(-1, "focus_workspace_size")
+        if self.buf is None or self.buf.numel() < need:
+            self.buf = torch.empty(need, dtype=torch.uint8, device=self.device)
+        return self.buf
+
+
+_default_ws: dict = {}
+
+
+def _ws(p: Params, ws, device) -> torch.Tensor:
+    if isinstance(ws, torch.Tensor):
+        return ws
+    if ws is None:
+        ws = _default_ws.setdefault(str(device), Workspace(device))
+    return ws.get(p)
+
+
+def _bf16_bits(t: torch.Tensor) -> torch.Tensor:
+    assert t.dtype == torch.bfloat16 and t.is_cuda and t.is_contiguous()
+    return t
+
+
+def route(p: Params, r: torch.Tensor, C: torch.Tensor, *, margin: bool = False, ws=None,
+          stream=None):
+    """Group bitmasks [B, R, N] uint32 (as int32 tensor) and optional fp32 margins."""
+    assert r.dtype == torch.float32 and C.dtype == torch.float32 and r.is_cuda and C.is_cuda
+    mask = torch.empty(p.B, p.R, p.N, dtype=torch.int32, device=r.device)
+    marg = torch.empty(p.B, p.R, p.N, dtype=torch.float32, device=r.device) if margin else None
+    w = _ws(p, ws, r.device)
+    _check(_lib.focus_route(ctypes.byref(p.c()), _ptr(r.contiguous()), _ptr(C.contiguous()),
+                            _ptr(mask), _ptr(marg), _ptr(w), w.numel(), _stream(stream)),
+           "focus_route")
+    return mask, marg
+
+
+def bucket(p: Params, mask: torch.Tensor, *, ws=None, stream=None):
+    """Stable mask-value bucketing: perm [B, R, N] int32 and seg_off [B, R, nseg+1] int32."""
+    perm = torch.empty(p.B, p.R, p.N, dtype=torch.int32, device=mask.device)
+    seg = torch.empty(p.B, p.R, p.nseg + 1, dtype=torch.int32, device=mask.device)
+    w = _ws(p, ws, mask.device)
+    _check(_lib.focus_bucket(ctypes.byref(p.c()), _ptr(mask.contiguous()), _ptr(perm), _ptr(seg),
+                             _ptr(w), w.numel(), _stream(stream)), "focus_bucket")
+    return perm, seg
+
+
+def attn_fwd(p: Params, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, r=None, C=None,
+             mask=None, *, out=None, lse=None, want_lse: bool = True, ws=None, stream=None,
+             stage_events=None):
+    """Focus attention forward on device tensors. Returns (o bf16 [B,N,H,d], lse fp32 [B,H,N]).
+
+    stage_events: optional list of N_STAGE_EVENTS torch.cuda.Event(enable_timing=True),
+    recorded at the stage boundaries (see focus_attn_fwd_ev)."""
+    for t in (q, k, v):
+        _bf16_bits(t)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty(p.B, p.H, p.N, dtype=torch.float32, device=q.device)
+    w = _ws(p, ws, q.device)
+    args = (ctypes.byref(p.c()), _ptr(q), _ptr(k), _ptr(v), _ptr(r), _ptr(C), _ptr(mask), _ptr(out),
+            _ptr(lse), _ptr(w), w.numel(), _stream(stream))
+    if stage_events is None:
+        _check(_lib.focus_attn_fwd(*args), "focus_attn_fwd")
+    else:
+        assert len(stage_events) == N_STAGE_EVENTS
+        evs = (ctypes.c_void_p * N_STAGE_EVENTS)(*[e.cuda_event for e in stage_events])
+        _check(_lib.focus_attn_fwd_ev(*args, evs), "focus_attn_fwd_ev")
+    return out, lse
+
+
+class HostSession:
+    """End-to-end calls on HOST tensors: each call copies the inputs (pinned host
+    memory recommended) to reusable device buffers, runs the forward pass and copies
+    O and LSE back into reusable pinned host tensors, then synchronises.  The
+    returned host tensors are overwritten by the next call."""
+
+    def __init__(self, p: Params, device="cuda", stream=None):
+        self.p = p
+        self.device = torch.device(device)
+        self.stream = stream
+        self.ws = Workspace(self.device)
+        self._dev: dict = {}
+        self.o_host = torch.empty(p.B, p.N, p.H, p.d_head, dtype=torch.bfloat16, pin_memory=True)
+        self.lse_host = torch.empty(p.B, p.H, p.N, dtype=torch.float32, pin_memory=True)
+        self._o = torch.empty(self.o_host.shape, dtype=torch.bfloat16, device=self.device)
+        self._lse = torch.empty(self.lse_host.shape, dtype=torch.float32, device=self.device)
+
+    def _stage(self, name: str, t: torch.Tensor) -> torch.Tensor:
+        d = self._dev.get(name)
+        if d is None or d.shape != t.shape or d.dtype != t.dtype:
+            d = torch.empty(t.shape, dtype=t.dtype, device=self.device)
+            self._dev[name] = d
+        d.copy_(t, non_blocking=True)
+        return d
+
+    def h2d_bytes(self, *tensors) -> int:
+        return sum(t.numel() * t.element_size() for t in tensors)
+
+    def d2h_bytes(self) -> int:
+        return self.o_host.numel() * 2 + self.lse_host.numel() * 4
+
+    def __call__(self, q, k, v, r, C, stage_events=None):
+        dev = [self._stage(n, t) for n, t in zip("qkvrC", (q, k, v, r, C))]
+        attn_fwd(self.p, *dev, out=self._o, lse=self._lse, ws=self.ws, stream=self.stream,
+                 stage_events=stage_events)
+        self.o_host.copy_(self._o, non_blocking=True)
+        self.lse_host.copy_(self._lse, non_blocking=True)
+        (self.stream or torch.cuda.current_stream()).synchronize()
+        return self.o_host, self.lse_host
+
+
+def attn_fwd_host(p: Params, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, r: torch.Tensor,
+                  C: torch.Tensor, *, device="cuda", stream=None):
+    """One end-to-end call on HOST tensors (see HostSession for repeated calls).
+    Returns host (o, lse)."""
+    o, lse = HostSession(p, device, stream)(q, k, v, r, C)
+    return o.clone(), lse.clone()
+
+
+def get_status(ws: torch.Tensor, stream=None) -> int:
+    """Synchronise and read the device status word of the last call on `ws`."""
+    return _lib.focus_get_status(_ptr(ws), _stream(stream))

@@ -1,0 +1,319 @@
+// Bucketing of tokens by group bitmask, the long-range query-block schedule, and
+// the permuted Q/K/V copies.
+//
+// Distant tokens attend only when their groups intersect ("Why Attend to
+// Everything? Focus is the Key", gist.science technical summary, section 2,
+// "Inference Efficiency (Top-k)"). Tokens are sorted stably by their mask
+// VALUE (the exact k-subset of groups, ranked in colex order), so every segment
+// holds tokens with one mask and ascending positions. A query segment S then
+// attends to whole key segments T with mask(S) & mask(T) != 0: every key appears
+// once in a query's candidate list, so the union softmax needs no deduplication,
+// and the tiles inside a segment are dense.
+#include "common.cuh"
+
+namespace focus {
+namespace {
+
+// Colex rank of a k-subset given as a bitmask: sum_m C(c_m, m + 1) over the set
+// bits c_0 < c_1 < ...  Returns -1 unless exactly top_k of the low K bits are set.
+__device__ __forceinline__ int seg_of(uint32_t m, int K, int top_k) {
+  if (K < 32 && (m >> K) != 0u) return -1;
+  if (__popc(m) != top_k) return -1;
+  int rank = 0, idx = 0;
+  while (m) {
+    const int c = __ffs(m) - 1;
+    m &= m - 1;
+    ++idx;
+    rank += (int)binom(c, idx);
+  }
+  return rank;
+}
+
+__device__ __forceinline__ unsigned lanemask_lt() {
+  unsigned r;
+  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(r));
+  return r;
+}
+
+// Histogram of segment ids over one chunk of kChunk tokens. One warp per chunk,
+// grid = (nchunk, B*R).  Invalid masks raise FOCUS_ERR_BOUNDS and count in segment 0.
+__global__ void __launch_bounds__(32)
+bucket_hist(int N, int K, int top_k, int nseg, const uint32_t* __restrict__ mask,
+            int* __restrict__ hist, int* status) {
+  extern __shared__ int cnt[];
+  const int br = blockIdx.y, chunk = blockIdx.x, lane = threadIdx.x;
+  for (int s = lane; s < nseg; s += 32) cnt[s] = 0;
+  __syncwarp();
+  const uint32_t* m = mask + (int64_t)br * N;
+  const int n0 = chunk * kChunk;
+  for (int it = 0; it < kChunk / 32; ++it) {
+    const int n = n0 + it * 32 + lane;
+    int sg = -2;
+    if (n < N) {
+      sg = seg_of(m[n], K, top_k);
+      if (sg < 0) {
+        raise_status(status, FOCUS_ERR_BOUNDS);
+        sg = 0;
+      }
+    }
+    const unsigned peers = __match_any_sync(0xffffffffu, sg);
+    if (sg >= 0 && (peers & lanemask_lt()) == 0u) cnt[sg] += __popc(peers);
+    __syncwarp();
+  }
+  int* h = hist + ((int64_t)br * gridDim.x + chunk) * nseg;
+  for (int s = lane; s < nseg; s += 32) h[s] = cnt[s];
+}
+
+// Segment offsets and per-chunk scatter bases. grid = B*R, 1024 threads (>= nseg).
+__global__ void __launch_bounds__(1024)
+bucket_scan(int nseg, int nchunk, const int* __restrict__ hist, int* __restrict__ seg_off,
+            int* __restrict__ cbase) {
+  __shared__ int wsum[32];
+  const int br = blockIdx.x, s = threadIdx.x;
+  const int* h = hist + (int64_t)br * nchunk * nseg;
+  int t = 0;
+  if (s < nseg)
+    for (int c = 0; c < nchunk; ++c) t += h[(int64_t)c * nseg + s];
+  // exclusive block scan of t over s
+  const int lane = s & 31, wid = s >> 5;
+  int x = t;
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) wsum[wid] = x;
+  __syncthreads();
+  if (wid == 0) {
+    int v = wsum[lane];
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, v, o);
+      if (lane >= o) v += y;
+    }
+    wsum[lane] = v;
+  }
+  __syncthreads();
+  const int excl = x - t + (wid > 0 ? wsum[wid - 1] : 0);
+  if (s < nseg) {
+    seg_off[(int64_t)br * (nseg + 1) + s] = excl;
+    if (s == nseg - 1) seg_off[(int64_t)br * (nseg + 1) + nseg] = excl + t;
+    int run = excl;
+    int* cb = cbase + (int64_t)br * nchunk * nseg;
+    for (int c = 0; c < nchunk; ++c) {
+      cb[(int64_t)c * nseg + s] = run;
+      run += h[(int64_t)c * nseg + s];
+    }
+  }
+}
+
+// Stable scatter: perm[seg_base + rank] = n. Same chunking as bucket_hist.
+__global__ void __launch_bounds__(32)
+bucket_scatter(int N, int K, int top_k, int nseg, const uint32_t* __restrict__ mask,
+               const int* __restrict__ cbase, int* __restrict__ perm) {
+  extern __shared__ int cur[];
+  const int br = blockIdx.y, chunk = blockIdx.x, lane = threadIdx.x;
+  const int* cb = cbase + ((int64_t)br * gridDim.x + chunk) * nseg;
+  for (int s = lane; s < nseg; s += 32) cur[s] = cb[s];
+  __syncwarp();
+  const uint32_t* m = mask + (int64_t)br * N;
+  int* P = perm + (int64_t)br * N;
+  const int n0 = chunk * kChunk;
+  for (int it = 0; it < kChunk / 32; ++it) {
+    const int n = n0 + it * 32 + lane;
+    int sg = -2;
+    if (n < N) {
+      sg = seg_of(m[n], K, top_k);
+      if (sg < 0) sg = 0;
+    }
+    const unsigned peers = __match_any_sync(0xffffffffu, sg);
+    if (sg >= 0) {
+      const int dst = cur[sg] + __popc(peers & lanemask_lt());
+      P[dst] = n;
+    }
+    __syncwarp();
+    if (sg >= 0 && (peers & lanemask_lt()) == 0u) cur[sg] += __popc(peers);
+    __syncwarp();
+  }
+}
+
+// Long-range schedule: one entry per query block of kAttnBM rows inside a segment,
+// ordered by descending position of the block's last row (the blocks with the most
+// candidate keys start first).  Single CTA.
+constexpr int kTabThreads = 1024;
+constexpr int kTabBuckets = 4096;
+
+__global__ void __launch_bounds__(kTabThreads)
+build_qtab(int N, int nseg, int BR, const int* __restrict__ seg_off, const int* __restrict__ perm,
+           int* __restrict__ entoff, QBlock* __restrict__ qtab, int* __restrict__ qtab_count) {
+  __shared__ int bucket[kTabBuckets];
+  __shared__ int wsum[32];
+  __shared__ int carry;
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int nitems = BR * nseg;
+  // exclusive scan of block counts over (br, seg)
+  if (tid == 0) carry = 0;
+  __syncthreads();
+  for (int base = 0; base < nitems; base += kTabThreads) {
+    const int it = base + tid;
+    int c = 0;
+    if (it < nitems) {
+      const int br = it / nseg, s = it % nseg;
+      const int* so = seg_off + (int64_t)br * (nseg + 1);
+      const int cnt = so[s + 1] - so[s];
+      c = (cnt + kAttnBM - 1) / kAttnBM;
+    }
+    int x = c;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) wsum[wid] = x;
+    __syncthreads();
+    if (wid == 0) {
+      int v = wsum[lane];
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += y;
+      }
+      wsum[lane] = v;
+    }
+    __syncthreads();
+    const int excl = carry + x - c + (wid > 0 ? wsum[wid - 1] : 0);
+    if (it < nitems) entoff[it] = excl;
+    __syncthreads();
+    if (tid == kTabThreads - 1) carry = excl + c;
+    __syncthreads();
+  }
+  const int E = carry;
+  if (tid == 0) {
+    entoff[nitems] = E;
+    *qtab_count = E;
+  }
+  int shift = 0;
+  while (((N - 1) >> shift) >= kTabBuckets) ++shift;
+  for (int i = tid; i < kTabBuckets; i += kTabThreads) bucket[i] = 0;
+  __syncthreads();
+  // pass 1: histogram of sort keys; pass 2: scatter
+  for (int pass = 0; pass < 2; ++pass) {
+    for (int e = tid; e < E; e += kTabThreads) {
+      int lo = 0, hi = nitems - 1;  // last item with entoff <= e
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (entoff[mid] <= e) lo = mid; else hi = mid - 1;
+      }
+      const int br = lo / nseg, s = lo % nseg;
+      const int t = e - entoff[lo];
+      const int* so = seg_off + (int64_t)br * (nseg + 1);
+      const int cnt = so[s + 1] - so[s];
+      const int row0 = so[s] + t * kAttnBM;
+      const int rows = min(kAttnBM, cnt - t * kAttnBM);
+      const int last = perm[(int64_t)br * N + row0 + rows - 1];
+      const int key = (N - 1 - last) >> shift;
+      if (pass == 0) {
+        atomicAdd(&bucket[key], 1);
+      } else {
+        const int dst = atomicAdd(&bucket[key], 1);
+        qtab[dst] = QBlock{br, s, row0, rows};
+      }
+    }
+    __syncthreads();
+    if (pass == 0) {  // exclusive scan of the buckets, in place (single thread chunks)
+      constexpr int per = kTabBuckets / kTabThreads;
+      int loc[per], sum = 0;
+      for (int j = 0; j < per; ++j) {
+        loc[j] = bucket[tid * per + j];
+        sum += loc[j];
+      }
+      int x = sum;
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      if (lane == 31) wsum[wid] = x;
+      __syncthreads();
+      if (wid == 0) {
+        int v = wsum[lane];
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, v, o);
+          if (lane >= o) v += y;
+        }
+        wsum[lane] = v;
+      }
+      __syncthreads();
+      int run = x - sum + (wid > 0 ? wsum[wid - 1] : 0);
+      for (int j = 0; j < per; ++j) {
+        bucket[tid * per + j] = run;
+        run += loc[j];
+      }
+      __syncthreads();
+    }
+  }
+}
+
+// Permuted, head-major copies: Qp[b][h][n'][:] = q[b][perm[n']][h][:] for the heads
+// of routing head rho, and likewise K/V for its KV heads.  One CTA per permuted row.
+__global__ void __launch_bounds__(256)
+permute_qkv(int N, int H, int H_kv, int R, int d, const int* __restrict__ perm,
+            const uint4* __restrict__ q, const uint4* __restrict__ k, const uint4* __restrict__ v,
+            uint4* __restrict__ qp, uint4* __restrict__ kp, uint4* __restrict__ vp) {
+  const int64_t row = blockIdx.x;  // (b * R + rho) * N + n'
+  const int br = (int)(row / N), np = (int)(row % N);
+  const int b = br / R, rho = br % R;
+  const int n = perm[row];
+  const int hq = H / R, hkv = H_kv / R;
+  const int vec = d / 8;  // uint4 per head row
+  const int nq = hq * vec, nk = hkv * vec;
+  for (int i = threadIdx.x; i < nq + 2 * nk; i += blockDim.x) {
+    if (i < nq) {
+      const int hh = rho * hq + i / vec, c = i % vec;
+      qp[(((int64_t)b * H + hh) * N + np) * vec + c] = q[(((int64_t)b * N + n) * H + hh) * vec + c];
+    } else {
+      const int j = (i - nq) % nk;
+      const int hh = rho * hkv + j / vec, c = j % vec;
+      const int64_t src = (((int64_t)b * N + n) * H_kv + hh) * vec + c;
+      const int64_t dst = (((int64_t)b * H_kv + hh) * N + np) * vec + c;
+      if (i < nq + nk) kp[dst] = k[src]; else vp[dst] = v[src];
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_bucket(const focus_params& p, const WsLayout& L, const uint32_t* mask, char* ws,
+                          cudaStream_t s) {
+  const int BR = p.B * p.R;
+  int* status = &reinterpret_cast<WsHeader*>(ws)->status;
+  int* hist = reinterpret_cast<int*>(ws + L.hist);
+  int* segoff = reinterpret_cast<int*>(ws + L.segoff);
+  int* cbase = reinterpret_cast<int*>(ws + L.cbase);
+  int* perm = reinterpret_cast<int*>(ws + L.perm);
+  const size_t shm = sizeof(int) * L.nseg;
+  dim3 grid(L.nchunk, BR);
+  bucket_hist<<<grid, 32, shm, s>>>(p.N, p.K, p.top_k, L.nseg, mask, hist, status);
+  bucket_scan<<<BR, 1024, 0, s>>>(L.nseg, L.nchunk, hist, segoff, cbase);
+  bucket_scatter<<<grid, 32, shm, s>>>(p.N, p.K, p.top_k, L.nseg, mask, cbase, perm);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_qtab(const focus_params& p, const WsLayout& L, const uint32_t* mask, char* ws,
+                        cudaStream_t s) {
+  (void)mask;
+  WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
+  build_qtab<<<1, kTabThreads, 0, s>>>(p.N, L.nseg, p.B * p.R, reinterpret_cast<int*>(ws + L.segoff),
+                                       reinterpret_cast<int*>(ws + L.perm),
+                                       reinterpret_cast<int*>(ws + L.entoff),
+                                       reinterpret_cast<QBlock*>(ws + L.qtab), &hdr->qtab_count);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_permute(const focus_params& p, const WsLayout& L, const bf16* q, const bf16* k,
+                           const bf16* v, char* ws, cudaStream_t s) {
+  const int64_t rows = (int64_t)p.B * p.R * p.N;
+  permute_qkv<<<(unsigned)rows, 256, 0, s>>>(
+      p.N, p.H, p.H_kv, p.R, p.d_head, reinterpret_cast<const int*>(ws + L.perm),
+      reinterpret_cast<const uint4*>(q), reinterpret_cast<const uint4*>(k),
+      reinterpret_cast<const uint4*>(v), reinterpret_cast<uint4*>(ws + L.qp),
+      reinterpret_cast<uint4*>(ws + L.kp), reinterpret_cast<uint4*>(ws + L.vp));
+  return cudaGetLastError();
+}
+
+}  // namespace focus

@@ -1,0 +1,72 @@
+// Shared device/host definitions of the Focus CUDA library (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/focus.h"
+
+namespace focus {
+
+using bf16 = __nv_bfloat16;
+
+// ---------------------------------------------------------------- workspace --
+// Header at the start of the workspace: device status word and counters.
+struct WsHeader {
+  int status;       // first error code raised by a kernel, 0 if none
+  int qtab_count;   // number of query blocks in the long-range schedule
+  int pad[62];
+};
+static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
+
+// Query-block entry of the long-range schedule: routing problem (b * R + rho),
+// segment, first permuted row, number of rows.
+struct QBlock {
+  int br, seg, row0, rows;
+};
+
+constexpr int kChunk = 1024;      // tokens per bucketing chunk (one warp)
+constexpr int kSinkBlock = 256;   // tokens per Sinkhorn partial-reduction block
+constexpr int kAttnBM = 128;      // query rows per attention CTA
+constexpr int kKeySentinel = 0x7fffffff;
+
+struct WsLayout {
+  size_t hdr, mask, beta, skpart, hist, segoff, cbase, perm, entoff, qtab, qp, kp, vp, olr, lselr;
+  size_t total;
+  int nseg, nchunk, nblk_sk, qtab_cap;
+};
+
+// Binomial coefficient C(n, r) for n <= 32 (fits uint32 for all r).
+__host__ __device__ inline uint32_t binom(int n, int r) {
+  if (r < 0 || r > n) return 0;
+  if (r > n - r) r = n - r;
+  uint64_t c = 1;
+  for (int i = 1; i <= r; ++i) c = c * (uint64_t)(n - r + i) / (uint64_t)i;
+  return (uint32_t)c;
+}
+
+// Raise a device status code (the first one raised wins).
+__device__ inline void raise_status(int* status, int code) { atomicCAS(status, 0, code); }
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// ------------------------------------------------------------ kernel launchers --
+// route.cu
+cudaError_t launch_route(const focus_params& p, const WsLayout& L, const float* r, const float* C,
+                         char* ws, uint32_t* mask_out, float* margin_out, cudaStream_t s);
+// bucket.cu
+cudaError_t launch_bucket(const focus_params& p, const WsLayout& L, const uint32_t* mask, char* ws,
+                          cudaStream_t s);
+cudaError_t launch_qtab(const focus_params& p, const WsLayout& L, const uint32_t* mask, char* ws,
+                        cudaStream_t s);
+cudaError_t launch_permute(const focus_params& p, const WsLayout& L, const bf16* q, const bf16* k,
+                           const bf16* v, char* ws, cudaStream_t s);
+// attn.cu
+cudaError_t launch_attn_long(const focus_params& p, const WsLayout& L, const uint32_t* mask,
+                             char* ws, float scale, cudaStream_t s);
+cudaError_t launch_attn_window(const focus_params& p, const WsLayout& L, const bf16* q,
+                               const bf16* k, const bf16* v, char* ws, bf16* o, float* lse,
+                               float scale, cudaStream_t s);
+
+}  // namespace focus

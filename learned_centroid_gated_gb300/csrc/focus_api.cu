@@ -1,0 +1,207 @@
+// C ABI of the Focus attention library: argument validation, workspace layout
+// and the launch sequence on the caller's stream.  See include/focus.h.
+#include <math.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace focus {
+namespace {
+
+bool aligned(const void* ptr, size_t a) { return ((uintptr_t)ptr % a) == 0; }
+
+// Shape checks shared by every entry point (host only, nothing launched).
+int check_params(const focus_params* p) {
+  if (!p) return FOCUS_ERR_INVALID_ARG;
+  if (p->B < 1 || p->N < 1 || p->H < 1 || p->H_kv < 1 || p->R < 1 || p->K < 1 || p->top_k < 1 ||
+      p->w < 1 || p->sinkhorn_iters < 0)
+    return FOCUS_ERR_INVALID_ARG;
+  if (p->H % p->H_kv != 0 || p->H_kv % p->R != 0) return FOCUS_ERR_INVALID_ARG;
+  if (p->K > FOCUS_MAX_K || p->top_k > p->K) return FOCUS_ERR_INVALID_ARG;
+  if (p->sinkhorn_iters > 0 && !(p->sinkhorn_eps > 0.0f)) return FOCUS_ERR_INVALID_ARG;
+  if (p->d_head != 64 && p->d_head != 128) return FOCUS_ERR_UNSUPPORTED;
+  if (binom(p->K, p->top_k) > (uint32_t)FOCUS_MAX_SEGMENTS) return FOCUS_ERR_UNSUPPORTED;
+  // 32-bit row indices: B * max(H, R) * N rows must fit in int32
+  const int64_t rows = (int64_t)p->B * (p->H > p->R ? p->H : p->R) * p->N;
+  if (rows >= (int64_t)INT32_MAX) return FOCUS_ERR_UNSUPPORTED;
+  return FOCUS_OK;
+}
+
+WsLayout layout(const focus_params& p) {
+  WsLayout L{};
+  const int BR = p.B * p.R;
+  L.nseg = (int)binom(p.K, p.top_k);
+  L.nchunk = (p.N + kChunk - 1) / kChunk;
+  L.nblk_sk = (p.N + 255) / 256;
+  L.qtab_cap = BR * ((p.N + kAttnBM - 1) / kAttnBM + L.nseg);
+  const size_t A = 256;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off = align_up(off + bytes, A);
+    return at;
+  };
+  L.hdr = take(sizeof(WsHeader));
+  L.mask = take(sizeof(uint32_t) * (size_t)BR * p.N);
+  L.beta = take(sizeof(float) * (size_t)BR * p.K);
+  L.skpart = take(sizeof(float2) * (size_t)BR * L.nblk_sk * p.K);
+  L.hist = take(sizeof(int) * (size_t)BR * L.nchunk * L.nseg);
+  L.segoff = take(sizeof(int) * (size_t)BR * (L.nseg + 1));
+  L.cbase = take(sizeof(int) * (size_t)BR * L.nchunk * L.nseg);
+  L.perm = take(sizeof(int) * (size_t)BR * p.N);
+  L.entoff = take(sizeof(int) * ((size_t)BR * L.nseg + 1));
+  L.qtab = take(sizeof(QBlock) * (size_t)L.qtab_cap);
+  L.qp = take(sizeof(uint16_t) * (size_t)p.B * p.H * p.N * p.d_head);
+  L.kp = take(sizeof(uint16_t) * (size_t)p.B * p.H_kv * p.N * p.d_head);
+  L.vp = take(sizeof(uint16_t) * (size_t)p.B * p.H_kv * p.N * p.d_head);
+  L.olr = take(sizeof(float) * (size_t)p.B * p.N * p.H * p.d_head);
+  L.lselr = take(sizeof(float) * (size_t)p.B * p.H * p.N);
+  L.total = off;
+  return L;
+}
+
+int check_ws(const WsLayout& L, const void* ws, size_t ws_bytes) {
+  if (!ws) return FOCUS_ERR_INVALID_ARG;
+  if (!aligned(ws, 256)) return FOCUS_ERR_ALIGNMENT;
+  if (ws_bytes < L.total) return FOCUS_ERR_WORKSPACE;
+  return FOCUS_OK;
+}
+
+int cuda_rc(cudaError_t e) { return e == cudaSuccess ? FOCUS_OK : FOCUS_ERR_CUDA; }
+
+// Clears the status word and the schedule counter at the start of a call.
+cudaError_t reset_header(char* ws, cudaStream_t s) {
+  return cudaMemsetAsync(ws, 0, sizeof(WsHeader), s);
+}
+
+}  // namespace
+}  // namespace focus
+
+using namespace focus;
+
+extern "C" {
+
+size_t focus_workspace_size(const focus_params* p) {
+  if (check_params(p) != FOCUS_OK) return 0;
+  return layout(*p).total;
+}
+
+int focus_route(const focus_params* p, const float* r, const float* C, uint32_t* mask_out,
+                float* margin_out, void* ws, size_t ws_bytes, void* stream) {
+  int rc = check_params(p);
+  if (rc) return rc;
+  if (!r || !C || !mask_out) return FOCUS_ERR_INVALID_ARG;
+  if (!aligned(r, 16) || !aligned(C, 4) || !aligned(mask_out, 4) || !aligned(margin_out, 4))
+    return FOCUS_ERR_ALIGNMENT;
+  const WsLayout L = layout(*p);
+  if ((rc = check_ws(L, ws, ws_bytes))) return rc;
+  cudaStream_t s = (cudaStream_t)stream;
+  char* w = (char*)ws;
+  if ((rc = cuda_rc(reset_header(w, s)))) return rc;
+  return cuda_rc(launch_route(*p, L, r, C, w, mask_out, margin_out, s));
+}
+
+int focus_bucket(const focus_params* p, const uint32_t* mask, int32_t* perm_out,
+                 int32_t* seg_off_out, void* ws, size_t ws_bytes, void* stream) {
+  int rc = check_params(p);
+  if (rc) return rc;
+  if (!mask) return FOCUS_ERR_INVALID_ARG;
+  if (!aligned(mask, 4) || !aligned(perm_out, 4) || !aligned(seg_off_out, 4))
+    return FOCUS_ERR_ALIGNMENT;
+  const WsLayout L = layout(*p);
+  if ((rc = check_ws(L, ws, ws_bytes))) return rc;
+  cudaStream_t s = (cudaStream_t)stream;
+  char* w = (char*)ws;
+  if ((rc = cuda_rc(reset_header(w, s)))) return rc;
+  if ((rc = cuda_rc(launch_bucket(*p, L, mask, w, s)))) return rc;
+  const size_t BR = (size_t)p->B * p->R;
+  if (perm_out &&
+      (rc = cuda_rc(cudaMemcpyAsync(perm_out, w + L.perm, sizeof(int) * BR * p->N,
+                                    cudaMemcpyDeviceToDevice, s))))
+    return rc;
+  if (seg_off_out &&
+      (rc = cuda_rc(cudaMemcpyAsync(seg_off_out, w + L.segoff, sizeof(int) * BR * (L.nseg + 1),
+                                    cudaMemcpyDeviceToDevice, s))))
+    return rc;
+  return FOCUS_OK;
+}
+
+int focus_attn_fwd_ev(const focus_params* p, const uint16_t* q, const uint16_t* k,
+                      const uint16_t* v, const float* r, const float* C,
+                      const uint32_t* mask_in, uint16_t* o, float* lse, void* ws,
+                      size_t ws_bytes, void* stream, void* const* stage_events) {
+  int rc = check_params(p);
+  if (rc) return rc;
+  if (!q || !k || !v || !o) return FOCUS_ERR_INVALID_ARG;
+  if (!mask_in && (!r || !C)) return FOCUS_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
+      !aligned(lse, 4) || !aligned(mask_in, 4) || !aligned(r, 16) || !aligned(C, 4))
+    return FOCUS_ERR_ALIGNMENT;
+  const WsLayout L = layout(*p);
+  if ((rc = check_ws(L, ws, ws_bytes))) return rc;
+  cudaStream_t s = (cudaStream_t)stream;
+  char* w = (char*)ws;
+  const float scale = p->softmax_scale > 0.0f ? p->softmax_scale : 1.0f / sqrtf((float)p->d_head);
+  const bf16* qb = reinterpret_cast<const bf16*>(q);
+  const bf16* kb = reinterpret_cast<const bf16*>(k);
+  const bf16* vb = reinterpret_cast<const bf16*>(v);
+  auto mark = [&](int i) -> int {
+    if (!stage_events) return FOCUS_OK;
+    return cuda_rc(cudaEventRecord((cudaEvent_t)stage_events[i], s));
+  };
+
+  if ((rc = mark(0))) return rc;
+  if ((rc = cuda_rc(reset_header(w, s)))) return rc;
+  const uint32_t* mask = mask_in;
+  if (!mask) {
+    uint32_t* m = reinterpret_cast<uint32_t*>(w + L.mask);
+    if ((rc = cuda_rc(launch_route(*p, L, r, C, w, m, nullptr, s)))) return rc;
+    mask = m;
+  }
+  if ((rc = mark(1))) return rc;
+  if ((rc = cuda_rc(launch_bucket(*p, L, mask, w, s)))) return rc;
+  if ((rc = cuda_rc(launch_qtab(*p, L, mask, w, s)))) return rc;
+  if ((rc = mark(2))) return rc;
+  if ((rc = cuda_rc(launch_permute(*p, L, qb, kb, vb, w, s)))) return rc;
+  if ((rc = mark(3))) return rc;
+  if ((rc = cuda_rc(launch_attn_long(*p, L, mask, w, scale, s)))) return rc;
+  if ((rc = mark(4))) return rc;
+  if ((rc = cuda_rc(launch_attn_window(*p, L, qb, kb, vb, w, reinterpret_cast<bf16*>(o), lse,
+                                       scale, s))))
+    return rc;
+  return mark(5);
+}
+
+int focus_attn_fwd(const focus_params* p, const uint16_t* q, const uint16_t* k,
+                   const uint16_t* v, const float* r, const float* C, const uint32_t* mask_in,
+                   uint16_t* o, float* lse, void* ws, size_t ws_bytes, void* stream) {
+  return focus_attn_fwd_ev(p, q, k, v, r, C, mask_in, o, lse, ws, ws_bytes, stream, nullptr);
+}
+
+int focus_get_status(const void* ws, void* stream) {
+  if (!ws) return FOCUS_ERR_INVALID_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  int status = 0;
+  if (cudaMemcpyAsync(&status, ws, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return FOCUS_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return FOCUS_ERR_CUDA;
+  return status;
+}
+
+const char* focus_strerror(int code) {
+  switch (code) {
+    case FOCUS_OK: return "ok";
+    case FOCUS_ERR_INVALID_ARG: return "invalid argument";
+    case FOCUS_ERR_UNSUPPORTED: return "unsupported parameters";
+    case FOCUS_ERR_WORKSPACE: return "workspace too small";
+    case FOCUS_ERR_CUDA: return "CUDA error";
+    case FOCUS_ERR_TIMEOUT: return "device wait timed out";
+    case FOCUS_ERR_BOUNDS: return "device index check failed (mask with wrong bit count?)";
+    case FOCUS_ERR_ALIGNMENT: return "misaligned pointer";
+    default: return "unknown status";
+  }
+}
+
+int focus_version(void) { return (1 << 16) | 0; }
+
+}  // extern "C"

@@ -1,0 +1,48 @@
+"""Exact count of allowed (query, key) pairs, for FLOP accounting (host side).
+
+A pair (i, j) is allowed when j <= i and either i - j < w (window) or the two
+tokens' group bitmasks intersect ("Why Attend to Everything? Focus is the Key",
+gist.science technical summary, section 2, "Inference Efficiency (Top-k)").
+The count is exact: window pairs in closed form, long-range pairs by binary
+search of each query position minus w in the sorted positions of every
+compatible mask value.  O(N log N * distinct masks), no N x N work.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+
+def window_pairs(N: int, w: int) -> int:
+    """sum_i min(i + 1, w) for i < N."""
+    if N <= w:
+        return N * (N + 1) // 2
+    return N * w - w * (w - 1) // 2
+
+
+def allowed_pairs(mask, w: int) -> np.ndarray:
+    """mask [B, R, N] (uint32 bit patterns, any integer dtype) -> [B, R] int64 counts."""
+    m = np.asarray(mask).astype(np.int64) & 0xFFFFFFFF
+    B, R, N = m.shape
+    out = np.zeros((B, R), np.int64)
+    win = window_pairs(N, w)
+    for b in range(B):
+        for rho in range(R):
+            row = m[b, rho]
+            vals, inv = np.unique(row, return_inverse=True)
+            pos = [np.nonzero(inv == a)[0] for a in range(len(vals))]  # ascending
+            far = 0
+            for a, va in enumerate(vals):
+                qpos = pos[a] - w  # keys j <= i - w
+                for c, vc in enumerate(vals):
+                    if int(va) & int(vc):
+                        far += int(np.searchsorted(pos[c], qpos, side="right").sum())
+            out[b, rho] = win + far
+    return out
+
+
+def allowed_flops(mask, w: int, H: int, H_kv: int, d_head: int) -> int:
+    """4 * d_head FLOPs per allowed pair per query head (QK^T and PV, 2 each)."""
+    cnt = allowed_pairs(mask, w)  # [B, R]
+    R = cnt.shape[1]
+    heads_per_rho = H // R
+    return int(4 * d_head * heads_per_rho * cnt.sum())

@@ -52,7 +52,8 @@ def _load():
         lib.oracle_route.restype = i32
         lib.oracle_allowed_pairs.argtypes = [i32, i32, i32, i32, P, P]
         lib.oracle_allowed_pairs.restype = i32
-        lib.oracle_attn.argtypes = [i32, i32, i32, i32, i32, i32, i32, f64, P, P, P, P, P, i64, P, P, i32]
+        lib.oracle_attn.argtypes = [i32, i32, i32, i32, i32, i32, i32, f64, P, P, P, P, P, i64, P, i32,
+                                    P, P, i32]
         lib.oracle_attn.restype = i32
         _lib = lib
     return _lib
@@ -110,12 +111,13 @@ def allowed_pairs(mask, w: int) -> np.ndarray:
     return out
 
 
-def attn(q, k, v, mask, *, w: int, scale: float | None = None, rows=None, n_threads: int | None = None):
+def attn(q, k, v, mask, *, w: int, scale: float | None = None, rows=None, heads=None,
+         n_threads: int | None = None):
     """Union-softmax attention for q [B, N, H, d], k/v [B, N, H_kv, d] (bf16 tensors or
     uint16 bit arrays) and mask [B, R, N].
 
-    rows: optional flattened query rows (b * N + i). Returns (o [n_rows, H, d] f64,
-    lse [n_rows, H] f64)."""
+    rows: optional flattened query rows (b * N + i); heads: optional query heads.
+    Returns (o [n_rows, n_heads, d] f64, lse [n_rows, n_heads] f64)."""
     q16, k16, v16 = _np(q, np.uint16), _np(k, np.uint16), _np(v, np.uint16)
     mask = _np(mask, np.uint32)
     B, N, H, d = q16.shape
@@ -126,11 +128,13 @@ def attn(q, k, v, mask, *, w: int, scale: float | None = None, rows=None, n_thre
         scale = 1.0 / np.sqrt(d)
     rows_a = None if rows is None else _np(rows, np.int64)
     n_rows = B * N if rows_a is None else rows_a.shape[0]
-    o = np.zeros((n_rows, H, d), np.float64)
-    lse = np.zeros((n_rows, H), np.float64)
+    heads_a = None if heads is None else _np(heads, np.int32)
+    n_heads = H if heads_a is None else heads_a.shape[0]
+    o = np.zeros((n_rows, n_heads, d), np.float64)
+    lse = np.zeros((n_rows, n_heads), np.float64)
     rc = _load().oracle_attn(B, N, H, H_kv, R, d, w, float(scale), _ptr(q16), _ptr(k16), _ptr(v16),
-                             _ptr(mask), _ptr(rows_a), n_rows, _ptr(o), _ptr(lse),
-                             n_threads or n_cores())
+                             _ptr(mask), _ptr(rows_a), n_rows, _ptr(heads_a), n_heads, _ptr(o),
+                             _ptr(lse), n_threads or n_cores())
     if rc != 0:
         raise ValueError("oracle_attn: bad arguments")
     return o, lse

@@ -195,14 +195,17 @@ typedef struct {
   const uint32_t* mask;
   const int64_t* rows; /* flattened (b * N + i) query rows, or NULL for all */
   int64_t n_rows;
+  const int32_t* heads; /* query heads to compute, or NULL for all H */
+  int n_heads;
   double *o, *lse;
   int64_t next;        /* work counter */
   pthread_mutex_t mu;
 } attn_job;
 
 /* One query row of one head: two-pass softmax over the union set A_i. */
-static void attn_row(const attn_job* J, int64_t out_row, int64_t bi, int h, double* s_buf,
+static void attn_row(const attn_job* J, int64_t out_row, int64_t bi, int hs, double* s_buf,
                      int64_t* j_buf, double* qv) {
+  const int h = J->heads ? J->heads[hs] : hs;
   const int b = (int)(bi / J->N);
   const int64_t i = bi % J->N;
   const int kvh = h / (J->H / J->H_kv);
@@ -230,14 +233,14 @@ static void attn_row(const attn_job* J, int64_t out_row, int64_t bi, int h, doub
   double sum = 0.0;
   for (int64_t a = 0; a < n; ++a) sum += exp(s_buf[a] - mx);
   const double lse = mx + log(sum);
-  double* o = J->o + (out_row * J->H + h) * d;
+  double* o = J->o + (out_row * J->n_heads + hs) * d;
   for (int t = 0; t < d; ++t) o[t] = 0.0;
   for (int64_t a = 0; a < n; ++a) {
     const double p = exp(s_buf[a] - lse);
     const uint16_t* vj = J->v + (((int64_t)b * J->N + j_buf[a]) * J->H_kv + kvh) * d;
     for (int t = 0; t < d; ++t) o[t] += p * bf16_to_double(vj[t]);
   }
-  J->lse[out_row * J->H + h] = lse;
+  J->lse[out_row * J->n_heads + hs] = lse;
 }
 
 static void* attn_worker(void* arg) {
@@ -245,7 +248,7 @@ static void* attn_worker(void* arg) {
   double* s_buf = (double*)malloc(sizeof(double) * (size_t)J->N);
   int64_t* j_buf = (int64_t*)malloc(sizeof(int64_t) * (size_t)J->N);
   double* qv = (double*)malloc(sizeof(double) * (size_t)J->d);
-  const int64_t total = J->n_rows * J->H;
+  const int64_t total = J->n_rows * J->n_heads;
   const int64_t chunk = 4;
   for (;;) {
     pthread_mutex_lock(&J->mu);
@@ -255,10 +258,10 @@ static void* attn_worker(void* arg) {
     if (start >= total) break;
     int64_t end = start + chunk < total ? start + chunk : total;
     for (int64_t u = start; u < end; ++u) {
-      int64_t out_row = u / J->H;
-      int h = (int)(u % J->H);
+      int64_t out_row = u / J->n_heads;
+      int hs = (int)(u % J->n_heads);
       int64_t bi = J->rows ? J->rows[out_row] : out_row;
-      attn_row(J, out_row, bi, h, s_buf, j_buf, qv);
+      attn_row(J, out_row, bi, hs, s_buf, j_buf, qv);
     }
   }
   free(s_buf); free(j_buf); free(qv);
@@ -270,19 +273,25 @@ static void* attn_worker(void* arg) {
  *   q [B, N, H, d], k/v [B, N, H_kv, d]: bf16 bit patterns
  *   mask [B, R, N] uint32 (from oracle_route or from the kernel under test)
  *   rows (nullable) flattened query rows b*N + i, n_rows of them; NULL = all B*N rows
- *   o   [n_rows, H, d] double out;  lse [n_rows, H] double out (natural log)
+ *   heads (nullable) query heads to compute, n_heads of them; NULL = all H heads
+ *   o   [n_rows, n_heads, d] double out;  lse [n_rows, n_heads] double out (natural log)
  * Head h reads KV head h / (H / H_kv) and routing head (h / (H / H_kv)) / (H_kv / R).
  */
 int oracle_attn(int B, int N, int H, int H_kv, int R, int d, int w, double scale,
                 const uint16_t* q, const uint16_t* k, const uint16_t* v, const uint32_t* mask,
-                const int64_t* rows, int64_t n_rows, double* o, double* lse, int n_threads) {
+                const int64_t* rows, int64_t n_rows, const int32_t* heads, int n_heads,
+                double* o, double* lse, int n_threads) {
   if (B < 1 || N < 1 || H < 1 || H_kv < 1 || R < 1 || d < 1 || w < 1 || H % H_kv ||
       H_kv % R || n_rows < 0)
     return -1;
   if (!rows) n_rows = (int64_t)B * N;
   for (int64_t a = 0; rows && a < n_rows; ++a)
     if (rows[a] < 0 || rows[a] >= (int64_t)B * N) return -1;
-  attn_job J = {B, N, H, H_kv, R, d, w, scale, q, k, v, mask, rows, n_rows, o, lse, 0};
+  if (!heads) n_heads = H;
+  for (int a = 0; heads && a < n_heads; ++a)
+    if (heads[a] < 0 || heads[a] >= H) return -1;
+  attn_job J = {B, N, H, H_kv, R, d, w, scale, q, k, v, mask, rows, n_rows, heads, n_heads,
+                o, lse, 0};
   pthread_mutex_init(&J.mu, NULL);
   if (n_threads < 1) n_threads = 1;
   if (n_threads > 256) n_threads = 256;

@@ -1,0 +1,89 @@
+"""Host-side checks of the C ABI (no GPU needed): the library loads, exports every
+function the header declares, sizes its workspace, and rejects bad arguments before
+launching anything. Also the host-side pair accounting against the oracle."""
+import ctypes
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import learned_centroid_gated_gb300 as focus
+import oracle
+from learned_centroid_gated_gb300 import pairs
+
+
+def _params(**kw):
+    base = dict(B=1, N=512, H=2, H_kv=2, d_head=64, R=1, K=4, top_k=2, w=64)
+    base.update(kw)
+    return focus.Params(**base)
+
+
+def test_every_declared_symbol_is_exported():
+    names = focus.declared_symbols()
+    assert set(names) >= {"focus_route", "focus_attn_fwd", "focus_bucket", "focus_workspace_size",
+                          "focus_get_status", "focus_strerror", "focus_version"}
+    lib = ctypes.CDLL(focus.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_version_and_strerror():
+    assert focus.version() >> 16 == 1
+    assert focus.strerror(0) == "ok"
+    for code in range(-7, 0):
+        assert focus.strerror(code) not in ("", "unknown status")
+    assert focus.strerror(-99) == "unknown status"
+
+
+def test_workspace_size_valid_and_invalid():
+    p = _params()
+    n = focus.workspace_size(p)
+    # at least the permuted copies and the fp32 long-range partial output
+    assert n >= 2 * 3 * p.N * p.H * p.d_head + 4 * p.N * p.H * p.d_head
+    assert focus.workspace_size(_params(N=1024)) > n
+    for bad in (dict(N=0), dict(H=3, H_kv=2), dict(H_kv=2, R=3), dict(top_k=5),
+                dict(K=33, top_k=1), dict(w=0), dict(d_head=96), dict(K=16, top_k=8),
+                dict(sinkhorn_iters=1, sinkhorn_eps=0.0)):
+        assert focus.workspace_size(_params(**bad)) == 0, bad
+
+
+def _call_attn(p, q=1 << 12, k=1 << 12, v=1 << 12, r=1 << 12, C=1 << 12, mask=None, o=1 << 12,
+               lse=None, ws=1 << 12, ws_bytes=None):
+    P = ctypes.c_void_p
+    nb = focus.workspace_size(p) if ws_bytes is None else ws_bytes
+    return focus._lib.focus_attn_fwd(ctypes.byref(p.c()), P(q), P(k), P(v), P(r), P(C), P(mask),
+                                     P(o), P(lse), P(ws), nb, None)
+
+
+def test_argument_errors_are_caught_on_the_host():
+    p = _params()
+    E = {v: k for k, v in focus.ERRORS.items()}
+    assert _call_attn(p, q=None) == E["FOCUS_ERR_INVALID_ARG"]
+    assert _call_attn(p, r=None) == E["FOCUS_ERR_INVALID_ARG"]   # no mask, no routing
+    assert _call_attn(p, q=(1 << 12) + 2) == E["FOCUS_ERR_ALIGNMENT"]
+    assert _call_attn(p, ws=(1 << 12) + 64) == E["FOCUS_ERR_ALIGNMENT"]
+    assert _call_attn(p, ws_bytes=focus.workspace_size(p) - 1) == E["FOCUS_ERR_WORKSPACE"]
+    assert _call_attn(_params(d_head=96)) == E["FOCUS_ERR_UNSUPPORTED"]
+    assert _call_attn(_params(K=16, top_k=8)) == E["FOCUS_ERR_UNSUPPORTED"]
+    assert _call_attn(_params(H=4, H_kv=3)) == E["FOCUS_ERR_INVALID_ARG"]
+    assert focus._lib.focus_route(None, None, None, None, None, None, 0, None) == E["FOCUS_ERR_INVALID_ARG"]
+
+
+@pytest.mark.parametrize("N,w,K,top_k,R", [(1, 1, 1, 1, 1), (97, 5, 4, 2, 2), (300, 16, 6, 2, 1),
+                                           (257, 300, 4, 1, 1), (200, 1, 5, 3, 1)])
+def test_pair_count_matches_oracle_brute_force(N, w, K, top_k, R):
+    g = torch.Generator().manual_seed(N + K)
+    r = torch.randn(2, N, R, 16, generator=g)
+    C = torch.randn(K, 16, generator=g)
+    mask, _, _, _ = oracle.route(r, C, K=K, top_k=top_k)
+    np.testing.assert_array_equal(pairs.allowed_pairs(mask, w), oracle.allowed_pairs(mask, w))
+
+
+def test_window_pairs_closed_form():
+    for N, w in [(1, 1), (5, 10), (10, 10), (100, 7)]:
+        assert pairs.window_pairs(N, w) == sum(min(i + 1, w) for i in range(N))
+
+
+def test_nseg_is_binomial():
+    assert _params(K=8, top_k=2).nseg == 28 == math.comb(8, 2)

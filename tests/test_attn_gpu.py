@@ -1,0 +1,104 @@
+"""Focus attention forward through the C ABI vs the CPU oracle (GPU).
+
+Small problems compare every output row; the full-size workloads compare a seeded
+sample of query rows (always including 0, w-1, w and N-1) in exactly the launch
+configuration the benchmark times.  The oracle runs on the mask the GPU produced
+(so a flipped near-tie cannot fail the output check); membership itself is
+compared separately, bit-exact away from near-ties."""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from parity import compare_membership, compare_outputs, mask_np
+
+focus = pytest.importorskip("learned_centroid_gated_gb300")
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(wl, seed=0, rows=None, heads=None, scale=0.0, use_mask_in=False):
+    x = synth.make_inputs(wl, seed=seed, device="cuda")
+    p = focus.Params.from_workload(wl, softmax_scale=scale)
+    mask, _ = focus.route(p, x["r"], x["C"])
+    if use_mask_in:
+        o, lse = focus.attn_fwd(p, x["q"], x["k"], x["v"], mask=mask)
+    else:
+        o, lse = focus.attn_fwd(p, x["q"], x["k"], x["v"], x["r"], x["C"])
+    ws = focus._default_ws[str(x["q"].device)].buf
+    assert focus.get_status(ws) == 0
+    m = mask_np(mask)
+    o_ref, lse_ref = oracle.attn(x["q"], x["k"], x["v"], m, w=wl.w,
+                                 scale=p.scale, rows=rows, heads=heads)
+    errs = compare_outputs(o, lse, o_ref, lse_ref, rows, heads)
+    return x, m, errs
+
+
+SMALL = {
+    "tiny": synth.WORKLOADS["tiny"],
+    "gpt2_layer": synth.WORKLOADS["gpt2_layer"],
+    "single_token": synth.WORKLOADS["tiny"].replace(N=1),
+    "ragged_gqa3": synth.WORKLOADS["tiny"].replace(N=300, H=3, H_kv=1, K=5, top_k=2, w=37),
+    "routing_per_kv_group_d128_b2": synth.WORKLOADS["tiny"].replace(
+        B=2, N=1000, H=4, H_kv=2, R=2, d_head=128, K=6, top_k=3, w=100),
+    "window_covers_all": synth.WORKLOADS["tiny"].replace(N=700, w=900, d_head=128),
+    "one_group": synth.WORKLOADS["tiny"].replace(N=513, K=1, top_k=1, d_head=128),
+    "topk_equals_K": synth.WORKLOADS["tiny"].replace(N=640, K=4, top_k=4),
+    "unit_window_top1": synth.WORKLOADS["tiny"].replace(N=1200, K=8, top_k=1, w=1),
+    "sinkhorn5": synth.WORKLOADS["tiny"].replace(N=2000, sinkhorn_iters=5, sinkhorn_eps=0.5, w=128),
+    "many_segments_K32": synth.WORKLOADS["tiny"].replace(N=3000, K=32, top_k=2, w=50),
+    "gqa4_R8_small": synth.WORKLOADS["gqa_128k"].replace(N=2048, w=128),
+    "extreme_small": synth.WORKLOADS["extreme_1m"].replace(N=4096, w=256),
+}
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_attention_all_rows(name):
+    wl = SMALL[name]
+    _, _, errs = _run(wl, seed=1)
+    print(f"{name}: max|dO|={errs[0]:.2e} max rel dLSE={errs[1]:.2e}")
+
+
+def test_precomputed_mask_and_explicit_scale():
+    wl = synth.WORKLOADS["tiny"].replace(N=777, w=33)
+    _run(wl, seed=2, scale=0.05, use_mask_in=True)
+
+
+def test_deterministic_across_calls():
+    wl = synth.WORKLOADS["gpt2_layer"]
+    x = synth.make_inputs(wl, seed=3, device="cuda")
+    p = focus.Params.from_workload(wl)
+    o1, l1 = focus.attn_fwd(p, x["q"], x["k"], x["v"], x["r"], x["C"])
+    o1, l1 = o1.clone(), l1.clone()
+    o2, l2 = focus.attn_fwd(p, x["q"], x["k"], x["v"], x["r"], x["C"])
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_host_buffer_entry_matches_device_entry():
+    wl = synth.WORKLOADS["tiny"]
+    x = synth.make_inputs(wl, seed=4, device="cpu")
+    p = focus.Params.from_workload(wl)
+    o_h, l_h = focus.attn_fwd_host(p, x["q"], x["k"], x["v"], x["r"], x["C"])
+    d = {k: v.cuda() for k, v in x.items()}
+    o_d, l_d = focus.attn_fwd(p, d["q"], d["k"], d["v"], d["r"], d["C"])
+    assert torch.equal(o_h, o_d.cpu()) and torch.equal(l_h, l_d.cpu())
+
+
+# Full-size workloads: sampled query rows and, for the 1M-token case, two query
+# heads on different KV heads (the oracle's cost grows with N).
+# FOCUS_TEST_SAMPLES overrides the row count.
+FULL = {"mha7b_32k": (512, None), "gqa_128k": (256, None), "extreme_1m": (4096, [0, 31])}
+
+
+@pytest.mark.parametrize("name", list(FULL))
+def test_full_size_sampled_rows(name):
+    wl = synth.WORKLOADS[name]
+    n = int(os.environ.get("FOCUS_TEST_SAMPLES", FULL[name][0]))
+    rows = synth.sample_queries(wl.N, n, wl.w, seed=5)
+    x, m, errs = _run(wl, seed=0, rows=rows, heads=FULL[name][1])
+    n_diff, n_near = compare_membership(wl, m, x["r"], x["C"])
+    print(f"{name}: {n} rows, max|dO|={errs[0]:.2e} max rel dLSE={errs[1]:.2e}, "
+          f"membership differences {n_diff} (near-ties {n_near})")
