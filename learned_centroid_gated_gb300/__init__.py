@@ -214,6 +214,9 @@ def attn_fwd(p: Params, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, r=Non
         _check(_lib.focus_attn_fwd(*args), "focus_attn_fwd")
     else:
         assert len(stage_events) == N_STAGE_EVENTS
+        for e in stage_events:
+            if e.cuda_event == 0:  # torch creates the CUDA event on its first record
+                e.record(stream or torch.cuda.current_stream())
         evs = (ctypes.c_void_p * N_STAGE_EVENTS)(*[e.cuda_event for e in stage_events])
         _check(_lib.focus_attn_fwd_ev(*args, evs), "focus_attn_fwd_ev")
     return out, lse
