@@ -144,6 +144,29 @@ int focus_attn_fwd_ev(const focus_params* p, const uint16_t* q, const uint16_t* 
                       const uint32_t* mask_in, uint16_t* o, float* lse, void* ws,
                       size_t ws_bytes, void* stream, void* const* stage_events);
 
+/*
+ * focus_route without a workspace argument, for callers that cannot allocate
+ * device memory on their call path: for example a custom op or plugin inside an
+ * inference engine that hands all device memory to its own pool at start-up and
+ * forbids cudaMalloc afterwards (cudaMalloc can also synchronise the device,
+ * which such hosts must not do mid-stream). The paper has no counterpart; this is
+ * a deployment variant of focus_route with identical results.
+ *   Arguments and outputs as in focus_route (r, C, mask_out, optional margin_out,
+ *   stream); the caller still owns every input and output buffer.
+ *   Scratch: a file-scope device array of 4 MiB inside the library, held by
+ *   every GPU that loads the library until the process exits. Problems needing
+ *   more (256 * ceil(B*R*K*4 / 256) + B*R*ceil(N/256)*K*8 bytes) return
+ *   FOCUS_ERR_WORKSPACE before anything is launched.
+ *   The first call on each device looks up the array's device address (once,
+ *   with that device current); make that first call before any stream capture.
+ *   All calls share the one array and nothing in it needs clearing between calls
+ *   (every value is written before it is read), but calls that overlap on the GPU
+ *   (concurrent streams, several host threads) race on it: serialise them.
+ *   No device memory is allocated or freed by this call.
+ */
+int focus_route_static(const focus_params* p, const float* r, const float* C,
+                       uint32_t* mask_out, float* margin_out, void* stream);
+
 /* Synchronises `stream` and returns the device status word of the last call
  * that used this workspace (FOCUS_OK, FOCUS_ERR_TIMEOUT, FOCUS_ERR_BOUNDS), or
  * FOCUS_ERR_CUDA if the synchronisation itself failed. */

@@ -98,6 +98,8 @@ _lib.focus_attn_fwd_ev.argtypes = [_PP, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctyp
 _lib.focus_attn_fwd_ev.restype = ctypes.c_int
 N_STAGE_EVENTS = 6
 STAGES = ("route", "bucket", "permute", "attn_long", "attn_window")
+_lib.focus_route_static.argtypes = [_PP, _P, _P, _P, _P, _P]
+_lib.focus_route_static.restype = ctypes.c_int
 _lib.focus_get_status.argtypes = [_P, _P]
 _lib.focus_get_status.restype = ctypes.c_int
 _lib.focus_strerror.argtypes = [ctypes.c_int]
@@ -181,6 +183,20 @@ def route(p: Params, r: torch.Tensor, C: torch.Tensor, *, margin: bool = False, 
     _check(_lib.focus_route(ctypes.byref(p.c()), _ptr(r.contiguous()), _ptr(C.contiguous()),
                             _ptr(mask), _ptr(marg), _ptr(w), w.numel(), _stream(stream)),
            "focus_route")
+    return mask, marg
+
+
+def route_static(p: Params, r: torch.Tensor, C: torch.Tensor, *, margin: bool = False,
+                 stream=None):
+    """route() without a workspace: the library's fixed 4 MiB device scratch is used
+    instead, for callers that must not allocate device memory when they call in.
+    The outputs here are still torch tensors; pass preallocated ones through the C
+    ABI (focus_route_static) to allocate nothing at all."""
+    assert r.dtype == torch.float32 and C.dtype == torch.float32 and r.is_cuda and C.is_cuda
+    mask = torch.empty(p.B, p.R, p.N, dtype=torch.int32, device=r.device)
+    marg = torch.empty(p.B, p.R, p.N, dtype=torch.float32, device=r.device) if margin else None
+    _check(_lib.focus_route_static(ctypes.byref(p.c()), _ptr(r.contiguous()), _ptr(C.contiguous()),
+                                   _ptr(mask), _ptr(marg), _stream(stream)), "focus_route_static")
     return mask, marg
 
 

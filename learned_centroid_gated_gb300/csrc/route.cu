@@ -220,3 +220,75 @@ cudaError_t launch_route(const focus_params& p, const WsLayout& L, const float* 
 }
 
 }  // namespace focus
+
+// ------------------------------------------------------ allocation-free entry --
+// focus_route_static: focus_route without a caller workspace.  Its scratch (the
+// Sinkhorn column partials and potentials) lives in the file-scope device array
+// below, which every GPU that loads this library holds until the process exits.
+#include <mutex>
+
+namespace focus {
+namespace {
+
+constexpr size_t kStaticScratchBytes = size_t(4) << 20;  // 4 MiB
+constexpr int kMaxDevices = 64;
+
+static __device__ __align__(256) unsigned char g_route_scratch[kStaticScratchBytes];
+
+std::mutex g_scratch_mu;
+void* g_scratch_ptr[kMaxDevices] = {};
+
+// Device address of g_route_scratch on the current device, looked up once per
+// device (host code cannot use the symbol itself as a device pointer).
+cudaError_t static_scratch(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (!g_scratch_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_route_scratch);
+    if (e != cudaSuccess) return e;
+    g_scratch_ptr[dev] = p;
+  }
+  *out = g_scratch_ptr[dev];
+  return cudaSuccess;
+}
+
+}  // namespace
+}  // namespace focus
+
+extern "C" int focus_route_static(const focus_params* p, const float* r, const float* C,
+                                  uint32_t* mask_out, float* margin_out, void* stream) {
+  using namespace focus;
+  if (!p) return FOCUS_ERR_INVALID_ARG;
+  if (focus_workspace_size(p) == 0) {  // the shape checks of every other entry point
+    const bool shape_ok = p->B >= 1 && p->N >= 1 && p->H >= 1 && p->H_kv >= 1 && p->R >= 1 &&
+                          p->K >= 1 && p->top_k >= 1 && p->w >= 1 && p->sinkhorn_iters >= 0 &&
+                          p->H % p->H_kv == 0 && p->H_kv % p->R == 0 && p->K <= FOCUS_MAX_K &&
+                          p->top_k <= p->K &&
+                          (p->sinkhorn_iters == 0 || p->sinkhorn_eps > 0.0f);
+    return shape_ok ? FOCUS_ERR_UNSUPPORTED : FOCUS_ERR_INVALID_ARG;
+  }
+  if (!r || !C || !mask_out) return FOCUS_ERR_INVALID_ARG;
+  if ((uintptr_t)r % 16 || (uintptr_t)C % 4 || (uintptr_t)mask_out % 4 ||
+      (uintptr_t)margin_out % 4)
+    return FOCUS_ERR_ALIGNMENT;
+  // Scratch layout inside the static array: beta [B*R, K] fp32, then the column
+  // partials [B*R, ceil(N/256), K] (max, sum) pairs.  Every partial is written
+  // before it is read and beta is not read before the first column step writes
+  // it, so nothing has to be cleared between calls.
+  WsLayout L{};
+  const size_t BR = (size_t)p->B * p->R;
+  L.nblk_sk = (p->N + kSinkBlock - 1) / kSinkBlock;
+  L.beta = 0;
+  L.skpart = align_up(sizeof(float) * BR * p->K, 256);
+  const size_t need = L.skpart + sizeof(float2) * BR * (size_t)L.nblk_sk * p->K;
+  if (need > kStaticScratchBytes) return FOCUS_ERR_WORKSPACE;
+  void* scratch = nullptr;
+  if (static_scratch(&scratch) != cudaSuccess) return FOCUS_ERR_CUDA;
+  const cudaError_t e = launch_route(*p, L, r, C, static_cast<char*>(scratch), mask_out,
+                                     margin_out, (cudaStream_t)stream);
+  return e == cudaSuccess ? FOCUS_OK : FOCUS_ERR_CUDA;
+}
