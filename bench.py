@@ -321,13 +321,13 @@ def run_focus(args):
     t_long = stage_ms["attn_long"] / 1e3
     achieved = flops_long / t_long / 1e12
     roofline = {
-        "kernel": "attn_long (long-range block-sparse attention)",
+        "kernel": "attn_tc<128, long> (long-range block-sparse attention, tcgen05)",
         "bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
         "frac": achieved / peaks["bf16_tflops"],
         "peak_source": f"{peak_src} bf16 dense burst",
         "peak_sustained": peaks["bf16_tflops_sustained"],
         "frac_sustained": achieved / peaks["bf16_tflops_sustained"],
-        "traffic": traffic_of(os.path.join(ROOT, "learned_centroid_gated_gb300", "csrc", "attn.cu")),
+        "traffic": traffic_of(os.path.join(ROOT, "learned_centroid_gated_gb300", "csrc", "attn_tc.cu")),
         "algorithmic_flops_per_launch": flops_long,
         "launch_ms": stage_ms["attn_long"],
     }

@@ -1,0 +1,652 @@
+// Focus attention on the 5th-generation tensor cores (tcgen05, TMEM, TMA).
+//
+// "Why Attend to Everything? Focus is the Key", gist.science technical summary,
+// section 2 "Core Architecture": a local window of w tokens attends with exact
+// softmax, distant tokens only within a shared group ("Inference Efficiency
+// (Top-k)": at least one shared group); jindou-blog deep read, method bullets:
+// exact softmax inside the groups too.  The two key sets are disjoint
+// (long-range keys have i - j >= w, window keys i - j < w), so the union
+// softmax is the log-sum-exp merge of two partial softmaxes; every key is
+// visited once because tokens are bucketed by their exact group set.
+//
+// One CTA = 256 query rows of one head, as two 128-row tiles A and B that
+// ping-pong on the tensor core:
+//   warp 8     TMA producer: Q tiles once, then K and V tiles through a 3-slot ring
+//   warp 9     MMA issuer (one thread): S = Q K^T into TMEM, O += P V into TMEM
+//   warps 0-3  softmax of tile A (thread = row = TMEM lane), warps 4-7 of tile B
+// TMEM (512 columns): S_A | S_B | O_A | O_B.  P goes to shared memory in the
+// 128-byte-swizzled K-major layout the MMA reads.  Issue order on the tensor
+// core: S_A(0) S_B(0) | PV_A(t) S_A(t+1) PV_B(t) S_B(t+1) | ..., so the softmax of
+// one tile runs while the tensor core works on the other.  The running max is
+// rescaled lazily (only when it grows by more than 2^8), in place in TMEM.
+//
+//   attn_tc<D, true>   long-range part: query block of one segment x the key
+//                      tiles of every compatible segment (permuted copies),
+//                      keys with pos_j <= pos_i - w.  Writes O_lr, LSE_lr.
+//   attn_tc<D, false>  window part in token order, keys (i - w, i]; merges
+//                      (O_lr, LSE_lr) and writes O (bf16) and LSE.
+#include <math.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "tc_ptx.cuh"
+
+namespace focus {
+namespace {
+
+using namespace ptx;
+
+constexpr int QT = 128;       // rows per query tile (MMA M)
+constexpr int BMQ = 2 * QT;   // query rows per CTA
+constexpr int BNK = 128;      // keys per tile (MMA N of S, K of PV)
+constexpr int NSTAGE = 3;     // K/V ring slots
+constexpr int NTHREADS = 320;
+constexpr int PRODUCER_WARP = 8;
+constexpr int MMA_WARP = 9;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescale = 8.0f;  // log2 units: rescale O only when the max grows by > 2^8
+
+template <int D>
+struct Layout {
+  static constexpr int BOX = QT * 128;        // one TMA box: 128 rows x 128 bytes
+  static constexpr int BOXES = D / 64;        // boxes per 128 x D tile
+  static constexpr int TILE = BOXES * BOX;    // a 128-row Q/K/V tile, bf16
+  static constexpr int PBYTES = 2 * BOX;      // P tile: 128 rows x 128 keys, bf16
+  static constexpr int Q = 0;
+  static constexpr int P = Q + 2 * TILE;
+  static constexpr int RING = P + 2 * PBYTES;
+  static constexpr int BAR = RING + NSTAGE * TILE;
+  static constexpr int SMEM = BAR + 128 + 1024;  // + barriers, + 1 KB alignment slack
+};
+
+struct TcArgs {
+  int B, N, H, H_kv, R, w, nseg, qtab_cap;
+  float sl2;  // softmax scale * log2(e)
+  const int* perm;
+  const int* seg_off;
+  const uint32_t* mask;
+  const QBlock* qtab;
+  const int* qtab_count;
+  float* o_lr;
+  float* lse_lr;
+  bf16* o;
+  float* lse;
+  int* status;
+};
+
+// First index in [lo, hi) with P[index] > x (P ascending), or hi.
+__device__ __forceinline__ int upper_bound_g(const int* __restrict__ P, int lo, int hi, int x) {
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(P + mid) <= x) lo = mid + 1; else hi = mid;
+  }
+  return lo;
+}
+
+// Long-range key segments of one query block.
+struct SegCtx {
+  const int* P;       // permuted token positions of this (b, rho)
+  const int* SO;      // segment offsets of this (b, rho)
+  const uint32_t* M;  // masks of this (b, rho)
+  int nseg, w, p_lo, p_hi;
+  uint32_t mS;
+};
+struct SegTile {
+  int start, cnt, nfull;
+};
+
+// Next segment T' >= T whose mask meets the query segment's and that holds keys
+// with pos <= p_hi - w; cnt counts those keys, nfull the leading tiles whose keys
+// all satisfy pos <= p_lo - w (no masking needed).
+__device__ bool next_seg(const SegCtx& c, int& T, SegTile& st) {
+  for (; T < c.nseg; ++T) {
+    const int s0 = __ldg(c.SO + T), s1 = __ldg(c.SO + T + 1);
+    if (s1 <= s0) continue;
+    const uint32_t mT = __ldg(c.M + __ldg(c.P + s0));
+    if (!(mT & c.mS)) continue;
+    const int hi = upper_bound_g(c.P, s0, s1, c.p_hi - c.w) - s0;
+    if (hi <= 0) continue;
+    st.start = s0;
+    st.cnt = hi;
+    st.nfull = (upper_bound_g(c.P, s0, s1, c.p_lo - c.w) - s0) / BNK;
+    ++T;
+    return true;
+  }
+  return false;
+}
+
+struct TileIt {
+  int T;
+  int t_in;
+  bool valid;
+  SegTile st;
+  __device__ void init(const SegCtx& c) {
+    T = 0;
+    t_in = 0;
+    valid = next_seg(c, T, st);
+  }
+  __device__ void advance(const SegCtx& c) {
+    if (++t_in * BNK >= st.cnt) {
+      t_in = 0;
+      valid = next_seg(c, T, st);
+    }
+  }
+};
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+template <int D, bool LONG>
+__global__ void __launch_bounds__(NTHREADS, 1)
+attn_tc(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
+        const __grid_constant__ CUtensorMap mv, const TcArgs a) {
+  using L = Layout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  // ---- the query block of this CTA ----
+  int b, h, kvh, rows, q_row0;
+  SegCtx sc{};
+  if constexpr (LONG) {
+    const int gq = a.H / a.H_kv, nkv = a.H_kv / a.R;
+    const int jq = blockIdx.x % gq;
+    const int rest = blockIdx.x / gq;
+    const int u = rest % a.qtab_cap, kvl = rest / a.qtab_cap;
+    if (u >= *a.qtab_count) return;
+    const QBlock e = a.qtab[u];
+    b = e.br / a.R;
+    const int rho = e.br % a.R;
+    kvh = rho * nkv + kvl;
+    h = kvh * gq + jq;
+    rows = e.rows;
+    q_row0 = e.row0;
+    sc.P = a.perm + (int64_t)e.br * a.N;
+    sc.SO = a.seg_off + (int64_t)e.br * (a.nseg + 1);
+    sc.M = a.mask + (int64_t)e.br * a.N;
+    sc.nseg = a.nseg;
+    sc.w = a.w;
+    sc.p_lo = __ldg(sc.P + e.row0);
+    sc.p_hi = __ldg(sc.P + e.row0 + rows - 1);
+    sc.mS = __ldg(sc.M + sc.p_lo);
+  } else {
+    q_row0 = blockIdx.x * BMQ;
+    h = blockIdx.y;
+    b = blockIdx.z;
+    kvh = h / (a.H / a.H_kv);
+    rows = min(BMQ, a.N - q_row0);
+  }
+  const int j_lo = LONG ? 0 : max(0, q_row0 - a.w + 1);
+  const int j_hi = LONG ? 0 : q_row0 + rows;
+
+  uint8_t* bar = sm + L::BAR;
+  const uint32_t b_q = smem_u32(bar);
+  const uint32_t b_full = b_q + 8, b_empty = b_q + 32;  // + 8 * stage
+  const uint32_t b_s = b_q + 56, b_p = b_q + 72, b_o = b_q + 88;  // + 8 * tile
+  const uint32_t b_drain = b_q + 104;
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(bar + 112);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bar + 116);
+  volatile int* ntiles_s = reinterpret_cast<volatile int*>(bar + 120);
+
+  if (warp == MMA_WARP) {
+    tmem_alloc(smem_u32(bar + 112), TMEM_COLS);
+    tmem_relinquish();
+  }
+  if (tid == 0) {
+    mbar_init(b_q, 1);
+    for (int s = 0; s < NSTAGE; ++s) {
+      mbar_init(b_full + 8 * s, 1);
+      mbar_init(b_empty + 8 * s, 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(b_s + 8 * t, 1);
+      mbar_init(b_p + 8 * t, 128);
+      mbar_init(b_o + 8 * t, 1);
+    }
+    mbar_init(b_drain, 1);
+    *abort_flag = 0;
+    int n = 0;
+    if constexpr (LONG) {
+      int T = 0;
+      SegTile st;
+      while (next_seg(sc, T, st)) n += (st.cnt + BNK - 1) / BNK;
+    } else {
+      n = (j_hi - j_lo + BNK - 1) / BNK;
+    }
+    *ntiles_s = n;
+    fence_barrier_init();
+    fence_proxy_async_smem();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int n = *ntiles_s;
+  int* status = a.status;
+
+  if (warp == PRODUCER_WARP) {
+    // ------------------------------------------------------------- producer --
+    if (lane == 0 && n > 0) {
+      tma_prefetch(&mq);
+      tma_prefetch(&mk);
+      tma_prefetch(&mv);
+      mbar_expect_tx(b_q, 2 * L::TILE);
+      for (int qt = 0; qt < 2; ++qt)
+        for (int bx = 0; bx < L::BOXES; ++bx) {
+          const uint32_t dst = smem_u32(sm + L::Q + qt * L::TILE + bx * L::BOX);
+          if constexpr (LONG)
+            tma_load_2d(dst, &mq, 64 * bx, ((b * a.H + h) * a.N) + q_row0 + qt * QT, b_q);
+          else
+            tma_load_3d(dst, &mq, 64 * bx, h, b * a.N + q_row0 + qt * QT, b_q);
+        }
+      int last_par[NSTAGE];
+      for (int s = 0; s < NSTAGE; ++s) last_par[s] = -1;
+      int stage = 0;
+      uint32_t phase = 0;
+      TileIt it;
+      if constexpr (LONG) it.init(sc);
+      bool ok = true;
+      for (int t = 0; t < n && ok; ++t) {
+        int row;
+        if constexpr (LONG) row = (b * a.H_kv + kvh) * a.N + it.st.start + it.t_in * BNK;
+        else row = b * a.N + j_lo + t * BNK;
+        for (int kv = 0; kv < 2; ++kv) {
+          if (!mbar_wait(b_empty + 8 * stage, phase ^ 1, abort_flag, status)) {
+            ok = false;
+            break;
+          }
+          const uint32_t full = b_full + 8 * stage;
+          mbar_expect_tx(full, L::TILE);
+          for (int bx = 0; bx < L::BOXES; ++bx) {
+            const uint32_t dst = smem_u32(sm + L::RING + stage * L::TILE + bx * L::BOX);
+            const CUtensorMap* m = kv ? &mv : &mk;
+            if constexpr (LONG) tma_load_2d(dst, m, 64 * bx, row, full);
+            else tma_load_3d(dst, m, 64 * bx, kvh, row, full);
+          }
+          last_par[stage] = (int)phase;
+          if (++stage == NSTAGE) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if constexpr (LONG) it.advance(sc);
+      }
+      if (*abort_flag) {  // let every copy in flight land before the CTA exits
+        mbar_drain(b_q, 0);
+        for (int s = 0; s < NSTAGE; ++s)
+          if (last_par[s] >= 0) mbar_drain(b_full + 8 * s, (uint32_t)last_par[s]);
+      }
+    }
+    __syncwarp();
+  } else if (warp == MMA_WARP) {
+    // ------------------------------------------------------------ MMA issue --
+    if (lane == 0 && n > 0) {
+      constexpr uint32_t IS = idesc_bf16(QT, BNK, 0);  // S = Q K^T, both K-major
+      constexpr uint32_t IPV = idesc_bf16(QT, D, 1);   // O += P V, V MN-major
+      const uint32_t q_base = smem_u32(sm + L::Q);
+      const uint32_t p_base = smem_u32(sm + L::P);
+      const uint32_t r_base = smem_u32(sm + L::RING);
+      auto slot = [&](int item) { return r_base + (item % NSTAGE) * L::TILE; };
+      auto ring_wait = [&](int item) {
+        return mbar_wait(b_full + 8 * (item % NSTAGE), (item / NSTAGE) & 1, abort_flag, status);
+      };
+      auto issue_S = [&](int qt, uint32_t kaddr) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk / 4) * L::BOX + (kk % 4) * 32;
+          umma_ss(tmem + qt * BNK, sw128_desc(q_base + qt * L::TILE + off, 16, 1024),
+                  sw128_desc(kaddr + off, 16, 1024), IS, kk > 0);
+        }
+      };
+      auto issue_PV = [&](int qt, uint32_t vaddr, bool acc) {
+#pragma unroll
+        for (int kk = 0; kk < BNK / 16; ++kk) {
+          const uint32_t poff = (kk / 4) * L::BOX + (kk % 4) * 32;
+          umma_ss(tmem + 2 * BNK + qt * D, sw128_desc(p_base + qt * L::PBYTES + poff, 16, 1024),
+                  sw128_desc(vaddr + kk * 2048, L::BOX, 1024), IPV, (acc || kk > 0) ? 1u : 0u);
+        }
+      };
+      bool ok = mbar_wait(b_q, 0, abort_flag, status) && ring_wait(0);
+      if (ok) {
+        tc_fence_after();
+        issue_S(0, slot(0));
+        umma_commit(b_s);
+        issue_S(1, slot(0));
+        umma_commit(b_s + 8);
+        umma_commit(b_empty + 8 * (0 % NSTAGE));
+      }
+      for (int t = 0; ok && t < n; ++t) {
+        const int iv = 2 * t + 1, ik = 2 * t + 2;
+        if (!(ok = ring_wait(iv) && mbar_wait(b_p, t & 1, abort_flag, status))) break;
+        tc_fence_after();
+        issue_PV(0, slot(iv), t > 0);
+        umma_commit(b_o);
+        if (t + 1 < n) {
+          if (!(ok = ring_wait(ik))) break;
+          tc_fence_after();
+          issue_S(0, slot(ik));
+          umma_commit(b_s);
+        }
+        if (!(ok = mbar_wait(b_p + 8, t & 1, abort_flag, status))) break;
+        tc_fence_after();
+        issue_PV(1, slot(iv), t > 0);
+        umma_commit(b_o + 8);
+        umma_commit(b_empty + 8 * (iv % NSTAGE));
+        if (t + 1 < n) {
+          issue_S(1, slot(ik));
+          umma_commit(b_s + 8);
+          umma_commit(b_empty + 8 * (ik % NSTAGE));
+        }
+      }
+      umma_commit(b_drain);  // every MMA issued above completes before TMEM is released
+      mbar_drain(b_drain, 0);
+    }
+    __syncwarp();
+  } else {
+    // -------------------------------------------------------------- softmax --
+    const int qt = warp >> 2;
+    const int r = (warp & 3) * 32 + lane;  // row in the tile = TMEM lane
+    const int rg = qt * QT + r;            // row in the CTA block
+    const bool row_ok = rg < rows;
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + lane_off + qt * BNK;
+    const uint32_t tO = tmem + lane_off + 2 * BNK + qt * D;
+    int qp;
+    if constexpr (LONG) qp = __ldg(sc.P + q_row0 + min(rg, rows - 1));
+    else qp = q_row0 + min(rg, rows - 1);
+    uint8_t* prow = sm + L::P + qt * L::PBYTES + r * 128;
+    const int rsw = r & 7;
+    float m_use = -INFINITY, l = 0.0f;
+    TileIt it;
+    if constexpr (LONG) it.init(sc);
+    bool ok = true;
+    for (int t = 0; t < n; ++t) {
+      int c_lo = 0, c_hi = BNK;
+      bool need_mask;
+      if constexpr (LONG) {
+        const int valid = min(BNK, it.st.cnt - it.t_in * BNK);
+        need_mask = it.t_in >= it.st.nfull;
+        if (need_mask) c_hi = upper_bound_g(sc.P + it.st.start + it.t_in * BNK, 0, valid, qp - a.w);
+        it.advance(sc);
+      } else {
+        const int j0 = j_lo + t * BNK;
+        c_lo = max(0, qp - a.w + 1 - j0);
+        c_hi = min(min(BNK, j_hi - j0), qp - j0 + 1);
+        need_mask = c_lo > 0 || c_hi < BNK;
+      }
+      ok = mbar_wait(b_s + 8 * qt, t & 1, abort_flag, status);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t x0[32], x1[32], x2[32], x3[32];
+      tmem_ld32(tS + 0, x0);
+      tmem_ld32(tS + 32, x1);
+      tmem_ld32(tS + 64, x2);
+      tmem_ld32(tS + 96, x3);
+      tmem_ld_wait(x0);
+      tie32(x1);
+      tie32(x2);
+      tie32(x3);
+      float mx = -INFINITY;
+      auto scale_mask = [&](uint32_t(&x)[32], int cb) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          float v = __uint_as_float(x[i]) * a.sl2;
+          if (need_mask && (cb + i < c_lo || cb + i >= c_hi)) v = -INFINITY;
+          x[i] = __float_as_uint(v);
+          mx = fmaxf(mx, v);
+        }
+      };
+      scale_mask(x0, 0);
+      scale_mask(x1, 32);
+      scale_mask(x2, 64);
+      scale_mask(x3, 96);
+      float f = 1.0f;
+      const bool rescale = mx > m_use + kRescale;
+      if (rescale) {
+        f = ex2(m_use - mx);  // 0 when m_use is -inf
+        l *= f;
+        m_use = mx;
+      }
+      const float ms = (m_use == -INFINITY) ? 0.0f : m_use;
+      auto emit = [&](uint32_t(&x)[32], int k) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float p0 = ex2(__uint_as_float(x[2 * i]) - ms);
+          const float p1 = ex2(__uint_as_float(x[2 * i + 1]) - ms);
+          l += p0 + p1;
+          pk[i] = pack_bf16(p0, p1);
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int cidx = 4 * k + q;  // 16-byte chunk (8 keys) index 0..15
+          uint8_t* dst = prow + (cidx >> 3) * L::BOX + (((cidx & 7) ^ rsw) << 4);
+          *reinterpret_cast<uint4*>(dst) = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+        }
+      };
+      emit(x0, 0);
+      emit(x1, 1);
+      emit(x2, 2);
+      emit(x3, 3);
+      // O (from PV of earlier tiles, all complete once S of this tile is) follows the
+      // new maximum; skipped while this row has seen no key (O is still zero then).
+      if (__any_sync(0xffffffffu, rescale && t > 0 && f != 0.0f)) {
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t y[32];
+          tmem_ld32(tO + 32 * c, y);
+          tmem_ld_wait(y);
+          const float g = (rescale && t > 0) ? f : 1.0f;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) y[i] = __float_as_uint(__uint_as_float(y[i]) * g);
+          tmem_st32(tO + 32 * c, y);
+        }
+        tmem_st_wait();
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(b_p + 8 * qt);
+    }
+    // ---- epilogue ----
+    if (ok && n > 0) {
+      ok = mbar_wait(b_o + 8 * qt, (n - 1) & 1, abort_flag, status);
+      ok = __all_sync(0xffffffffu, ok);
+      if (ok) tc_fence_after();
+    }
+    if (ok) {
+      const int64_t orow = (((int64_t)b * a.N + qp) * a.H + h) * D;
+      const int64_t lrow = ((int64_t)b * a.H + h) * a.N + qp;
+      if constexpr (LONG) {
+        const float inv = l > 0.0f ? 1.0f / l : 0.0f;
+        const float lse = l > 0.0f ? (m_use + log2f(l)) * kLn2 : -INFINITY;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t y[32];
+          if (n > 0) {
+            tmem_ld32(tO + 32 * c, y);
+            tmem_ld_wait(y);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) y[i] = 0u;
+          }
+          if (row_ok) {
+            float4* dst = reinterpret_cast<float4*>(a.o_lr + orow + 32 * c);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              dst[i] = make_float4(__uint_as_float(y[4 * i]) * inv, __uint_as_float(y[4 * i + 1]) * inv,
+                                   __uint_as_float(y[4 * i + 2]) * inv, __uint_as_float(y[4 * i + 3]) * inv);
+          }
+        }
+        if (row_ok) a.lse_lr[lrow] = lse;
+      } else {
+        float ww = 0.0f, wl = 0.0f, lse = 0.0f;
+        if (row_ok) {
+          const float lse_w = (m_use + log2f(l)) * kLn2;
+          const float lse_l = a.lse_lr[lrow];
+          if (lse_l == -INFINITY) {
+            ww = 1.0f / l;
+            lse = lse_w;
+          } else {
+            const float M = fmaxf(lse_w, lse_l);
+            const float ew = expf(lse_w - M), el = expf(lse_l - M);
+            const float tot = ew + el;
+            lse = M + logf(tot);
+            ww = ew / tot / l;
+            wl = el / tot;
+          }
+        }
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t y[32];
+          tmem_ld32(tO + 32 * c, y);
+          tmem_ld_wait(y);
+          if (row_ok) {
+            const float4* src = reinterpret_cast<const float4*>(a.o_lr + orow + 32 * c);
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              float4 ol = make_float4(0.f, 0.f, 0.f, 0.f);
+              if (wl != 0.0f) ol = src[i];
+              pk[2 * i] = pack_bf16(__uint_as_float(y[4 * i]) * ww + ol.x * wl,
+                                    __uint_as_float(y[4 * i + 1]) * ww + ol.y * wl);
+              pk[2 * i + 1] = pack_bf16(__uint_as_float(y[4 * i + 2]) * ww + ol.z * wl,
+                                        __uint_as_float(y[4 * i + 3]) * ww + ol.w * wl);
+            }
+            uint4* dst = reinterpret_cast<uint4*>(a.o + orow + 32 * c);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+          }
+        }
+        if (row_ok && a.lse) a.lse[lrow] = lse;
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == MMA_WARP) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------------ host side --
+using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                 const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                 const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                 CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiled encode_fn() {
+  static EncodeTiled fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiled>(p);
+  });
+  return fn;
+}
+
+// Tensor map over rows of D bf16 values: `heads` rows per token when heads > 0
+// (3-D: d, head, token), else plain rows (2-D: d, row).  Box: 64 columns x 128 rows
+// (x 1 head), 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* base, int D, int64_t rows, int heads) {
+  EncodeTiled fn = encode_fn();
+  if (!fn) return false;
+  const cuuint32_t es[3] = {1, 1, 1};
+  CUresult r;
+  if (heads > 0) {
+    const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)heads, (cuuint64_t)rows};
+    const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)heads * D * 2};
+    const cuuint32_t box[3] = {64, 1, 128};
+    r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  } else {
+    const cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)D * 2};
+    const cuuint32_t box[2] = {64, 128};
+    r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  }
+  return r == CUDA_SUCCESS;
+}
+
+TcArgs make_args(const focus_params& p, const WsLayout& L, char* ws, float scale) {
+  TcArgs a{};
+  a.B = p.B;
+  a.N = p.N;
+  a.H = p.H;
+  a.H_kv = p.H_kv;
+  a.R = p.R;
+  a.w = p.w;
+  a.nseg = L.nseg;
+  a.qtab_cap = p.B * p.R * ((p.N + BMQ - 1) / BMQ + L.nseg);
+  a.sl2 = scale * kLog2e;
+  a.perm = reinterpret_cast<const int*>(ws + L.perm);
+  a.seg_off = reinterpret_cast<const int*>(ws + L.segoff);
+  a.qtab = reinterpret_cast<const QBlock*>(ws + L.qtab);
+  a.qtab_count = &reinterpret_cast<const WsHeader*>(ws)->qtab_count;
+  a.o_lr = reinterpret_cast<float*>(ws + L.olr);
+  a.lse_lr = reinterpret_cast<float*>(ws + L.lselr);
+  a.status = &reinterpret_cast<WsHeader*>(ws)->status;
+  return a;
+}
+
+template <int D, bool LONG>
+cudaError_t launch_tc(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                      const TcArgs& a, dim3 grid, cudaStream_t s) {
+  const int smem = Layout<D>::SMEM;
+  cudaError_t e = cudaFuncSetAttribute(attn_tc<D, LONG>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  attn_tc<D, LONG><<<grid, NTHREADS, smem, s>>>(mq, mk, mv, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int tc_block_rows() { return BMQ; }
+
+cudaError_t launch_attn_long_tc(const focus_params& p, const WsLayout& L, const uint32_t* mask,
+                                char* ws, float scale, cudaStream_t s) {
+  TcArgs a = make_args(p, L, ws, scale);
+  a.mask = mask;
+  CUtensorMap mq, mk, mv;
+  if (!make_map(&mq, ws + L.qp, p.d_head, (int64_t)p.B * p.H * p.N, 0) ||
+      !make_map(&mk, ws + L.kp, p.d_head, (int64_t)p.B * p.H_kv * p.N, 0) ||
+      !make_map(&mv, ws + L.vp, p.d_head, (int64_t)p.B * p.H_kv * p.N, 0))
+    return cudaErrorInvalidValue;
+  dim3 grid((unsigned)((int64_t)a.qtab_cap * (p.H / p.R)));
+  return p.d_head == 64 ? launch_tc<64, true>(mq, mk, mv, a, grid, s)
+                        : launch_tc<128, true>(mq, mk, mv, a, grid, s);
+}
+
+cudaError_t launch_attn_window_tc(const focus_params& p, const WsLayout& L, const bf16* q,
+                                  const bf16* k, const bf16* v, char* ws, bf16* o, float* lse,
+                                  float scale, cudaStream_t s) {
+  TcArgs a = make_args(p, L, ws, scale);
+  a.o = o;
+  a.lse = lse;
+  CUtensorMap mq, mk, mv;
+  if (!make_map(&mq, q, p.d_head, (int64_t)p.B * p.N, p.H) ||
+      !make_map(&mk, k, p.d_head, (int64_t)p.B * p.N, p.H_kv) ||
+      !make_map(&mv, v, p.d_head, (int64_t)p.B * p.N, p.H_kv))
+    return cudaErrorInvalidValue;
+  dim3 grid((p.N + BMQ - 1) / BMQ, p.H, p.B);
+  return p.d_head == 64 ? launch_tc<64, false>(mq, mk, mv, a, grid, s)
+                        : launch_tc<128, false>(mq, mk, mv, a, grid, s);
+}
+
+}  // namespace focus

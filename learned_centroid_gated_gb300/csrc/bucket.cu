@@ -135,14 +135,14 @@ bucket_scatter(int N, int K, int top_k, int nseg, const uint32_t* __restrict__ m
   }
 }
 
-// Long-range schedule: one entry per query block of kAttnBM rows inside a segment,
+// Long-range schedule: one entry per query block of bm rows inside a segment,
 // ordered by descending position of the block's last row (the blocks with the most
 // candidate keys start first).  Single CTA.
 constexpr int kTabThreads = 1024;
 constexpr int kTabBuckets = 4096;
 
 __global__ void __launch_bounds__(kTabThreads)
-build_qtab(int N, int nseg, int BR, const int* __restrict__ seg_off, const int* __restrict__ perm,
+build_qtab(int N, int nseg, int BR, int bm, const int* __restrict__ seg_off, const int* __restrict__ perm,
            int* __restrict__ entoff, QBlock* __restrict__ qtab, int* __restrict__ qtab_count) {
   __shared__ int bucket[kTabBuckets];
   __shared__ int wsum[32];
@@ -159,7 +159,7 @@ build_qtab(int N, int nseg, int BR, const int* __restrict__ seg_off, const int* 
       const int br = it / nseg, s = it % nseg;
       const int* so = seg_off + (int64_t)br * (nseg + 1);
       const int cnt = so[s + 1] - so[s];
-      c = (cnt + kAttnBM - 1) / kAttnBM;
+      c = (cnt + bm - 1) / bm;
     }
     int x = c;
     for (int o = 1; o < 32; o <<= 1) {
@@ -204,8 +204,8 @@ build_qtab(int N, int nseg, int BR, const int* __restrict__ seg_off, const int* 
       const int t = e - entoff[lo];
       const int* so = seg_off + (int64_t)br * (nseg + 1);
       const int cnt = so[s + 1] - so[s];
-      const int row0 = so[s] + t * kAttnBM;
-      const int rows = min(kAttnBM, cnt - t * kAttnBM);
+      const int row0 = so[s] + t * bm;
+      const int rows = min(bm, cnt - t * bm);
       const int last = perm[(int64_t)br * N + row0 + rows - 1];
       const int key = (N - 1 - last) >> shift;
       if (pass == 0) {
@@ -294,11 +294,11 @@ cudaError_t launch_bucket(const focus_params& p, const WsLayout& L, const uint32
   return cudaGetLastError();
 }
 
-cudaError_t launch_qtab(const focus_params& p, const WsLayout& L, const uint32_t* mask, char* ws,
+cudaError_t launch_qtab(const focus_params& p, const WsLayout& L, char* ws, int block_rows,
                         cudaStream_t s) {
-  (void)mask;
   WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
-  build_qtab<<<1, kTabThreads, 0, s>>>(p.N, L.nseg, p.B * p.R, reinterpret_cast<int*>(ws + L.segoff),
+  build_qtab<<<1, kTabThreads, 0, s>>>(p.N, L.nseg, p.B * p.R, block_rows,
+                                       reinterpret_cast<int*>(ws + L.segoff),
                                        reinterpret_cast<int*>(ws + L.perm),
                                        reinterpret_cast<int*>(ws + L.entoff),
                                        reinterpret_cast<QBlock*>(ws + L.qtab), &hdr->qtab_count);

@@ -28,7 +28,7 @@ struct QBlock {
 
 constexpr int kChunk = 1024;      // tokens per bucketing chunk (one warp)
 constexpr int kSinkBlock = 256;   // tokens per Sinkhorn partial-reduction block
-constexpr int kAttnBM = 128;      // query rows per attention CTA
+constexpr int kAttnBM = 128;      // smallest query block of the long-range schedule
 constexpr int kKeySentinel = 0x7fffffff;
 
 struct WsLayout {
@@ -58,11 +58,18 @@ cudaError_t launch_route(const focus_params& p, const WsLayout& L, const float* 
 // bucket.cu
 cudaError_t launch_bucket(const focus_params& p, const WsLayout& L, const uint32_t* mask, char* ws,
                           cudaStream_t s);
-cudaError_t launch_qtab(const focus_params& p, const WsLayout& L, const uint32_t* mask, char* ws,
+cudaError_t launch_qtab(const focus_params& p, const WsLayout& L, char* ws, int block_rows,
                         cudaStream_t s);
 cudaError_t launch_permute(const focus_params& p, const WsLayout& L, const bf16* q, const bf16* k,
                            const bf16* v, char* ws, cudaStream_t s);
-// attn.cu
+// attn_tc.cu (tcgen05 engine)
+int tc_block_rows();
+cudaError_t launch_attn_long_tc(const focus_params& p, const WsLayout& L, const uint32_t* mask,
+                                char* ws, float scale, cudaStream_t s);
+cudaError_t launch_attn_window_tc(const focus_params& p, const WsLayout& L, const bf16* q,
+                                  const bf16* k, const bf16* v, char* ws, bf16* o, float* lse,
+                                  float scale, cudaStream_t s);
+// attn.cu (mma.sync engine)
 cudaError_t launch_attn_long(const focus_params& p, const WsLayout& L, const uint32_t* mask,
                              char* ws, float scale, cudaStream_t s);
 cudaError_t launch_attn_window(const focus_params& p, const WsLayout& L, const bf16* q,
