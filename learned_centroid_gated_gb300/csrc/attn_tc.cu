@@ -394,20 +394,32 @@ attn_tc(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensor
       tie32(x1);
       tie32(x2);
       tie32(x3);
-      float mx = -INFINITY;
-      auto scale_mask = [&](uint32_t(&x)[32], int cb) {
+      // mask (raw logits; the scale is positive, so the max commutes with it)
+      if (need_mask) {
+        const uint32_t width = (uint32_t)max(c_hi - c_lo, 0);
+        auto mask32 = [&](uint32_t(&x)[32], int cb) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          float v = __uint_as_float(x[i]) * a.sl2;
-          if (need_mask && (cb + i < c_lo || cb + i >= c_hi)) v = -INFINITY;
-          x[i] = __float_as_uint(v);
-          mx = fmaxf(mx, v);
+          for (int i = 0; i < 32; ++i)
+            if ((uint32_t)(cb + i - c_lo) >= width) x[i] = 0xff800000u;  // -inf
+        };
+        mask32(x0, 0);
+        mask32(x1, 32);
+        mask32(x2, 64);
+        mask32(x3, 96);
+      }
+      float ma = -INFINITY, mb = -INFINITY;
+      auto max32 = [&](uint32_t(&x)[32]) {
+#pragma unroll
+        for (int i = 0; i < 32; i += 4) {
+          ma = max3(ma, __uint_as_float(x[i]), __uint_as_float(x[i + 1]));
+          mb = max3(mb, __uint_as_float(x[i + 2]), __uint_as_float(x[i + 3]));
         }
       };
-      scale_mask(x0, 0);
-      scale_mask(x1, 32);
-      scale_mask(x2, 64);
-      scale_mask(x3, 96);
+      max32(x0);
+      max32(x1);
+      max32(x2);
+      max32(x3);
+      const float mx = fmaxf(ma, mb) * a.sl2;
       float f = 1.0f;
       const bool rescale = mx > m_use + kRescale;
       if (rescale) {
@@ -415,14 +427,17 @@ attn_tc(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensor
         l *= f;
         m_use = mx;
       }
-      const float ms = (m_use == -INFINITY) ? 0.0f : m_use;
+      const float nms = (m_use == -INFINITY) ? 0.0f : -m_use;
+      const float sl2 = a.sl2;
+      float la = 0.0f, lb = 0.0f;
       auto emit = [&](uint32_t(&x)[32], int k) {
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float p0 = ex2(__uint_as_float(x[2 * i]) - ms);
-          const float p1 = ex2(__uint_as_float(x[2 * i + 1]) - ms);
-          l += p0 + p1;
+          float y0, y1;
+          ffma2(y0, y1, __uint_as_float(x[2 * i]), __uint_as_float(x[2 * i + 1]), sl2, sl2, nms, nms);
+          const float p0 = ex2(y0), p1 = ex2(y1);
+          fadd2(la, lb, la, lb, p0, p1);
           pk[i] = pack_bf16(p0, p1);
         }
 #pragma unroll
@@ -436,6 +451,7 @@ attn_tc(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensor
       emit(x1, 1);
       emit(x2, 2);
       emit(x3, 3);
+      l += la + lb;
       // O (from PV of earlier tiles, all complete once S of this tile is) follows the
       // new maximum; skipped while this row has seen no key (O is still zero then).
       if (__any_sync(0xffffffffu, rescale && t > 0 && f != 0.0f)) {
