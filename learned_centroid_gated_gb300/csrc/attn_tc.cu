@@ -9,16 +9,22 @@
 // softmax is the log-sum-exp merge of two partial softmaxes; every key is
 // visited once because tokens are bucketed by their exact group set.
 //
-// One CTA = 256 query rows of one head, as two 128-row tiles A and B that
-// ping-pong on the tensor core:
-//   warp 8     TMA producer: Q tiles once, then K and V tiles through a 3-slot ring
-//   warp 9     MMA issuer (one thread): S = Q K^T into TMEM, O += P V into TMEM
-//   warps 0-3  softmax of tile A (thread = row = TMEM lane), warps 4-7 of tile B
+// Persistent kernel: one CTA per SM walks a static round-robin share of the work
+// items (query blocks of 256 rows of one head).  Each item is two 128-row query
+// tiles A and B that ping-pong on the tensor core:
+//   warp 8      TMA producer: Q tiles of each item, then K and V tiles through a
+//               3-slot ring; runs ahead across item boundaries
+//   warp 9      MMA issuer (one thread): S = Q K^T into TMEM, O += P V into TMEM
+//   warps 0-3   softmax of tile A (thread = row = TMEM lane), warps 4-7 of tile B;
+//               each warpgroup also writes its tile's output rows
+//   warps 10-11 idle (they complete the third warpgroup for the register split)
 // TMEM (512 columns): S_A | S_B | O_A | O_B.  P goes to shared memory in the
 // 128-byte-swizzled K-major layout the MMA reads.  Issue order on the tensor
 // core: S_A(0) S_B(0) | PV_A(t) S_A(t+1) PV_B(t) S_B(t+1) | ..., so the softmax of
 // one tile runs while the tensor core works on the other.  The running max is
 // rescaled lazily (only when it grows by more than 2^8), in place in TMEM.
+// Barrier phases run on across items; a tile's P barrier also orders the previous
+// item's reads of O before the next item's first P V.
 //
 //   attn_tc<D, true>   long-range part: query block of one segment x the key
 //                      tiles of every compatible segment (permuted copies),
@@ -37,17 +43,22 @@ namespace {
 
 using namespace ptx;
 
-constexpr int QT = 128;       // rows per query tile (MMA M)
-constexpr int BMQ = 2 * QT;   // query rows per CTA
-constexpr int BNK = 128;      // keys per tile (MMA N of S, K of PV)
-constexpr int NSTAGE = 3;     // K/V ring slots
-constexpr int NTHREADS = 320;
+constexpr int QT = 128;        // rows per query tile (MMA M)
+constexpr int BMQ = 2 * QT;    // query rows per work item
+constexpr int BNK = kKeyTile;  // keys per tile (MMA N of S, K of P V)
+constexpr int NSTAGE = 3;      // K/V ring slots
+constexpr int NTHREADS = 384;
 constexpr int PRODUCER_WARP = 8;
 constexpr int MMA_WARP = 9;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescale = 8.0f;  // log2 units: rescale O only when the max grows by > 2^8
+// Register split after launch (384 threads x 168): warpgroup 2 (producer, MMA,
+// idle) drops to 104, the two softmax warpgroups rise to 192:
+// 128 * 104 + 256 * 192 = 62464 <= 384 * 168 = 64512.
+constexpr int kRegsLow = 104;
+constexpr int kRegsHigh = 192;
 
 template <int D>
 struct Layout {
@@ -66,10 +77,10 @@ struct TcArgs {
   int B, N, H, H_kv, R, w, nseg, qtab_cap;
   float sl2;  // softmax scale * log2(e)
   const int* perm;
-  const int* seg_off;
-  const uint32_t* mask;
   const QBlock* qtab;
   const int* qtab_count;
+  const PlanHead* plan_head;
+  const PlanEnt* plan_ent;
   float* o_lr;
   float* lse_lr;
   bf16* o;
@@ -86,119 +97,92 @@ __device__ __forceinline__ int upper_bound_g(const int* __restrict__ P, int lo, 
   return lo;
 }
 
-// Long-range key segments of one query block.
-struct SegCtx {
-  const int* P;       // permuted token positions of this (b, rho)
-  const int* SO;      // segment offsets of this (b, rho)
-  const uint32_t* M;  // masks of this (b, rho)
-  int nseg, w, p_lo, p_hi;
-  uint32_t mS;
-};
-struct SegTile {
-  int start, cnt, nfull;
-};
-
-// Next segment T' >= T whose mask meets the query segment's and that holds keys
-// with pos <= p_hi - w; cnt counts those keys, nfull the leading tiles whose keys
-// all satisfy pos <= p_lo - w (no masking needed).
-__device__ bool next_seg(const SegCtx& c, int& T, SegTile& st) {
-  for (; T < c.nseg; ++T) {
-    const int s0 = __ldg(c.SO + T), s1 = __ldg(c.SO + T + 1);
-    if (s1 <= s0) continue;
-    const uint32_t mT = __ldg(c.M + __ldg(c.P + s0));
-    if (!(mT & c.mS)) continue;
-    const int hi = upper_bound_g(c.P, s0, s1, c.p_hi - c.w) - s0;
-    if (hi <= 0) continue;
-    st.start = s0;
-    st.cnt = hi;
-    st.nfull = (upper_bound_g(c.P, s0, s1, c.p_lo - c.w) - s0) / BNK;
-    ++T;
-    return true;
-  }
-  return false;
-}
-
-struct TileIt {
-  int T;
-  int t_in;
-  bool valid;
-  SegTile st;
-  __device__ void init(const SegCtx& c) {
-    T = 0;
-    t_in = 0;
-    valid = next_seg(c, T, st);
-  }
-  __device__ void advance(const SegCtx& c) {
-    if (++t_in * BNK >= st.cnt) {
-      t_in = 0;
-      valid = next_seg(c, T, st);
-    }
-  }
-};
-
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsHigh));
+}
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow));
+}
+
+// One work item: a 256-row query block of one head.
+struct Item {
+  bool valid;
+  int b, h, kvh, rows, row0;  // row0: first permuted row (long) or first token (window)
+  int n;                      // key tiles
+  int u;                      // long: schedule entry
+  int br;                     // long: b * R + rho
+  int j_lo, j_hi;             // window key range
+};
+
+template <bool LONG>
+__device__ __forceinline__ Item decode(const TcArgs& a, int x) {
+  Item it{};
+  if constexpr (LONG) {
+    // Heads sharing a KV head are adjacent, then the schedule entries (heaviest
+    // first), then the KV heads of a routing head: co-resident CTAs share K/V in L2.
+    const int gq = a.H / a.H_kv, nkv = a.H_kv / a.R;
+    const int jq = x % gq;
+    const int rest = x / gq;
+    const int u = rest % a.qtab_cap, kvl = rest / a.qtab_cap;
+    it.valid = u < *a.qtab_count;
+    if (!it.valid) return it;
+    const QBlock e = a.qtab[u];
+    it.u = u;
+    it.br = e.br;
+    it.b = e.br / a.R;
+    const int rho = e.br % a.R;
+    it.kvh = rho * nkv + kvl;
+    it.h = it.kvh * gq + jq;
+    it.rows = e.rows;
+    it.row0 = e.row0;
+    it.n = a.plan_head[u].n_tiles;
+  } else {
+    const int nqb = (a.N + BMQ - 1) / BMQ;
+    const int qb = x % nqb;
+    const int bh = x / nqb;
+    it.valid = true;
+    it.h = bh % a.H;
+    it.b = bh / a.H;
+    it.kvh = it.h / (a.H / a.H_kv);
+    it.row0 = qb * BMQ;
+    it.rows = min(BMQ, a.N - it.row0);
+    it.j_lo = max(0, it.row0 - a.w + 1);
+    it.j_hi = it.row0 + it.rows;
+    it.n = (it.j_hi - it.j_lo + BNK - 1) / BNK;
+  }
+  return it;
+}
+
 template <int D, bool LONG>
 __global__ void __launch_bounds__(NTHREADS, 1)
 attn_tc(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
-        const __grid_constant__ CUtensorMap mv, const TcArgs a) {
+        const __grid_constant__ CUtensorMap mv, const TcArgs a, const int n_items) {
   using L = Layout<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-  // ---- the query block of this CTA ----
-  int b, h, kvh, rows, q_row0;
-  SegCtx sc{};
-  if constexpr (LONG) {
-    const int gq = a.H / a.H_kv, nkv = a.H_kv / a.R;
-    const int jq = blockIdx.x % gq;
-    const int rest = blockIdx.x / gq;
-    const int u = rest % a.qtab_cap, kvl = rest / a.qtab_cap;
-    if (u >= *a.qtab_count) return;
-    const QBlock e = a.qtab[u];
-    b = e.br / a.R;
-    const int rho = e.br % a.R;
-    kvh = rho * nkv + kvl;
-    h = kvh * gq + jq;
-    rows = e.rows;
-    q_row0 = e.row0;
-    sc.P = a.perm + (int64_t)e.br * a.N;
-    sc.SO = a.seg_off + (int64_t)e.br * (a.nseg + 1);
-    sc.M = a.mask + (int64_t)e.br * a.N;
-    sc.nseg = a.nseg;
-    sc.w = a.w;
-    sc.p_lo = __ldg(sc.P + e.row0);
-    sc.p_hi = __ldg(sc.P + e.row0 + rows - 1);
-    sc.mS = __ldg(sc.M + sc.p_lo);
-  } else {
-    q_row0 = blockIdx.x * BMQ;
-    h = blockIdx.y;
-    b = blockIdx.z;
-    kvh = h / (a.H / a.H_kv);
-    rows = min(BMQ, a.N - q_row0);
-  }
-  const int j_lo = LONG ? 0 : max(0, q_row0 - a.w + 1);
-  const int j_hi = LONG ? 0 : q_row0 + rows;
-
   uint8_t* bar = sm + L::BAR;
-  const uint32_t b_q = smem_u32(bar);
-  const uint32_t b_full = b_q + 8, b_empty = b_q + 32;  // + 8 * stage
-  const uint32_t b_s = b_q + 56, b_p = b_q + 72, b_o = b_q + 88;  // + 8 * tile
-  const uint32_t b_drain = b_q + 104;
-  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(bar + 112);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(bar + 116);
-  volatile int* ntiles_s = reinterpret_cast<volatile int*>(bar + 120);
+  const uint32_t b_q = smem_u32(bar);                    // Q tiles landed
+  const uint32_t b_qe = b_q + 8;                         // Q buffer free (last S of an item done)
+  const uint32_t b_full = b_q + 16, b_empty = b_q + 40;  // + 8 * stage
+  const uint32_t b_s = b_q + 64, b_p = b_q + 80, b_o = b_q + 96;  // + 8 * query tile
+  const uint32_t b_drain = b_q + 112;
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(bar + 120);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bar + 124);
 
   if (warp == MMA_WARP) {
-    tmem_alloc(smem_u32(bar + 112), TMEM_COLS);
+    tmem_alloc(smem_u32(bar + 120), TMEM_COLS);
     tmem_relinquish();
   }
   if (tid == 0) {
     mbar_init(b_q, 1);
+    mbar_init(b_qe, 1);
     for (int s = 0; s < NSTAGE; ++s) {
       mbar_init(b_full + 8 * s, 1);
       mbar_init(b_empty + 8 * s, 1);
@@ -210,15 +194,6 @@ attn_tc(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensor
     }
     mbar_init(b_drain, 1);
     *abort_flag = 0;
-    int n = 0;
-    if constexpr (LONG) {
-      int T = 0;
-      SegTile st;
-      while (next_seg(sc, T, st)) n += (st.cnt + BNK - 1) / BNK;
-    } else {
-      n = (j_hi - j_lo + BNK - 1) / BNK;
-    }
-    *ntiles_s = n;
     fence_barrier_init();
     fence_proxy_async_smem();
   }
@@ -226,66 +201,75 @@ attn_tc(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensor
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int n = *ntiles_s;
   int* status = a.status;
 
-  if (warp == PRODUCER_WARP) {
-    // ------------------------------------------------------------- producer --
-    if (lane == 0 && n > 0) {
+  if (warp >= 8) {
+    setmaxnreg_dec();
+    if (warp == PRODUCER_WARP && lane == 0) {
+      // ----------------------------------------------------------- producer --
       tma_prefetch(&mq);
       tma_prefetch(&mk);
       tma_prefetch(&mv);
-      mbar_expect_tx(b_q, 2 * L::TILE);
-      for (int qt = 0; qt < 2; ++qt)
-        for (int bx = 0; bx < L::BOXES; ++bx) {
-          const uint32_t dst = smem_u32(sm + L::Q + qt * L::TILE + bx * L::BOX);
-          if constexpr (LONG)
-            tma_load_2d(dst, &mq, 64 * bx, ((b * a.H + h) * a.N) + q_row0 + qt * QT, b_q);
-          else
-            tma_load_3d(dst, &mq, 64 * bx, h, b * a.N + q_row0 + qt * QT, b_q);
-        }
       int last_par[NSTAGE];
       for (int s = 0; s < NSTAGE; ++s) last_par[s] = -1;
-      int stage = 0;
+      int stage = 0, qcnt = 0, q_par = -1;
       uint32_t phase = 0;
-      TileIt it;
-      if constexpr (LONG) it.init(sc);
       bool ok = true;
-      for (int t = 0; t < n && ok; ++t) {
-        int row;
-        if constexpr (LONG) row = (b * a.H_kv + kvh) * a.N + it.st.start + it.t_in * BNK;
-        else row = b * a.N + j_lo + t * BNK;
-        for (int kv = 0; kv < 2; ++kv) {
-          if (!mbar_wait(b_empty + 8 * stage, phase ^ 1, abort_flag, status)) {
-            ok = false;
-            break;
-          }
-          const uint32_t full = b_full + 8 * stage;
-          mbar_expect_tx(full, L::TILE);
+      for (int x = blockIdx.x; ok && x < n_items; x += gridDim.x) {
+        const Item it = decode<LONG>(a, x);
+        if (!it.valid || it.n == 0) continue;
+        if (!(ok = mbar_wait(b_qe, (qcnt & 1) ^ 1, abort_flag, status))) break;
+        mbar_expect_tx(b_q, 2 * L::TILE);
+        for (int qt = 0; qt < 2; ++qt)
           for (int bx = 0; bx < L::BOXES; ++bx) {
-            const uint32_t dst = smem_u32(sm + L::RING + stage * L::TILE + bx * L::BOX);
-            const CUtensorMap* m = kv ? &mv : &mk;
-            if constexpr (LONG) tma_load_2d(dst, m, 64 * bx, row, full);
-            else tma_load_3d(dst, m, 64 * bx, kvh, row, full);
+            const uint32_t dst = smem_u32(sm + L::Q + qt * L::TILE + bx * L::BOX);
+            if constexpr (LONG)
+              tma_load_2d(dst, &mq, 64 * bx, (it.b * a.H + it.h) * a.N + it.row0 + qt * QT, b_q);
+            else
+              tma_load_3d(dst, &mq, 64 * bx, it.h, it.b * a.N + it.row0 + qt * QT, b_q);
           }
-          last_par[stage] = (int)phase;
-          if (++stage == NSTAGE) {
-            stage = 0;
-            phase ^= 1;
+        q_par = qcnt & 1;
+        ++qcnt;
+        // key tiles: long = each plan entry's tiles in order; window = consecutive
+        int e = 0, t_in = 0;
+        PlanEnt pe{};
+        if constexpr (LONG) pe = a.plan_ent[(int64_t)it.u * a.nseg];
+        for (int t = 0; t < it.n && ok; ++t) {
+          int row;
+          if constexpr (LONG) {
+            row = (it.b * a.H_kv + it.kvh) * a.N + pe.start + t_in * BNK;
+            if (++t_in * BNK >= pe.cnt && ++e < a.nseg) {
+              t_in = 0;
+              pe = a.plan_ent[(int64_t)it.u * a.nseg + e];
+            }
+          } else {
+            row = it.b * a.N + it.j_lo + t * BNK;
+          }
+          for (int kv = 0; kv < 2; ++kv) {
+            if (!(ok = mbar_wait(b_empty + 8 * stage, phase ^ 1, abort_flag, status))) break;
+            const uint32_t full = b_full + 8 * stage;
+            mbar_expect_tx(full, L::TILE);
+            for (int bx = 0; bx < L::BOXES; ++bx) {
+              const uint32_t dst = smem_u32(sm + L::RING + stage * L::TILE + bx * L::BOX);
+              const CUtensorMap* m = kv ? &mv : &mk;
+              if constexpr (LONG) tma_load_2d(dst, m, 64 * bx, row, full);
+              else tma_load_3d(dst, m, 64 * bx, it.kvh, row, full);
+            }
+            last_par[stage] = (int)phase;
+            if (++stage == NSTAGE) {
+              stage = 0;
+              phase ^= 1;
+            }
           }
         }
-        if constexpr (LONG) it.advance(sc);
       }
       if (*abort_flag) {  // let every copy in flight land before the CTA exits
-        mbar_drain(b_q, 0);
+        if (q_par >= 0) mbar_drain(b_q, (uint32_t)q_par);
         for (int s = 0; s < NSTAGE; ++s)
           if (last_par[s] >= 0) mbar_drain(b_full + 8 * s, (uint32_t)last_par[s]);
       }
-    }
-    __syncwarp();
-  } else if (warp == MMA_WARP) {
-    // ------------------------------------------------------------ MMA issue --
-    if (lane == 0 && n > 0) {
+    } else if (warp == MMA_WARP && lane == 0) {
+      // ---------------------------------------------------------- MMA issue --
       constexpr uint32_t IS = idesc_bf16(QT, BNK, 0);  // S = Q K^T, both K-major
       constexpr uint32_t IPV = idesc_bf16(QT, D, 1);   // O += P V, V MN-major
       const uint32_t q_base = smem_u32(sm + L::Q);
@@ -311,175 +295,203 @@ attn_tc(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensor
                   sw128_desc(vaddr + kk * 2048, L::BOX, 1024), IPV, (acc || kk > 0) ? 1u : 0u);
         }
       };
-      bool ok = mbar_wait(b_q, 0, abort_flag, status) && ring_wait(0);
-      if (ok) {
+      int ri = 0, gt = 0, qcnt = 0;
+      bool ok = true;
+      for (int x = blockIdx.x; ok && x < n_items; x += gridDim.x) {
+        const Item it = decode<LONG>(a, x);
+        if (!it.valid || it.n == 0) continue;
+        const int n = it.n;
+        if (!(ok = mbar_wait(b_q, qcnt & 1, abort_flag, status) && ring_wait(ri))) break;
+        ++qcnt;
         tc_fence_after();
-        issue_S(0, slot(0));
+        issue_S(0, slot(ri));
         umma_commit(b_s);
-        issue_S(1, slot(0));
+        issue_S(1, slot(ri));
         umma_commit(b_s + 8);
-        umma_commit(b_empty + 8 * (0 % NSTAGE));
-      }
-      for (int t = 0; ok && t < n; ++t) {
-        const int iv = 2 * t + 1, ik = 2 * t + 2;
-        if (!(ok = ring_wait(iv) && mbar_wait(b_p, t & 1, abort_flag, status))) break;
-        tc_fence_after();
-        issue_PV(0, slot(iv), t > 0);
-        umma_commit(b_o);
-        if (t + 1 < n) {
-          if (!(ok = ring_wait(ik))) break;
+        umma_commit(b_empty + 8 * (ri % NSTAGE));
+        if (n == 1) umma_commit(b_qe);
+        for (int t = 0; t < n; ++t) {
+          const int iv = ri + 2 * t + 1, ik = ri + 2 * t + 2;
+          const uint32_t par = (uint32_t)((gt + t) & 1);
+          if (!(ok = ring_wait(iv) && mbar_wait(b_p, par, abort_flag, status))) break;
           tc_fence_after();
-          issue_S(0, slot(ik));
-          umma_commit(b_s);
+          issue_PV(0, slot(iv), t > 0);
+          umma_commit(b_o);
+          if (t + 1 < n) {
+            if (!(ok = ring_wait(ik))) break;
+            tc_fence_after();
+            issue_S(0, slot(ik));
+            umma_commit(b_s);
+          }
+          if (!(ok = mbar_wait(b_p + 8, par, abort_flag, status))) break;
+          tc_fence_after();
+          issue_PV(1, slot(iv), t > 0);
+          umma_commit(b_o + 8);
+          umma_commit(b_empty + 8 * (iv % NSTAGE));
+          if (t + 1 < n) {
+            issue_S(1, slot(ik));
+            umma_commit(b_s + 8);
+            umma_commit(b_empty + 8 * (ik % NSTAGE));
+            if (t + 2 == n) umma_commit(b_qe);  // last S of this item issued
+          }
         }
-        if (!(ok = mbar_wait(b_p + 8, t & 1, abort_flag, status))) break;
-        tc_fence_after();
-        issue_PV(1, slot(iv), t > 0);
-        umma_commit(b_o + 8);
-        umma_commit(b_empty + 8 * (iv % NSTAGE));
-        if (t + 1 < n) {
-          issue_S(1, slot(ik));
-          umma_commit(b_s + 8);
-          umma_commit(b_empty + 8 * (ik % NSTAGE));
-        }
+        ri += 2 * n;
+        gt += n;
       }
       umma_commit(b_drain);  // every MMA issued above completes before TMEM is released
       mbar_drain(b_drain, 0);
     }
     __syncwarp();
   } else {
+    setmaxnreg_inc();
     // -------------------------------------------------------------- softmax --
     const int qt = warp >> 2;
     const int r = (warp & 3) * 32 + lane;  // row in the tile = TMEM lane
-    const int rg = qt * QT + r;            // row in the CTA block
-    const bool row_ok = rg < rows;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + lane_off + qt * BNK;
     const uint32_t tO = tmem + lane_off + 2 * BNK + qt * D;
-    int qp;
-    if constexpr (LONG) qp = __ldg(sc.P + q_row0 + min(rg, rows - 1));
-    else qp = q_row0 + min(rg, rows - 1);
     uint8_t* prow = sm + L::P + qt * L::PBYTES + r * 128;
     const int rsw = r & 7;
-    float m_use = -INFINITY, l = 0.0f;
-    TileIt it;
-    if constexpr (LONG) it.init(sc);
+    const float sl2 = a.sl2;
+    int gt = 0;
     bool ok = true;
-    for (int t = 0; t < n; ++t) {
-      int c_lo = 0, c_hi = BNK;
-      bool need_mask;
+    for (int x = blockIdx.x; ok && x < n_items; x += gridDim.x) {
+      const Item it = decode<LONG>(a, x);
+      if (!it.valid) continue;
+      const int n = it.n;
+      const int rg = qt * QT + r;  // row in the item
+      const bool row_ok = rg < it.rows;
+      const int* P = LONG ? a.perm + (int64_t)it.br * a.N : nullptr;
+      int qp;
+      if constexpr (LONG) qp = __ldg(P + it.row0 + min(rg, it.rows - 1));
+      else qp = it.row0 + min(rg, it.rows - 1);
+      float m_use = -INFINITY, l = 0.0f;
+      int e = 0, t_in = 0;
+      PlanEnt pe{};
       if constexpr (LONG) {
-        const int valid = min(BNK, it.st.cnt - it.t_in * BNK);
-        need_mask = it.t_in >= it.st.nfull;
-        if (need_mask) c_hi = upper_bound_g(sc.P + it.st.start + it.t_in * BNK, 0, valid, qp - a.w);
-        it.advance(sc);
-      } else {
-        const int j0 = j_lo + t * BNK;
-        c_lo = max(0, qp - a.w + 1 - j0);
-        c_hi = min(min(BNK, j_hi - j0), qp - j0 + 1);
-        need_mask = c_lo > 0 || c_hi < BNK;
+        if (n > 0) pe = a.plan_ent[(int64_t)it.u * a.nseg];
       }
-      ok = mbar_wait(b_s + 8 * qt, t & 1, abort_flag, status);
-      if (!__all_sync(0xffffffffu, ok)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      uint32_t x0[32], x1[32], x2[32], x3[32];
-      tmem_ld32(tS + 0, x0);
-      tmem_ld32(tS + 32, x1);
-      tmem_ld32(tS + 64, x2);
-      tmem_ld32(tS + 96, x3);
-      tmem_ld_wait(x0);
-      tie32(x1);
-      tie32(x2);
-      tie32(x3);
-      // mask (raw logits; the scale is positive, so the max commutes with it)
-      if (need_mask) {
-        const uint32_t width = (uint32_t)max(c_hi - c_lo, 0);
-        auto mask32 = [&](uint32_t(&x)[32], int cb) {
+      for (int t = 0; t < n; ++t) {
+        int c_lo = 0, c_hi = BNK;
+        bool need_mask;
+        if constexpr (LONG) {
+          const int valid = min(BNK, pe.cnt - t_in * BNK);
+          need_mask = t_in >= pe.nfull;
+          if (need_mask) c_hi = upper_bound_g(P + pe.start + t_in * BNK, 0, valid, qp - a.w);
+          if (++t_in * BNK >= pe.cnt && ++e < a.nseg) {
+            t_in = 0;
+            pe = a.plan_ent[(int64_t)it.u * a.nseg + e];
+          }
+        } else {
+          const int j0 = it.j_lo + t * BNK;
+          c_lo = max(0, qp - a.w + 1 - j0);
+          c_hi = min(min(BNK, it.j_hi - j0), qp - j0 + 1);
+          need_mask = c_lo > 0 || c_hi < BNK;
+        }
+        ok = mbar_wait(b_s + 8 * qt, (uint32_t)((gt + t) & 1), abort_flag, status);
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t x0[32], x1[32], x2[32], x3[32];
+        tmem_ld32(tS + 0, x0);
+        tmem_ld32(tS + 32, x1);
+        tmem_ld32(tS + 64, x2);
+        tmem_ld32(tS + 96, x3);
+        tmem_ld_wait(x0);
+        tie32(x1);
+        tie32(x2);
+        tie32(x3);
+        // mask (raw logits; the scale is positive, so the max commutes with it)
+        if (need_mask) {
+          const uint32_t width = (uint32_t)max(c_hi - c_lo, 0);
+          auto mask32 = [&](uint32_t(&xx)[32], int cb) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if ((uint32_t)(cb + i - c_lo) >= width) x[i] = 0xff800000u;  // -inf
+            for (int i = 0; i < 32; ++i)
+              if ((uint32_t)(cb + i - c_lo) >= width) xx[i] = 0xff800000u;  // -inf
+          };
+          mask32(x0, 0);
+          mask32(x1, 32);
+          mask32(x2, 64);
+          mask32(x3, 96);
+        }
+        float ma = -INFINITY, mb = -INFINITY;
+        auto max32 = [&](uint32_t(&xx)[32]) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 4) {
+            ma = max3(ma, __uint_as_float(xx[i]), __uint_as_float(xx[i + 1]));
+            mb = max3(mb, __uint_as_float(xx[i + 2]), __uint_as_float(xx[i + 3]));
+          }
         };
-        mask32(x0, 0);
-        mask32(x1, 32);
-        mask32(x2, 64);
-        mask32(x3, 96);
+        max32(x0);
+        max32(x1);
+        max32(x2);
+        max32(x3);
+        const float mx = fmaxf(ma, mb) * sl2;
+        float f = 1.0f;
+        const bool rescale = mx > m_use + kRescale;
+        if (rescale) {
+          f = ex2(m_use - mx);  // 0 when m_use is -inf
+          l *= f;
+          m_use = mx;
+        }
+        const float nms = (m_use == -INFINITY) ? 0.0f : -m_use;
+        float la = 0.0f, lb = 0.0f;
+        auto emit = [&](uint32_t(&xx)[32], int k) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            float y0, y1;
+            ffma2(y0, y1, __uint_as_float(xx[2 * i]), __uint_as_float(xx[2 * i + 1]), sl2, sl2, nms, nms);
+            const float p0 = ex2(y0), p1 = ex2(y1);
+            fadd2(la, lb, la, lb, p0, p1);
+            pk[i] = pack_bf16(p0, p1);
+          }
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int cidx = 4 * k + q;  // 16-byte chunk (8 keys) index 0..15
+            uint8_t* dst = prow + (cidx >> 3) * L::BOX + (((cidx & 7) ^ rsw) << 4);
+            *reinterpret_cast<uint4*>(dst) = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+          }
+        };
+        emit(x0, 0);
+        emit(x1, 1);
+        emit(x2, 2);
+        emit(x3, 3);
+        l += la + lb;
+        // O (from P V of earlier tiles, all complete once S of this tile is) follows
+        // the new maximum; skipped while this row has seen no key (O is still zero).
+        if (__any_sync(0xffffffffu, rescale && t > 0 && f != 0.0f)) {
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t y[32];
+            tmem_ld32(tO + 32 * c, y);
+            tmem_ld_wait(y);
+            const float g = (rescale && t > 0) ? f : 1.0f;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) y[i] = __float_as_uint(__uint_as_float(y[i]) * g);
+            tmem_st32(tO + 32 * c, y);
+          }
+          tmem_st_wait();
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(b_p + 8 * qt);
       }
-      float ma = -INFINITY, mb = -INFINITY;
-      auto max32 = [&](uint32_t(&x)[32]) {
-#pragma unroll
-        for (int i = 0; i < 32; i += 4) {
-          ma = max3(ma, __uint_as_float(x[i]), __uint_as_float(x[i + 1]));
-          mb = max3(mb, __uint_as_float(x[i + 2]), __uint_as_float(x[i + 3]));
+      if (!ok) break;
+      // ---- epilogue of this item ----
+      if (n > 0) {
+        ok = mbar_wait(b_o + 8 * qt, (uint32_t)((gt + n - 1) & 1), abort_flag, status);
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
         }
-      };
-      max32(x0);
-      max32(x1);
-      max32(x2);
-      max32(x3);
-      const float mx = fmaxf(ma, mb) * a.sl2;
-      float f = 1.0f;
-      const bool rescale = mx > m_use + kRescale;
-      if (rescale) {
-        f = ex2(m_use - mx);  // 0 when m_use is -inf
-        l *= f;
-        m_use = mx;
+        tc_fence_after();
       }
-      const float nms = (m_use == -INFINITY) ? 0.0f : -m_use;
-      const float sl2 = a.sl2;
-      float la = 0.0f, lb = 0.0f;
-      auto emit = [&](uint32_t(&x)[32], int k) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          float y0, y1;
-          ffma2(y0, y1, __uint_as_float(x[2 * i]), __uint_as_float(x[2 * i + 1]), sl2, sl2, nms, nms);
-          const float p0 = ex2(y0), p1 = ex2(y1);
-          fadd2(la, lb, la, lb, p0, p1);
-          pk[i] = pack_bf16(p0, p1);
-        }
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int cidx = 4 * k + q;  // 16-byte chunk (8 keys) index 0..15
-          uint8_t* dst = prow + (cidx >> 3) * L::BOX + (((cidx & 7) ^ rsw) << 4);
-          *reinterpret_cast<uint4*>(dst) = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
-        }
-      };
-      emit(x0, 0);
-      emit(x1, 1);
-      emit(x2, 2);
-      emit(x3, 3);
-      l += la + lb;
-      // O (from PV of earlier tiles, all complete once S of this tile is) follows the
-      // new maximum; skipped while this row has seen no key (O is still zero then).
-      if (__any_sync(0xffffffffu, rescale && t > 0 && f != 0.0f)) {
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t y[32];
-          tmem_ld32(tO + 32 * c, y);
-          tmem_ld_wait(y);
-          const float g = (rescale && t > 0) ? f : 1.0f;
-#pragma unroll
-          for (int i = 0; i < 32; ++i) y[i] = __float_as_uint(__uint_as_float(y[i]) * g);
-          tmem_st32(tO + 32 * c, y);
-        }
-        tmem_st_wait();
-      }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(b_p + 8 * qt);
-    }
-    // ---- epilogue ----
-    if (ok && n > 0) {
-      ok = mbar_wait(b_o + 8 * qt, (n - 1) & 1, abort_flag, status);
-      ok = __all_sync(0xffffffffu, ok);
-      if (ok) tc_fence_after();
-    }
-    if (ok) {
-      const int64_t orow = (((int64_t)b * a.N + qp) * a.H + h) * D;
-      const int64_t lrow = ((int64_t)b * a.H + h) * a.N + qp;
+      gt += n;
+      const int64_t orow = (((int64_t)it.b * a.N + qp) * a.H + it.h) * D;
+      const int64_t lrow = ((int64_t)it.b * a.H + it.h) * a.N + qp;
       if constexpr (LONG) {
         const float inv = l > 0.0f ? 1.0f / l : 0.0f;
         const float lse = l > 0.0f ? (m_use + log2f(l)) * kLn2 : -INFINITY;
@@ -600,6 +612,14 @@ bool make_map(CUtensorMap* m, const void* base, int D, int64_t rows, int heads) 
   return r == CUDA_SUCCESS;
 }
 
+int num_sms() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+    return 148;
+  return n;
+}
+
 TcArgs make_args(const focus_params& p, const WsLayout& L, char* ws, float scale) {
   TcArgs a{};
   a.B = p.B;
@@ -612,9 +632,10 @@ TcArgs make_args(const focus_params& p, const WsLayout& L, char* ws, float scale
   a.qtab_cap = p.B * p.R * ((p.N + BMQ - 1) / BMQ + L.nseg);
   a.sl2 = scale * kLog2e;
   a.perm = reinterpret_cast<const int*>(ws + L.perm);
-  a.seg_off = reinterpret_cast<const int*>(ws + L.segoff);
   a.qtab = reinterpret_cast<const QBlock*>(ws + L.qtab);
   a.qtab_count = &reinterpret_cast<const WsHeader*>(ws)->qtab_count;
+  a.plan_head = reinterpret_cast<const PlanHead*>(ws + L.plan_head);
+  a.plan_ent = reinterpret_cast<const PlanEnt*>(ws + L.plan_ent);
   a.o_lr = reinterpret_cast<float*>(ws + L.olr);
   a.lse_lr = reinterpret_cast<float*>(ws + L.lselr);
   a.status = &reinterpret_cast<WsHeader*>(ws)->status;
@@ -623,11 +644,14 @@ TcArgs make_args(const focus_params& p, const WsLayout& L, char* ws, float scale
 
 template <int D, bool LONG>
 cudaError_t launch_tc(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-                      const TcArgs& a, dim3 grid, cudaStream_t s) {
+                      const TcArgs& a, int n_items, cudaStream_t s) {
   const int smem = Layout<D>::SMEM;
   cudaError_t e = cudaFuncSetAttribute(attn_tc<D, LONG>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  attn_tc<D, LONG><<<grid, NTHREADS, smem, s>>>(mq, mk, mv, a);
+  const int sms = num_sms();
+  const int grid = n_items < sms ? n_items : sms;
+  if (grid < 1) return cudaSuccess;
+  attn_tc<D, LONG><<<grid, NTHREADS, smem, s>>>(mq, mk, mv, a, n_items);
   return cudaGetLastError();
 }
 
@@ -637,16 +661,16 @@ int tc_block_rows() { return BMQ; }
 
 cudaError_t launch_attn_long_tc(const focus_params& p, const WsLayout& L, const uint32_t* mask,
                                 char* ws, float scale, cudaStream_t s) {
+  (void)mask;
   TcArgs a = make_args(p, L, ws, scale);
-  a.mask = mask;
   CUtensorMap mq, mk, mv;
   if (!make_map(&mq, ws + L.qp, p.d_head, (int64_t)p.B * p.H * p.N, 0) ||
       !make_map(&mk, ws + L.kp, p.d_head, (int64_t)p.B * p.H_kv * p.N, 0) ||
       !make_map(&mv, ws + L.vp, p.d_head, (int64_t)p.B * p.H_kv * p.N, 0))
     return cudaErrorInvalidValue;
-  dim3 grid((unsigned)((int64_t)a.qtab_cap * (p.H / p.R)));
-  return p.d_head == 64 ? launch_tc<64, true>(mq, mk, mv, a, grid, s)
-                        : launch_tc<128, true>(mq, mk, mv, a, grid, s);
+  const int n_items = a.qtab_cap * (p.H / p.R);
+  return p.d_head == 64 ? launch_tc<64, true>(mq, mk, mv, a, n_items, s)
+                        : launch_tc<128, true>(mq, mk, mv, a, n_items, s);
 }
 
 cudaError_t launch_attn_window_tc(const focus_params& p, const WsLayout& L, const bf16* q,
@@ -660,9 +684,9 @@ cudaError_t launch_attn_window_tc(const focus_params& p, const WsLayout& L, cons
       !make_map(&mk, k, p.d_head, (int64_t)p.B * p.N, p.H_kv) ||
       !make_map(&mv, v, p.d_head, (int64_t)p.B * p.N, p.H_kv))
     return cudaErrorInvalidValue;
-  dim3 grid((p.N + BMQ - 1) / BMQ, p.H, p.B);
-  return p.d_head == 64 ? launch_tc<64, false>(mq, mk, mv, a, grid, s)
-                        : launch_tc<128, false>(mq, mk, mv, a, grid, s);
+  const int n_items = p.B * p.H * ((p.N + BMQ - 1) / BMQ);
+  return p.d_head == 64 ? launch_tc<64, false>(mq, mk, mv, a, n_items, s)
+                        : launch_tc<128, false>(mq, mk, mv, a, n_items, s);
 }
 
 }  // namespace focus

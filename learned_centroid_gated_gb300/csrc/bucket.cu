@@ -249,6 +249,59 @@ build_qtab(int N, int nseg, int BR, int bm, const int* __restrict__ seg_off, con
   }
 }
 
+// First index in P[lo, hi) whose value exceeds x (P ascending).
+__device__ __forceinline__ int upper_bound_pos(const int* __restrict__ P, int lo, int hi, int x) {
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(P + mid) <= x) lo = mid + 1; else hi = mid;
+  }
+  return lo;
+}
+
+// Long-range plan: for query block u (segment S, positions p_lo..p_hi), every
+// segment T with mask(S) & mask(T) != 0 and keys at pos <= p_hi - w, in segment
+// order.  One warp per block; lanes take segments in parallel.
+__global__ void __launch_bounds__(32)
+build_plan(int N, int w, int nseg, const int* __restrict__ seg_off, const int* __restrict__ perm,
+           const uint32_t* __restrict__ mask, const QBlock* __restrict__ qtab,
+           const int* __restrict__ qtab_count, PlanHead* __restrict__ heads,
+           PlanEnt* __restrict__ ents) {
+  const int u = blockIdx.x, lane = threadIdx.x;
+  if (u >= *qtab_count) return;
+  const QBlock e = qtab[u];
+  const int* P = perm + (int64_t)e.br * N;
+  const int* SO = seg_off + (int64_t)e.br * (nseg + 1);
+  const uint32_t* M = mask + (int64_t)e.br * N;
+  const int p_lo = __ldg(P + e.row0), p_hi = __ldg(P + e.row0 + e.rows - 1);
+  const uint32_t mS = __ldg(M + p_lo);
+  PlanEnt* out = ents + (int64_t)u * nseg;
+  int n_ent = 0, n_tiles = 0;
+  for (int T0 = 0; T0 < nseg; T0 += 32) {
+    const int T = T0 + lane;
+    bool ok = false;
+    PlanEnt pe{0, 0, 0, 0};
+    if (T < nseg) {
+      const int s0 = __ldg(SO + T), s1 = __ldg(SO + T + 1);
+      if (s1 > s0 && (__ldg(M + __ldg(P + s0)) & mS)) {
+        const int hi = upper_bound_pos(P, s0, s1, p_hi - w) - s0;
+        if (hi > 0) {
+          ok = true;
+          pe.start = s0;
+          pe.cnt = hi;
+          pe.nfull = (upper_bound_pos(P, s0, s1, p_lo - w) - s0) / kKeyTile;
+        }
+      }
+    }
+    const unsigned bal = __ballot_sync(0xffffffffu, ok);
+    if (ok) out[n_ent + __popc(bal & lanemask_lt())] = pe;
+    n_ent += __popc(bal);
+    int tiles = ok ? (pe.cnt + kKeyTile - 1) / kKeyTile : 0;
+    for (int o = 16; o > 0; o >>= 1) tiles += __shfl_xor_sync(0xffffffffu, tiles, o);
+    n_tiles += tiles;
+  }
+  if (lane == 0) heads[u] = PlanHead{n_ent, n_tiles, 0, 0};
+}
+
 // Permuted, head-major copies: Qp[b][h][n'][:] = q[b][perm[n']][h][:] for the heads
 // of routing head rho, and likewise K/V for its KV heads.  One CTA per permuted row.
 __global__ void __launch_bounds__(256)
@@ -302,6 +355,18 @@ cudaError_t launch_qtab(const focus_params& p, const WsLayout& L, char* ws, int 
                                        reinterpret_cast<int*>(ws + L.perm),
                                        reinterpret_cast<int*>(ws + L.entoff),
                                        reinterpret_cast<QBlock*>(ws + L.qtab), &hdr->qtab_count);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_plan(const focus_params& p, const WsLayout& L, const uint32_t* mask, char* ws,
+                        int block_rows, cudaStream_t s) {
+  const int cap = p.B * p.R * ((p.N + block_rows - 1) / block_rows + L.nseg);
+  build_plan<<<cap, 32, 0, s>>>(p.N, p.w, L.nseg, reinterpret_cast<const int*>(ws + L.segoff),
+                                reinterpret_cast<const int*>(ws + L.perm), mask,
+                                reinterpret_cast<const QBlock*>(ws + L.qtab),
+                                &reinterpret_cast<const WsHeader*>(ws)->qtab_count,
+                                reinterpret_cast<PlanHead*>(ws + L.plan_head),
+                                reinterpret_cast<PlanEnt*>(ws + L.plan_ent));
   return cudaGetLastError();
 }
 

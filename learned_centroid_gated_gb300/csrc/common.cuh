@@ -26,13 +26,25 @@ struct QBlock {
   int br, seg, row0, rows;
 };
 
+// Long-range plan of one query block: its compatible key segments, in segment
+// order, each as (first permuted row, keys with pos <= p_hi - w, leading tiles
+// whose keys all satisfy pos <= p_lo - w), and the total number of key tiles.
+struct PlanHead {
+  int n_ent, n_tiles, pad0, pad1;
+};
+struct PlanEnt {
+  int start, cnt, nfull, pad;
+};
+
+constexpr int kKeyTile = 128;     // keys per attention key tile
 constexpr int kChunk = 1024;      // tokens per bucketing chunk (one warp)
 constexpr int kSinkBlock = 256;   // tokens per Sinkhorn partial-reduction block
 constexpr int kAttnBM = 128;      // smallest query block of the long-range schedule
 constexpr int kKeySentinel = 0x7fffffff;
 
 struct WsLayout {
-  size_t hdr, mask, beta, skpart, hist, segoff, cbase, perm, entoff, qtab, qp, kp, vp, olr, lselr;
+  size_t hdr, mask, beta, skpart, hist, segoff, cbase, perm, entoff, qtab, plan_head, plan_ent, qp, kp,
+      vp, olr, lselr;
   size_t total;
   int nseg, nchunk, nblk_sk, qtab_cap;
 };
@@ -60,6 +72,8 @@ cudaError_t launch_bucket(const focus_params& p, const WsLayout& L, const uint32
                           cudaStream_t s);
 cudaError_t launch_qtab(const focus_params& p, const WsLayout& L, char* ws, int block_rows,
                         cudaStream_t s);
+cudaError_t launch_plan(const focus_params& p, const WsLayout& L, const uint32_t* mask, char* ws,
+                        int block_rows, cudaStream_t s);
 cudaError_t launch_permute(const focus_params& p, const WsLayout& L, const bf16* q, const bf16* k,
                            const bf16* v, char* ws, cudaStream_t s);
 // attn_tc.cu (tcgen05 engine)

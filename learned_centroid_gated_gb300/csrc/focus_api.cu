@@ -53,6 +53,8 @@ WsLayout layout(const focus_params& p) {
   L.perm = take(sizeof(int) * (size_t)BR * p.N);
   L.entoff = take(sizeof(int) * ((size_t)BR * L.nseg + 1));
   L.qtab = take(sizeof(QBlock) * (size_t)L.qtab_cap);
+  L.plan_head = take(sizeof(PlanHead) * (size_t)L.qtab_cap);
+  L.plan_ent = take(sizeof(PlanEnt) * (size_t)L.qtab_cap * L.nseg);
   L.qp = take(sizeof(uint16_t) * (size_t)p.B * p.H * p.N * p.d_head);
   L.kp = take(sizeof(uint16_t) * (size_t)p.B * p.H_kv * p.N * p.d_head);
   L.vp = take(sizeof(uint16_t) * (size_t)p.B * p.H_kv * p.N * p.d_head);
@@ -174,6 +176,7 @@ int focus_attn_fwd_ev(const focus_params* p, const uint16_t* q, const uint16_t* 
   if ((rc = cuda_rc(launch_bucket(*p, L, mask, w, s)))) return rc;
   const bool mma = use_mma_engine();
   if ((rc = cuda_rc(launch_qtab(*p, L, w, mma ? kAttnBM : tc_block_rows(), s)))) return rc;
+  if (!mma && (rc = cuda_rc(launch_plan(*p, L, mask, w, tc_block_rows(), s)))) return rc;
   if ((rc = mark(2))) return rc;
   if ((rc = cuda_rc(launch_permute(*p, L, qb, kb, vb, w, s)))) return rc;
   if ((rc = mark(3))) return rc;
