@@ -216,6 +216,26 @@ def traffic_of(kernel_src: str):
     return None
 
 
+# ------------------------------------------------------------ multi-rank --
+def rank_seed(base_seed: int, rank: int) -> int:
+    """Each rank processes its own independent problem (weak scaling)."""
+    return base_seed + rank
+
+
+def reduce_max(value: float, dist, device) -> float:
+    """Max of a per-rank scalar over all ranks (the job's time is its slowest rank)."""
+    if dist is None:
+        return value
+    t = torch.tensor([value], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world: int, units_per_rank: float, seconds: float) -> float:
+    """Whole-job units per second: every rank processed units_per_rank in <= seconds."""
+    return world * units_per_rank / seconds
+
+
 # ---------------------------------------------------------------- GPU arm --
 def run_focus(args):
     import learned_centroid_gated_gb300 as focus
@@ -238,7 +258,7 @@ def run_focus(args):
 
     wl = synth.WORKLOADS[args.workload]
     p = focus.Params.from_workload(wl)
-    x = synth.make_inputs(wl, seed=args.seed + rank, device=dev)
+    x = synth.make_inputs(wl, seed=rank_seed(args.seed, rank), device=dev)
     ws = focus.Workspace(dev).get(p)
     o = torch.empty_like(x["q"])
     lse = torch.empty(p.B, p.H, p.N, dtype=torch.float32, device=dev)
@@ -266,6 +286,11 @@ def run_focus(args):
     longrange = allowed - window
     flops = 4.0 * wl.d_head * allowed
     flops_long = 4.0 * wl.d_head * longrange
+    # executed tensor-core work (whole 256 x 128 tiles, masked elements included)
+    lt, wt = pairs.executed_tiles(mask_np, wl.w)
+    tile_flops = 4.0 * wl.d_head * 256 * 128
+    exec_long = tile_flops * int(lt.sum()) * heads_per_rho
+    exec_win = tile_flops * wt * wl.B * wl.H
     causal = wl.B * wl.H * wl.N * (wl.N + 1) // 2
 
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(focus.N_STAGE_EVENTS)]
@@ -284,17 +309,13 @@ def run_focus(args):
         barrier()
         time.sleep(0.1)
     clocks = clk.summary()
-    ms = t_start.elapsed_time(t_end)
-    if dist is not None:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = reduce_max(t_start.elapsed_time(t_end), dist, dev)
     ms_step = ms / K
     stage_ms = {}
     for si, name in enumerate(focus.STAGES):
         stage_ms[name] = statistics.mean(e[si].elapsed_time(e[si + 1]) for e in evs)
 
-    value = world * wl.B * wl.N / (ms_step / 1e3)
+    value = job_throughput(world, wl.B * wl.N, ms_step / 1e3)
     tflops = flops / (ms_step / 1e3) / 1e12
 
     # end-to-end through the public host-buffer API (pinned host inputs)
@@ -308,12 +329,8 @@ def run_focus(args):
     for _ in range(ke):
         sess(host["q"], host["k"], host["v"], host["r"], host["C"])
     barrier()
-    e_s = (time.perf_counter() - e0) / ke
-    if dist is not None:
-        t = torch.tensor([e_s], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e_s = float(t.item())
-    e2e = {"value": world * wl.B * wl.N / e_s, "unit": UNIT,
+    e_s = reduce_max((time.perf_counter() - e0) / ke, dist, dev)
+    e2e = {"value": job_throughput(world, wl.B * wl.N, e_s), "unit": UNIT,
            "h2d_bytes_per_step": sess.h2d_bytes(*host.values()),
            "d2h_bytes_per_step": sess.d2h_bytes(), "ms_per_step": 1e3 * e_s}
 
@@ -329,6 +346,9 @@ def run_focus(args):
         "frac_sustained": achieved / peaks["bf16_tflops_sustained"],
         "traffic": traffic_of(os.path.join(ROOT, "learned_centroid_gated_gb300", "csrc", "attn_tc.cu")),
         "algorithmic_flops_per_launch": flops_long,
+        "executed_flops_per_launch": exec_long,
+        "tile_efficiency": flops_long / exec_long,
+        "executed_tflops": exec_long / t_long / 1e12,
         "launch_ms": stage_ms["attn_long"],
     }
     launches_per_step = (1 + 2 * wl.sinkhorn_iters) + 3 + 1 + 1 + 1 + 1
@@ -345,6 +365,9 @@ def run_focus(args):
         "allowed_pair_frac_of_peak": tflops / peaks["bf16_tflops"],
         "allowed_pairs": allowed, "allowed_fraction_of_causal": allowed / causal,
         "stages_ms": stage_ms,
+        "window": {"algorithmic_tflops": 4.0 * wl.d_head * window / (stage_ms["attn_window"] / 1e3) / 1e12,
+                   "executed_tflops": exec_win / (stage_ms["attn_window"] / 1e3) / 1e12,
+                   "tile_efficiency": 4.0 * wl.d_head * window / exec_win},
         "roofline": roofline,
         "e2e": e2e,
         "gpu_launches": launches_per_step * K,

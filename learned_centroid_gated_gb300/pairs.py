@@ -46,3 +46,32 @@ def allowed_flops(mask, w: int, H: int, H_kv: int, d_head: int) -> int:
     R = cnt.shape[1]
     heads_per_rho = H // R
     return int(4 * d_head * heads_per_rho * cnt.sum())
+
+
+def executed_tiles(mask, w: int, block_rows: int = 256, key_tile: int = 128):
+    """Key tiles the tensor-core kernels run, per (b, routing head), for FLOP
+    accounting of executed (not just allowed) work: long-range = for every block of
+    `block_rows` consecutive rows of one mask value, ceil(keys / key_tile) over each
+    compatible mask value's keys with pos <= (last row's pos) - w; window = for every
+    block of `block_rows` consecutive tokens, ceil(span / key_tile) with span the
+    keys (first row - w, last row].  Returns (long_tiles [B, R], window_tiles)."""
+    m = np.asarray(mask).astype(np.int64) & 0xFFFFFFFF
+    B, R, N = m.shape
+    long_t = np.zeros((B, R), np.int64)
+    for b in range(B):
+        for rho in range(R):
+            row = m[b, rho]
+            vals, inv = np.unique(row, return_inverse=True)
+            pos = [np.nonzero(inv == a)[0] for a in range(len(vals))]
+            for a, va in enumerate(vals):
+                last = pos[a][np.minimum(np.arange(block_rows - 1, len(pos[a]) + block_rows - 1,
+                                                   block_rows), len(pos[a]) - 1)]
+                for c, vc in enumerate(vals):
+                    if int(va) & int(vc):
+                        cnt = np.searchsorted(pos[c], last - w, side="right")
+                        long_t[b, rho] += int(((cnt + key_tile - 1) // key_tile).sum())
+    starts = np.arange(0, N, block_rows)
+    ends = np.minimum(starts + block_rows, N)
+    span = ends - np.maximum(0, starts - w + 1)
+    win_t = int(((span + key_tile - 1) // key_tile).sum())
+    return long_t, win_t
