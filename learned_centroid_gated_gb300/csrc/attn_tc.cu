@@ -18,8 +18,10 @@
 //   warps 0-3   softmax of tile A (thread = row = TMEM lane), warps 4-7 of tile B;
 //               each warpgroup also writes its tile's output rows
 //   warps 10-11 idle (they complete the third warpgroup for the register split)
-// TMEM (512 columns): S_A | S_B | O_A | O_B.  P goes to shared memory in the
-// 128-byte-swizzled K-major layout the MMA reads.  Issue order on the tensor
+// TMEM (512 columns): S_A | S_B | O_A | O_B.  P (bf16) is written over the first
+// 64 columns of its S tile once S is in registers and is the TMEM A operand of
+// O += P V, so neither P nor its reads touch shared memory (the S and PV operand
+// traffic through shared memory is what bounds this kernel).  Issue order on the tensor
 // core: S_A(0) S_B(0) | PV_A(t) S_A(t+1) PV_B(t) S_B(t+1) | ..., so the softmax of
 // one tile runs while the tensor core works on the other.  The running max is
 // rescaled lazily (only when it grows by more than 2^8), in place in TMEM.
@@ -65,10 +67,8 @@ struct Layout {
   static constexpr int BOX = QT * 128;        // one TMA box: 128 rows x 128 bytes
   static constexpr int BOXES = D / 64;        // boxes per 128 x D tile
   static constexpr int TILE = BOXES * BOX;    // a 128-row Q/K/V tile, bf16
-  static constexpr int PBYTES = 2 * BOX;      // P tile: 128 rows x 128 keys, bf16
   static constexpr int Q = 0;
-  static constexpr int P = Q + 2 * TILE;
-  static constexpr int RING = P + 2 * PBYTES;
+  static constexpr int RING = Q + 2 * TILE;
   static constexpr int BAR = RING + NSTAGE * TILE;
   static constexpr int SMEM = BAR + 128 + 1024;  // + barriers, + 1 KB alignment slack
 };
@@ -273,7 +273,6 @@ attn_tc(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensor
       constexpr uint32_t IS = idesc_bf16(QT, BNK, 0);  // S = Q K^T, both K-major
       constexpr uint32_t IPV = idesc_bf16(QT, D, 1);   // O += P V, V MN-major
       const uint32_t q_base = smem_u32(sm + L::Q);
-      const uint32_t p_base = smem_u32(sm + L::P);
       const uint32_t r_base = smem_u32(sm + L::RING);
       auto slot = [&](int item) { return r_base + (item % NSTAGE) * L::TILE; };
       auto ring_wait = [&](int item) {
@@ -288,12 +287,11 @@ attn_tc(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensor
         }
       };
       auto issue_PV = [&](int qt, uint32_t vaddr, bool acc) {
+        // A = P in TMEM (written over the first 64 columns of S_qt), 8 columns per K step
 #pragma unroll
-        for (int kk = 0; kk < BNK / 16; ++kk) {
-          const uint32_t poff = (kk / 4) * L::BOX + (kk % 4) * 32;
-          umma_ss(tmem + 2 * BNK + qt * D, sw128_desc(p_base + qt * L::PBYTES + poff, 16, 1024),
+        for (int kk = 0; kk < BNK / 16; ++kk)
+          umma_ts(tmem + 2 * BNK + qt * D, tmem + qt * BNK + 8 * kk,
                   sw128_desc(vaddr + kk * 2048, L::BOX, 1024), IPV, (acc || kk > 0) ? 1u : 0u);
-        }
       };
       int ri = 0, gt = 0, qcnt = 0;
       bool ok = true;
@@ -350,8 +348,6 @@ attn_tc(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensor
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + lane_off + qt * BNK;
     const uint32_t tO = tmem + lane_off + 2 * BNK + qt * D;
-    uint8_t* prow = sm + L::P + qt * L::PBYTES + r * 128;
-    const int rsw = r & 7;
     const float sl2 = a.sl2;
     int gt = 0;
     bool ok = true;
@@ -438,6 +434,8 @@ attn_tc(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensor
         }
         const float nms = (m_use == -INFINITY) ? 0.0f : -m_use;
         float la = 0.0f, lb = 0.0f;
+        // P (bf16 pairs) goes over the first 64 TMEM columns of this tile's S, which
+        // are already in registers: column 16k + i holds keys 32k + 2i and 32k + 2i + 1.
         auto emit = [&](uint32_t(&xx)[32], int k) {
           uint32_t pk[16];
 #pragma unroll
@@ -448,12 +446,7 @@ attn_tc(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensor
             fadd2(la, lb, la, lb, p0, p1);
             pk[i] = pack_bf16(p0, p1);
           }
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int cidx = 4 * k + q;  // 16-byte chunk (8 keys) index 0..15
-            uint8_t* dst = prow + (cidx >> 3) * L::BOX + (((cidx & 7) ^ rsw) << 4);
-            *reinterpret_cast<uint4*>(dst) = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
-          }
+          tmem_st16(tS + 16 * k, pk);
         };
         emit(x0, 0);
         emit(x1, 1);
@@ -473,9 +466,8 @@ attn_tc(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensor
             for (int i = 0; i < 32; ++i) y[i] = __float_as_uint(__uint_as_float(y[i]) * g);
             tmem_st32(tO + 32 * c, y);
           }
-          tmem_st_wait();
         }
-        fence_proxy_async_smem();
+        tmem_st_wait();
         tc_fence_before();
         mbar_arrive(b_p + 8 * qt);
       }
