@@ -70,7 +70,15 @@ struct Layout {
   static constexpr int Q = 0;
   static constexpr int RING = Q + 2 * TILE;
   static constexpr int BAR = RING + NSTAGE * TILE;
-  static constexpr int SMEM = BAR + 128 + 1024;  // + barriers, + 1 KB alignment slack
+  // barrier block: q, q_empty, full[NSTAGE], empty[NSTAGE], s[2], p[2], o[2], drain
+  // (8 bytes each), then the TMEM address word and the abort flag
+  static constexpr int BAR_Q = 0, BAR_QE = 8, BAR_FULL = 16, BAR_EMPTY = BAR_FULL + 8 * NSTAGE;
+  static constexpr int BAR_S = BAR_EMPTY + 8 * NSTAGE, BAR_P = BAR_S + 16, BAR_O = BAR_P + 16;
+  static constexpr int BAR_DRAIN = BAR_O + 16, TMEM_SLOT = BAR_DRAIN + 8, ABORT = TMEM_SLOT + 4;
+  static constexpr int BAR_BYTES = 256;
+  static_assert(ABORT + 4 <= BAR_BYTES, "barrier block overflow");
+  static constexpr int SMEM = BAR + BAR_BYTES + 1024;  // + barriers, + 1 KB alignment slack
+  static_assert(SMEM <= 232448, "shared memory budget");
 };
 
 struct TcArgs {
@@ -168,16 +176,17 @@ attn_tc(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensor
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   uint8_t* bar = sm + L::BAR;
-  const uint32_t b_q = smem_u32(bar);                    // Q tiles landed
-  const uint32_t b_qe = b_q + 8;                         // Q buffer free (last S of an item done)
-  const uint32_t b_full = b_q + 16, b_empty = b_q + 40;  // + 8 * stage
-  const uint32_t b_s = b_q + 64, b_p = b_q + 80, b_o = b_q + 96;  // + 8 * query tile
-  const uint32_t b_drain = b_q + 112;
-  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(bar + 120);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(bar + 124);
+  const uint32_t b_q = smem_u32(bar) + L::BAR_Q;     // Q tiles landed
+  const uint32_t b_qe = smem_u32(bar) + L::BAR_QE;   // Q buffer free (last S of an item done)
+  const uint32_t b_full = smem_u32(bar) + L::BAR_FULL, b_empty = smem_u32(bar) + L::BAR_EMPTY;  // + 8 * stage
+  const uint32_t b_s = smem_u32(bar) + L::BAR_S, b_p = smem_u32(bar) + L::BAR_P;  // + 8 * query tile
+  const uint32_t b_o = smem_u32(bar) + L::BAR_O;
+  const uint32_t b_drain = smem_u32(bar) + L::BAR_DRAIN;
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(bar + L::TMEM_SLOT);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bar + L::ABORT);
 
   if (warp == MMA_WARP) {
-    tmem_alloc(smem_u32(bar + 120), TMEM_COLS);
+    tmem_alloc(smem_u32(bar + L::TMEM_SLOT), TMEM_COLS);
     tmem_relinquish();
   }
   if (tid == 0) {
