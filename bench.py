@@ -323,7 +323,7 @@ def run_focus(args):
 
     # end-to-end through the public host-buffer API (pinned host inputs)
     host = {n: t.cpu().pin_memory() for n, t in x.items()}
-    sess = focus.HostSession(p, dev, stream)
+    sess = focus.HostSession(p, dev)
     for _ in range(2):
         sess(host["q"], host["k"], host["v"], host["r"], host["C"])
     barrier()

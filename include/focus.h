@@ -167,6 +167,30 @@ int focus_attn_fwd_ev(const focus_params* p, const uint16_t* q, const uint16_t* 
 int focus_route_static(const focus_params* p, const float* r, const float* C,
                        uint32_t* mask_out, float* margin_out, void* stream);
 
+/*
+ * Forward pass on HOST buffers, with host-device copies overlapped with compute.
+ * The heads are split into n_groups groups of consecutive KV heads (with their
+ * query heads and, when R > 1, their routing heads); group g+1's inputs are copied
+ * in while group g computes, and group g's outputs are copied out meanwhile.
+ * Each group is an independent problem (attention never mixes heads), so the
+ * result equals focus_attn_fwd on the whole problem.
+ *   q_h, k_h, v_h, r_h, C_h  host inputs, layouts as in focus_attn_fwd (r and C
+ *                            are required: routing runs inside, per group)
+ *   o_h [B, N, H, d] bf16, lse_h [B, H, N] fp32 or NULL: host outputs
+ *   n_groups   number of groups, 0 = automatic (4, 2 or 1: the largest that divides
+ *              H_kv and, when R > 1, R)
+ *   ws         device workspace of focus_host_workspace_size(p, n_groups) bytes
+ *   compute_stream, copy_stream  two different streams (NULL = legacy default)
+ * Host memory should be page-locked (cudaHostAlloc / cudaHostRegister), else the
+ * copies are staged synchronously by CUDA. Returns after enqueuing: the outputs are
+ * complete once copy_stream has been synchronised.
+ */
+size_t focus_host_workspace_size(const focus_params* p, int n_groups);
+int focus_attn_fwd_host(const focus_params* p, const uint16_t* q_h, const uint16_t* k_h,
+                        const uint16_t* v_h, const float* r_h, const float* C_h, uint16_t* o_h,
+                        float* lse_h, int n_groups, void* ws, size_t ws_bytes,
+                        void* compute_stream, void* copy_stream);
+
 /* Synchronises `stream` and returns the device status word of the last call
  * that used this workspace (FOCUS_OK, FOCUS_ERR_TIMEOUT, FOCUS_ERR_BOUNDS), or
  * FOCUS_ERR_CUDA if the synchronisation itself failed. */

@@ -238,30 +238,36 @@ def attn_fwd(p: Params, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, r=Non
     return out, lse
 
 
-class HostSession:
-    """End-to-end calls on HOST tensors: each call copies the inputs (pinned host
-    memory recommended) to reusable device buffers, runs the forward pass and copies
-    O and LSE back into reusable pinned host tensors, then synchronises.  The
-    returned host tensors are overwritten by the next call."""
+_lib.focus_host_workspace_size.argtypes = [_PP, ctypes.c_int]
+_lib.focus_host_workspace_size.restype = ctypes.c_size_t
+_lib.focus_attn_fwd_host.argtypes = [_PP, _P, _P, _P, _P, _P, _P, _P, ctypes.c_int, _P, ctypes.c_size_t,
+                                     _P, _P]
+_lib.focus_attn_fwd_host.restype = ctypes.c_int
 
-    def __init__(self, p: Params, device="cuda", stream=None):
+
+def host_workspace_size(p: Params, n_groups: int = 0) -> int:
+    return int(_lib.focus_host_workspace_size(ctypes.byref(p.c()), n_groups))
+
+
+class HostSession:
+    """End-to-end calls on HOST tensors through focus_attn_fwd_host: the heads are
+    processed in groups, copies of one group overlapping the compute of another, on
+    two streams of this session.  Inputs should be pinned (tensor.pin_memory()) for
+    the copies to overlap.  Each call returns pinned host tensors (o, lse) that the
+    next call overwrites."""
+
+    def __init__(self, p: Params, device="cuda", n_groups: int = 0):
         self.p = p
         self.device = torch.device(device)
-        self.stream = stream
-        self.ws = Workspace(self.device)
-        self._dev: dict = {}
+        self.n_groups = n_groups
+        need = host_workspace_size(p, n_groups)
+        if need == 0:
+            raise FocusError(-1, "focus_host_workspace_size")
+        self.ws = torch.empty(need, dtype=torch.uint8, device=self.device)
+        self.compute = torch.cuda.Stream(self.device)
+        self.copy = torch.cuda.Stream(self.device)
         self.o_host = torch.empty(p.B, p.N, p.H, p.d_head, dtype=torch.bfloat16, pin_memory=True)
         self.lse_host = torch.empty(p.B, p.H, p.N, dtype=torch.float32, pin_memory=True)
-        self._o = torch.empty(self.o_host.shape, dtype=torch.bfloat16, device=self.device)
-        self._lse = torch.empty(self.lse_host.shape, dtype=torch.float32, device=self.device)
-
-    def _stage(self, name: str, t: torch.Tensor) -> torch.Tensor:
-        d = self._dev.get(name)
-        if d is None or d.shape != t.shape or d.dtype != t.dtype:
-            d = torch.empty(t.shape, dtype=t.dtype, device=self.device)
-            self._dev[name] = d
-        d.copy_(t, non_blocking=True)
-        return d
 
     def h2d_bytes(self, *tensors) -> int:
         return sum(t.numel() * t.element_size() for t in tensors)
@@ -269,21 +275,25 @@ class HostSession:
     def d2h_bytes(self) -> int:
         return self.o_host.numel() * 2 + self.lse_host.numel() * 4
 
-    def __call__(self, q, k, v, r, C, stage_events=None):
-        dev = [self._stage(n, t) for n, t in zip("qkvrC", (q, k, v, r, C))]
-        attn_fwd(self.p, *dev, out=self._o, lse=self._lse, ws=self.ws, stream=self.stream,
-                 stage_events=stage_events)
-        self.o_host.copy_(self._o, non_blocking=True)
-        self.lse_host.copy_(self._lse, non_blocking=True)
-        (self.stream or torch.cuda.current_stream()).synchronize()
+    def __call__(self, q, k, v, r, C):
+        for t, dt in ((q, torch.bfloat16), (k, torch.bfloat16), (v, torch.bfloat16),
+                      (r, torch.float32), (C, torch.float32)):
+            assert t.device.type == "cpu" and t.dtype == dt and t.is_contiguous()
+        _check(_lib.focus_attn_fwd_host(ctypes.byref(self.p.c()), _ptr(q), _ptr(k), _ptr(v), _ptr(r),
+                                        _ptr(C), _ptr(self.o_host), _ptr(self.lse_host), self.n_groups,
+                                        _ptr(self.ws), self.ws.numel(),
+                                        ctypes.c_void_p(self.compute.cuda_stream),
+                                        ctypes.c_void_p(self.copy.cuda_stream)),
+               "focus_attn_fwd_host")
+        self.copy.synchronize()
         return self.o_host, self.lse_host
 
 
 def attn_fwd_host(p: Params, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, r: torch.Tensor,
-                  C: torch.Tensor, *, device="cuda", stream=None):
+                  C: torch.Tensor, *, device="cuda", n_groups: int = 0):
     """One end-to-end call on HOST tensors (see HostSession for repeated calls).
     Returns host (o, lse)."""
-    o, lse = HostSession(p, device, stream)(q, k, v, r, C)
+    o, lse = HostSession(p, device, n_groups)(q, k, v, r, C)
     return o.clone(), lse.clone()
 
 

@@ -197,6 +197,156 @@ int focus_attn_fwd(const focus_params* p, const uint16_t* q, const uint16_t* k,
   return focus_attn_fwd_ev(p, q, k, v, r, C, mask_in, o, lse, ws, ws_bytes, stream, nullptr);
 }
 
+// ------------------------------------------------------------ host buffers --
+namespace {
+
+int host_groups(const focus_params& p, int n_groups) {
+  auto ok = [&](int g) {
+    return g >= 1 && p.H_kv % g == 0 && (p.R == 1 || p.R % g == 0);
+  };
+  if (n_groups > 0) return ok(n_groups) ? n_groups : -1;
+  for (int g : {4, 2, 1})
+    if (ok(g)) return g;
+  return 1;
+}
+
+focus_params group_params(const focus_params& p, int G) {
+  focus_params q = p;
+  q.H = p.H / G;
+  q.H_kv = p.H_kv / G;
+  q.R = p.R == 1 ? 1 : p.R / G;
+  return q;
+}
+
+struct HostLayout {
+  size_t q, k, v, o, lse, r, set_bytes, C, attn, total;
+};
+
+HostLayout host_layout(const focus_params& p, int G) {
+  const focus_params g = group_params(p, G);
+  HostLayout H{};
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off = align_up(off + bytes, 256);
+    return at;
+  };
+  const size_t BN = (size_t)p.B * p.N;
+  H.q = take(BN * g.H * p.d_head * 2);
+  H.k = take(BN * g.H_kv * p.d_head * 2);
+  H.v = take(BN * g.H_kv * p.d_head * 2);
+  H.o = take(BN * g.H * p.d_head * 2);
+  H.lse = take((size_t)p.B * g.H * p.N * 4);
+  H.r = take(BN * g.R * FOCUS_D_G * 4);
+  H.set_bytes = off;
+  off = 2 * H.set_bytes;  // two staging sets
+  H.C = take((size_t)p.K * FOCUS_D_G * 4);
+  H.attn = take(layout(g).total);
+  H.total = off;
+  return H;
+}
+
+}  // namespace
+
+size_t focus_host_workspace_size(const focus_params* p, int n_groups) {
+  if (check_params(p) != FOCUS_OK) return 0;
+  const int G = host_groups(*p, n_groups);
+  if (G < 1) return 0;
+  return host_layout(*p, G).total;
+}
+
+int focus_attn_fwd_host(const focus_params* p, const uint16_t* q_h, const uint16_t* k_h,
+                        const uint16_t* v_h, const float* r_h, const float* C_h, uint16_t* o_h,
+                        float* lse_h, int n_groups, void* ws, size_t ws_bytes,
+                        void* compute_stream, void* copy_stream) {
+  int rc = check_params(p);
+  if (rc) return rc;
+  if (!q_h || !k_h || !v_h || !r_h || !C_h || !o_h) return FOCUS_ERR_INVALID_ARG;
+  const int G = host_groups(*p, n_groups);
+  if (G < 1) return FOCUS_ERR_INVALID_ARG;
+  if (compute_stream == copy_stream) return FOCUS_ERR_INVALID_ARG;
+  const HostLayout HL = host_layout(*p, G);
+  if (!ws) return FOCUS_ERR_INVALID_ARG;
+  if (!aligned(ws, 256)) return FOCUS_ERR_ALIGNMENT;
+  if (ws_bytes < HL.total) return FOCUS_ERR_WORKSPACE;
+  const focus_params gp = group_params(*p, G);
+  const size_t attn_bytes = layout(gp).total;
+  cudaStream_t cs = (cudaStream_t)compute_stream, xs = (cudaStream_t)copy_stream;
+  char* w = (char*)ws;
+  const size_t d2 = (size_t)p->d_head * 2;
+  const size_t BN = (size_t)p->B * p->N;
+
+  cudaEvent_t ev_in[2], ev_comp[2];
+  for (int i = 0; i < 2; ++i) {
+    if (cudaEventCreateWithFlags(&ev_in[i], cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&ev_comp[i], cudaEventDisableTiming) != cudaSuccess)
+      return FOCUS_ERR_CUDA;
+  }
+  auto cleanup = [&](int code) {
+    for (int i = 0; i < 2; ++i) {
+      cudaEventDestroy(ev_in[i]);
+      cudaEventDestroy(ev_comp[i]);
+    }
+    return code;
+  };
+  auto set_ptr = [&](int g, size_t off) { return w + (g & 1) * HL.set_bytes + off; };
+  // inputs of group g into staging set g % 2 (strided 2-D copies out of the host layout)
+  auto copy_in = [&](int g) -> cudaError_t {
+    cudaError_t e;
+    if (g >= 2 && (e = cudaStreamWaitEvent(xs, ev_comp[g & 1], 0)) != cudaSuccess) return e;
+    if ((e = cudaMemcpy2DAsync(set_ptr(g, HL.q), gp.H * d2, q_h + (size_t)g * gp.H * p->d_head,
+                               p->H * d2, gp.H * d2, BN, cudaMemcpyHostToDevice, xs)))
+      return e;
+    if ((e = cudaMemcpy2DAsync(set_ptr(g, HL.k), gp.H_kv * d2, k_h + (size_t)g * gp.H_kv * p->d_head,
+                               p->H_kv * d2, gp.H_kv * d2, BN, cudaMemcpyHostToDevice, xs)))
+      return e;
+    if ((e = cudaMemcpy2DAsync(set_ptr(g, HL.v), gp.H_kv * d2, v_h + (size_t)g * gp.H_kv * p->d_head,
+                               p->H_kv * d2, gp.H_kv * d2, BN, cudaMemcpyHostToDevice, xs)))
+      return e;
+    const size_t rw = (size_t)gp.R * FOCUS_D_G * 4;
+    const float* rsrc = r_h + (p->R == 1 ? 0 : (size_t)g * gp.R * FOCUS_D_G);
+    if ((e = cudaMemcpy2DAsync(set_ptr(g, HL.r), rw, rsrc, (size_t)p->R * FOCUS_D_G * 4, rw, BN,
+                               cudaMemcpyHostToDevice, xs)))
+      return e;
+    return cudaEventRecord(ev_in[g & 1], xs);
+  };
+  auto copy_out = [&](int g) -> cudaError_t {
+    cudaError_t e;
+    if ((e = cudaStreamWaitEvent(xs, ev_comp[g & 1], 0))) return e;
+    if ((e = cudaMemcpy2DAsync(o_h + (size_t)g * gp.H * p->d_head, p->H * d2, set_ptr(g, HL.o),
+                               gp.H * d2, gp.H * d2, BN, cudaMemcpyDeviceToHost, xs)))
+      return e;
+    if (lse_h &&
+        (e = cudaMemcpy2DAsync(lse_h + (size_t)g * gp.H * p->N, (size_t)p->H * p->N * 4,
+                               set_ptr(g, HL.lse), (size_t)gp.H * p->N * 4,
+                               (size_t)gp.H * p->N * 4, p->B, cudaMemcpyDeviceToHost, xs)))
+      return e;
+    return cudaSuccess;
+  };
+
+  if ((rc = cuda_rc(cudaMemcpyAsync(w + HL.C, C_h, (size_t)p->K * FOCUS_D_G * 4,
+                                    cudaMemcpyHostToDevice, xs))))
+    return cleanup(rc);
+  if ((rc = cuda_rc(copy_in(0)))) return cleanup(rc);
+  for (int g = 0; g < G; ++g) {
+    if (g + 1 < G && (rc = cuda_rc(copy_in(g + 1)))) return cleanup(rc);
+    // compute of group g: inputs landed; staging outputs of set g % 2 were copied out
+    // (copy_out(g - 2) precedes copy_in(g) on the copy stream, which the event covers)
+    if ((rc = cuda_rc(cudaStreamWaitEvent(cs, ev_in[g & 1], 0)))) return cleanup(rc);
+    rc = focus_attn_fwd(&gp, reinterpret_cast<const uint16_t*>(set_ptr(g, HL.q)),
+                        reinterpret_cast<const uint16_t*>(set_ptr(g, HL.k)),
+                        reinterpret_cast<const uint16_t*>(set_ptr(g, HL.v)),
+                        reinterpret_cast<const float*>(set_ptr(g, HL.r)),
+                        reinterpret_cast<const float*>(w + HL.C), nullptr,
+                        reinterpret_cast<uint16_t*>(set_ptr(g, HL.o)),
+                        reinterpret_cast<float*>(set_ptr(g, HL.lse)), w + HL.attn, attn_bytes, cs);
+    if (rc) return cleanup(rc);
+    if ((rc = cuda_rc(cudaEventRecord(ev_comp[g & 1], cs)))) return cleanup(rc);
+    if ((rc = cuda_rc(copy_out(g)))) return cleanup(rc);
+  }
+  return cleanup(FOCUS_OK);
+}
+
 int focus_get_status(const void* ws, void* stream) {
   if (!ws) return FOCUS_ERR_INVALID_ARG;
   cudaStream_t s = (cudaStream_t)stream;

@@ -87,3 +87,22 @@ def test_window_pairs_closed_form():
 
 def test_nseg_is_binomial():
     assert _params(K=8, top_k=2).nseg == 28 == math.comb(8, 2)
+
+
+def test_host_entry_sizes_and_argument_errors():
+    p = _params(H=8, H_kv=4, R=2)
+    assert focus.host_workspace_size(p) > focus.workspace_size(focus.Params(**{**p.__dict__, "H": 4, "H_kv": 2, "R": 1}))
+    assert focus.host_workspace_size(p, 3) == 0          # 3 does not divide H_kv
+    assert focus.host_workspace_size(p, 4) == 0          # 4 does not divide R = 2
+    assert focus.host_workspace_size(p, 2) > 0
+    E = {v: k for k, v in focus.ERRORS.items()}
+    P = ctypes.c_void_p
+    h = P(1 << 12)
+    n = focus.host_workspace_size(p)
+    same = P(1 << 20)
+    rc = focus._lib.focus_attn_fwd_host(ctypes.byref(p.c()), h, h, h, h, h, h, None, 0, P(1 << 12), n, same, same)
+    assert rc == E["FOCUS_ERR_INVALID_ARG"]               # one stream for both roles
+    rc = focus._lib.focus_attn_fwd_host(ctypes.byref(p.c()), h, h, h, None, h, h, None, 0, P(1 << 12), n, None, same)
+    assert rc == E["FOCUS_ERR_INVALID_ARG"]               # routing inputs are required
+    rc = focus._lib.focus_attn_fwd_host(ctypes.byref(p.c()), h, h, h, h, h, h, None, 0, P(1 << 12), n - 1, None, same)
+    assert rc == E["FOCUS_ERR_WORKSPACE"]

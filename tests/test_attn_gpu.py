@@ -77,11 +77,15 @@ def test_deterministic_across_calls():
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
 
-def test_host_buffer_entry_matches_device_entry():
-    wl = synth.WORKLOADS["tiny"]
-    x = synth.make_inputs(wl, seed=4, device="cpu")
+@pytest.mark.parametrize("name,n_groups", [("tiny", 0), ("gpt2_layer", 4), ("gpt2_layer", 3),
+                                           ("gqa4_R8_small", 0), ("gqa4_R8_small", 2)])
+def test_host_buffer_entry_matches_device_entry(name, n_groups):
+    """Grouped, copy-overlapped host entry = device entry, bit for bit (heads are
+    independent problems and each head's arithmetic is the same)."""
+    wl = SMALL[name] if name in SMALL else synth.WORKLOADS[name]
+    x = {k: v.pin_memory() for k, v in synth.make_inputs(wl, seed=4, device="cpu").items()}
     p = focus.Params.from_workload(wl)
-    o_h, l_h = focus.attn_fwd_host(p, x["q"], x["k"], x["v"], x["r"], x["C"])
+    o_h, l_h = focus.attn_fwd_host(p, x["q"], x["k"], x["v"], x["r"], x["C"], n_groups=n_groups)
     d = {k: v.cuda() for k, v in x.items()}
     o_d, l_d = focus.attn_fwd(p, d["q"], d["k"], d["v"], d["r"], d["C"])
     assert torch.equal(o_h, o_d.cpu()) and torch.equal(l_h, l_d.cpu())
