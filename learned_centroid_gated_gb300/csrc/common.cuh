@@ -39,7 +39,7 @@ struct PlanEnt {
 constexpr int kKeyTile = 128;     // keys per attention key tile
 constexpr int kChunk = 1024;      // tokens per bucketing chunk (one warp)
 constexpr int kSinkBlock = 256;   // tokens per Sinkhorn partial-reduction block
-constexpr int kAttnBM = 128;      // smallest query block of the long-range schedule
+constexpr int kAttnBM = 256;      // query rows per long-range work item
 constexpr int kKeySentinel = 0x7fffffff;
 
 struct WsLayout {
@@ -83,11 +83,5 @@ cudaError_t launch_attn_long_tc(const focus_params& p, const WsLayout& L, const 
 cudaError_t launch_attn_window_tc(const focus_params& p, const WsLayout& L, const bf16* q,
                                   const bf16* k, const bf16* v, char* ws, bf16* o, float* lse,
                                   float scale, cudaStream_t s);
-// attn.cu (mma.sync engine)
-cudaError_t launch_attn_long(const focus_params& p, const WsLayout& L, const uint32_t* mask,
-                             char* ws, float scale, cudaStream_t s);
-cudaError_t launch_attn_window(const focus_params& p, const WsLayout& L, const bf16* q,
-                               const bf16* k, const bf16* v, char* ws, bf16* o, float* lse,
-                               float scale, cudaStream_t s);
 
 }  // namespace focus

@@ -2,8 +2,6 @@
 // and the launch sequence on the caller's stream.  See include/focus.h.
 #include <math.h>
 #include <stdint.h>
-#include <stdlib.h>
-#include <string.h>
 
 #include "common.cuh"
 
@@ -72,16 +70,6 @@ int check_ws(const WsLayout& L, const void* ws, size_t ws_bytes) {
 }
 
 int cuda_rc(cudaError_t e) { return e == cudaSuccess ? FOCUS_OK : FOCUS_ERR_CUDA; }
-
-// Attention engine: tcgen05 (default) or the warp-level mma.sync engine, selected
-// by FOCUS_ATTN_ENGINE=mma for A/B comparison.
-bool use_mma_engine() {
-  static const bool mma = [] {
-    const char* e = getenv("FOCUS_ATTN_ENGINE");
-    return e && strcmp(e, "mma") == 0;
-  }();
-  return mma;
-}
 
 // Clears the status word and the schedule counter at the start of a call.
 cudaError_t reset_header(char* ws, cudaStream_t s) {
@@ -174,20 +162,15 @@ int focus_attn_fwd_ev(const focus_params* p, const uint16_t* q, const uint16_t* 
   }
   if ((rc = mark(1))) return rc;
   if ((rc = cuda_rc(launch_bucket(*p, L, mask, w, s)))) return rc;
-  const bool mma = use_mma_engine();
-  if ((rc = cuda_rc(launch_qtab(*p, L, w, mma ? kAttnBM : tc_block_rows(), s)))) return rc;
-  if (!mma && (rc = cuda_rc(launch_plan(*p, L, mask, w, tc_block_rows(), s)))) return rc;
+  if ((rc = cuda_rc(launch_qtab(*p, L, w, tc_block_rows(), s)))) return rc;
+  if ((rc = cuda_rc(launch_plan(*p, L, mask, w, tc_block_rows(), s)))) return rc;
   if ((rc = mark(2))) return rc;
   if ((rc = cuda_rc(launch_permute(*p, L, qb, kb, vb, w, s)))) return rc;
   if ((rc = mark(3))) return rc;
-  if ((rc = cuda_rc(mma ? launch_attn_long(*p, L, mask, w, scale, s)
-                        : launch_attn_long_tc(*p, L, mask, w, scale, s))))
-    return rc;
+  if ((rc = cuda_rc(launch_attn_long_tc(*p, L, mask, w, scale, s)))) return rc;
   if ((rc = mark(4))) return rc;
   bf16* ob = reinterpret_cast<bf16*>(o);
-  if ((rc = cuda_rc(mma ? launch_attn_window(*p, L, qb, kb, vb, w, ob, lse, scale, s)
-                        : launch_attn_window_tc(*p, L, qb, kb, vb, w, ob, lse, scale, s))))
-    return rc;
+  if ((rc = cuda_rc(launch_attn_window_tc(*p, L, qb, kb, vb, w, ob, lse, scale, s)))) return rc;
   return mark(5);
 }
 
