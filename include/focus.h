@@ -120,7 +120,7 @@ int focus_bucket(const focus_params* p, const uint32_t* mask, int32_t* perm_out,
  *   o        [B, N, H, d_head] bf16 out
  *   lse      [B, H, N] fp32 out (natural log of the scaled logits), may be NULL
  * Steps on `stream`: route (if mask_in is NULL), bucket, permuted copies of
- * Q/K/V, long-range attention over compatible segments, window attention with
+ * Q/K/V, window attention, long-range attention over compatible segments with
  * the union merge.
  */
 int focus_attn_fwd(const focus_params* p, const uint16_t* q, const uint16_t* k,
@@ -134,9 +134,9 @@ int focus_attn_fwd(const focus_params* p, const uint16_t* q, const uint16_t* k,
  *   stage_events  array of FOCUS_N_STAGE_EVENTS cudaEvent_t handles (cast to
  *                 void*) created by the caller, or NULL (then this is exactly
  *                 focus_attn_fwd). Recorded in order: [0] start, [1] after routing,
- *                 [2] after bucketing and the long-range schedule, [3] after the
- *                 permuted Q/K/V copies, [4] after long-range attention, [5] after
- *                 window attention and the union merge.
+ *                 [2] after bucketing, the long-range schedule and its plans, [3]
+ *                 after the permuted Q/K/V copies, [4] after window attention, [5]
+ *                 after long-range attention and the union merge.
  */
 #define FOCUS_N_STAGE_EVENTS 6
 int focus_attn_fwd_ev(const focus_params* p, const uint16_t* q, const uint16_t* k,

@@ -97,7 +97,7 @@ _lib.focus_attn_fwd_ev.argtypes = [_PP, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctyp
                                    ctypes.POINTER(ctypes.c_void_p)]
 _lib.focus_attn_fwd_ev.restype = ctypes.c_int
 N_STAGE_EVENTS = 6
-STAGES = ("route", "bucket", "permute", "attn_long", "attn_window")
+STAGES = ("route", "bucket", "permute", "attn_window", "attn_long")
 _lib.focus_route_static.argtypes = [_PP, _P, _P, _P, _P, _P]
 _lib.focus_route_static.restype = ctypes.c_int
 _lib.focus_get_status.argtypes = [_P, _P]

@@ -28,11 +28,13 @@
 // Barrier phases run on across items; a tile's P barrier also orders the previous
 // item's reads of O before the next item's first P V.
 //
+//   attn_tc<D, false>  window part (runs first), token order, keys (i - w, i];
+//                      writes the normalised partial O_w (fp32) and LSE_w.
 //   attn_tc<D, true>   long-range part: query block of one segment x the key
 //                      tiles of every compatible segment (permuted copies),
-//                      keys with pos_j <= pos_i - w.  Writes O_lr, LSE_lr.
-//   attn_tc<D, false>  window part in token order, keys (i - w, i]; merges
-//                      (O_lr, LSE_lr) and writes O (bf16) and LSE.
+//                      keys with pos_j <= pos_i - w; merges with (O_w, LSE_w)
+//                      and writes O (bf16) and LSE.  Long items run ~100 key
+//                      tiles, so the merge's loads cost little there.
 #include <math.h>
 
 #include <mutex>
@@ -89,8 +91,8 @@ struct TcArgs {
   const int* qtab_count;
   const PlanHead* plan_head;
   const PlanEnt* plan_ent;
-  float* o_lr;
-  float* lse_lr;
+  float* o_part;   // window pass output, [B, N, H, d] fp32, normalised
+  float* lse_part; // window pass LSE, [B, H, N]
   bf16* o;
   float* lse;
   int* status;
@@ -493,9 +495,41 @@ attn_tc(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensor
       gt += n;
       const int64_t orow = (((int64_t)it.b * a.N + qp) * a.H + it.h) * D;
       const int64_t lrow = ((int64_t)it.b * a.H + it.h) * a.N + qp;
-      if constexpr (LONG) {
-        const float inv = l > 0.0f ? 1.0f / l : 0.0f;
-        const float lse = l > 0.0f ? (m_use + log2f(l)) * kLn2 : -INFINITY;
+      if constexpr (!LONG) {
+        // window pass (runs first): normalised partial output and its LSE
+        const float inv = 1.0f / l;  // the diagonal key is always in the window
+        const float lse = (m_use + log2f(l)) * kLn2;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t y[32];
+          tmem_ld32(tO + 32 * c, y);
+          tmem_ld_wait(y);
+          if (row_ok) {
+            float4* dst = reinterpret_cast<float4*>(a.o_part + orow + 32 * c);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              dst[i] = make_float4(__uint_as_float(y[4 * i]) * inv, __uint_as_float(y[4 * i + 1]) * inv,
+                                   __uint_as_float(y[4 * i + 2]) * inv, __uint_as_float(y[4 * i + 3]) * inv);
+          }
+        }
+        if (row_ok) a.lse_part[lrow] = lse;
+      } else {
+        // long-range pass: one softmax over the union = LSE merge of this pass with
+        // the window pass (disjoint key sets); writes the final O and LSE
+        float wo = 0.0f, ww = 1.0f, lse = 0.0f;
+        if (row_ok) {
+          const float lse_w = a.lse_part[lrow];
+          lse = lse_w;
+          if (l > 0.0f) {
+            const float lse_o = (m_use + log2f(l)) * kLn2;
+            const float M = fmaxf(lse_w, lse_o);
+            const float ew = expf(lse_w - M), eo = expf(lse_o - M);
+            const float tot = ew + eo;
+            lse = M + logf(tot);
+            wo = eo / tot / l;
+            ww = ew / tot;
+          }
+        }
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t y[32];
@@ -507,47 +541,15 @@ attn_tc(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensor
             for (int i = 0; i < 32; ++i) y[i] = 0u;
           }
           if (row_ok) {
-            float4* dst = reinterpret_cast<float4*>(a.o_lr + orow + 32 * c);
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-              dst[i] = make_float4(__uint_as_float(y[4 * i]) * inv, __uint_as_float(y[4 * i + 1]) * inv,
-                                   __uint_as_float(y[4 * i + 2]) * inv, __uint_as_float(y[4 * i + 3]) * inv);
-          }
-        }
-        if (row_ok) a.lse_lr[lrow] = lse;
-      } else {
-        float ww = 0.0f, wl = 0.0f, lse = 0.0f;
-        if (row_ok) {
-          const float lse_w = (m_use + log2f(l)) * kLn2;
-          const float lse_l = a.lse_lr[lrow];
-          if (lse_l == -INFINITY) {
-            ww = 1.0f / l;
-            lse = lse_w;
-          } else {
-            const float M = fmaxf(lse_w, lse_l);
-            const float ew = expf(lse_w - M), el = expf(lse_l - M);
-            const float tot = ew + el;
-            lse = M + logf(tot);
-            ww = ew / tot / l;
-            wl = el / tot;
-          }
-        }
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t y[32];
-          tmem_ld32(tO + 32 * c, y);
-          tmem_ld_wait(y);
-          if (row_ok) {
-            const float4* src = reinterpret_cast<const float4*>(a.o_lr + orow + 32 * c);
+            const float4* src = reinterpret_cast<const float4*>(a.o_part + orow + 32 * c);
             uint32_t pk[16];
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-              float4 ol = make_float4(0.f, 0.f, 0.f, 0.f);
-              if (wl != 0.0f) ol = src[i];
-              pk[2 * i] = pack_bf16(__uint_as_float(y[4 * i]) * ww + ol.x * wl,
-                                    __uint_as_float(y[4 * i + 1]) * ww + ol.y * wl);
-              pk[2 * i + 1] = pack_bf16(__uint_as_float(y[4 * i + 2]) * ww + ol.z * wl,
-                                        __uint_as_float(y[4 * i + 3]) * ww + ol.w * wl);
+              const float4 ow = src[i];
+              pk[2 * i] = pack_bf16(__uint_as_float(y[4 * i]) * wo + ow.x * ww,
+                                    __uint_as_float(y[4 * i + 1]) * wo + ow.y * ww);
+              pk[2 * i + 1] = pack_bf16(__uint_as_float(y[4 * i + 2]) * wo + ow.z * ww,
+                                        __uint_as_float(y[4 * i + 3]) * wo + ow.w * ww);
             }
             uint4* dst = reinterpret_cast<uint4*>(a.o + orow + 32 * c);
 #pragma unroll
@@ -637,8 +639,8 @@ TcArgs make_args(const focus_params& p, const WsLayout& L, char* ws, float scale
   a.qtab_count = &reinterpret_cast<const WsHeader*>(ws)->qtab_count;
   a.plan_head = reinterpret_cast<const PlanHead*>(ws + L.plan_head);
   a.plan_ent = reinterpret_cast<const PlanEnt*>(ws + L.plan_ent);
-  a.o_lr = reinterpret_cast<float*>(ws + L.olr);
-  a.lse_lr = reinterpret_cast<float*>(ws + L.lselr);
+  a.o_part = reinterpret_cast<float*>(ws + L.olr);
+  a.lse_part = reinterpret_cast<float*>(ws + L.lselr);
   a.status = &reinterpret_cast<WsHeader*>(ws)->status;
   return a;
 }
@@ -660,10 +662,11 @@ cudaError_t launch_tc(const CUtensorMap& mq, const CUtensorMap& mk, const CUtens
 
 int tc_block_rows() { return BMQ; }
 
-cudaError_t launch_attn_long_tc(const focus_params& p, const WsLayout& L, const uint32_t* mask,
-                                char* ws, float scale, cudaStream_t s) {
-  (void)mask;
+cudaError_t launch_attn_long_tc(const focus_params& p, const WsLayout& L, char* ws, bf16* o,
+                                float* lse, float scale, cudaStream_t s) {
   TcArgs a = make_args(p, L, ws, scale);
+  a.o = o;
+  a.lse = lse;
   CUtensorMap mq, mk, mv;
   if (!make_map(&mq, ws + L.qp, p.d_head, (int64_t)p.B * p.H * p.N, 0) ||
       !make_map(&mk, ws + L.kp, p.d_head, (int64_t)p.B * p.H_kv * p.N, 0) ||
@@ -675,11 +678,9 @@ cudaError_t launch_attn_long_tc(const focus_params& p, const WsLayout& L, const 
 }
 
 cudaError_t launch_attn_window_tc(const focus_params& p, const WsLayout& L, const bf16* q,
-                                  const bf16* k, const bf16* v, char* ws, bf16* o, float* lse,
-                                  float scale, cudaStream_t s) {
+                                  const bf16* k, const bf16* v, char* ws, float scale,
+                                  cudaStream_t s) {
   TcArgs a = make_args(p, L, ws, scale);
-  a.o = o;
-  a.lse = lse;
   CUtensorMap mq, mk, mv;
   if (!make_map(&mq, q, p.d_head, (int64_t)p.B * p.N, p.H) ||
       !make_map(&mk, k, p.d_head, (int64_t)p.B * p.N, p.H_kv) ||

@@ -78,10 +78,10 @@ cudaError_t launch_permute(const focus_params& p, const WsLayout& L, const bf16*
                            const bf16* v, char* ws, cudaStream_t s);
 // attn_tc.cu (tcgen05 engine)
 int tc_block_rows();
-cudaError_t launch_attn_long_tc(const focus_params& p, const WsLayout& L, const uint32_t* mask,
-                                char* ws, float scale, cudaStream_t s);
+cudaError_t launch_attn_long_tc(const focus_params& p, const WsLayout& L, char* ws, bf16* o,
+                                float* lse, float scale, cudaStream_t s);
 cudaError_t launch_attn_window_tc(const focus_params& p, const WsLayout& L, const bf16* q,
-                                  const bf16* k, const bf16* v, char* ws, bf16* o, float* lse,
-                                  float scale, cudaStream_t s);
+                                  const bf16* k, const bf16* v, char* ws, float scale,
+                                  cudaStream_t s);
 
 }  // namespace focus

@@ -167,10 +167,10 @@ int focus_attn_fwd_ev(const focus_params* p, const uint16_t* q, const uint16_t* 
   if ((rc = mark(2))) return rc;
   if ((rc = cuda_rc(launch_permute(*p, L, qb, kb, vb, w, s)))) return rc;
   if ((rc = mark(3))) return rc;
-  if ((rc = cuda_rc(launch_attn_long_tc(*p, L, mask, w, scale, s)))) return rc;
+  if ((rc = cuda_rc(launch_attn_window_tc(*p, L, qb, kb, vb, w, scale, s)))) return rc;
   if ((rc = mark(4))) return rc;
-  bf16* ob = reinterpret_cast<bf16*>(o);
-  if ((rc = cuda_rc(launch_attn_window_tc(*p, L, qb, kb, vb, w, ob, lse, scale, s)))) return rc;
+  if ((rc = cuda_rc(launch_attn_long_tc(*p, L, w, reinterpret_cast<bf16*>(o), lse, scale, s))))
+    return rc;
   return mark(5);
 }
 
