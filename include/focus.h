@@ -196,6 +196,17 @@ int focus_attn_fwd_host(const focus_params* p, const uint16_t* q_h, const uint16
  * FOCUS_ERR_CUDA if the synchronisation itself failed. */
 int focus_get_status(const void* ws, void* stream);
 
+/*
+ * Diagnostic of the device-side failure path (no counterpart in the paper): runs
+ * the attention kernel on a tiny problem with its TMA producer held back and
+ * ~10 ms wait limits, so the tensor-core issuer's first bounded wait runs out. The
+ * kernel must raise FOCUS_ERR_TIMEOUT, abort every role, free its tensor memory
+ * and exit, leaving the CUDA context usable. Synchronises `stream` and returns
+ * the status word (FOCUS_ERR_TIMEOUT when the failure path works).
+ *   ws  device buffer of at least 1 MiB, 256-byte aligned (contents overwritten)
+ */
+int focus_selftest_timeout(void* ws, size_t ws_bytes, void* stream);
+
 /* Static, human-readable text for a status code. */
 const char* focus_strerror(int code);
 

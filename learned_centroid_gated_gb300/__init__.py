@@ -100,6 +100,8 @@ N_STAGE_EVENTS = 6
 STAGES = ("route", "bucket", "permute", "attn_window", "attn_long")
 _lib.focus_route_static.argtypes = [_PP, _P, _P, _P, _P, _P]
 _lib.focus_route_static.restype = ctypes.c_int
+_lib.focus_selftest_timeout.argtypes = [_P, ctypes.c_size_t, _P]
+_lib.focus_selftest_timeout.restype = ctypes.c_int
 _lib.focus_get_status.argtypes = [_P, _P]
 _lib.focus_get_status.restype = ctypes.c_int
 _lib.focus_strerror.argtypes = [ctypes.c_int]
@@ -295,6 +297,12 @@ def attn_fwd_host(p: Params, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, 
     Returns host (o, lse)."""
     o, lse = HostSession(p, device, n_groups)(q, k, v, r, C)
     return o.clone(), lse.clone()
+
+
+def selftest_timeout(device="cuda", stream=None) -> int:
+    """Run the device failure-path diagnostic; returns the status (-5 = FOCUS_ERR_TIMEOUT)."""
+    ws = torch.empty(1 << 20, dtype=torch.uint8, device=device)
+    return _lib.focus_selftest_timeout(_ptr(ws), ws.numel(), _stream(stream))
 
 
 def get_status(ws: torch.Tensor, stream=None) -> int:

@@ -96,6 +96,8 @@ struct TcArgs {
   bf16* o;
   float* lse;
   int* status;
+  long long timeout_cycles;  // limit of every bounded wait
+  int stall_producer;        // diagnostic: the producer issues nothing (waits run out)
 };
 
 // First index in [lo, hi) with P[index] > x (P ascending), or hi.
@@ -213,6 +215,7 @@ attn_tc(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensor
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   int* status = a.status;
+  const long long tlim = a.timeout_cycles;
 
   if (warp >= 8) {
     setmaxnreg_dec();
@@ -226,10 +229,10 @@ attn_tc(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensor
       int stage = 0, qcnt = 0, q_par = -1;
       uint32_t phase = 0;
       bool ok = true;
-      for (int x = blockIdx.x; ok && x < n_items; x += gridDim.x) {
+      for (int x = a.stall_producer ? n_items : blockIdx.x; ok && x < n_items; x += gridDim.x) {
         const Item it = decode<LONG>(a, x);
         if (!it.valid || it.n == 0) continue;
-        if (!(ok = mbar_wait(b_qe, (qcnt & 1) ^ 1, abort_flag, status))) break;
+        if (!(ok = mbar_wait(b_qe, (qcnt & 1) ^ 1, abort_flag, status, tlim))) break;
         mbar_expect_tx(b_q, 2 * L::TILE);
         for (int qt = 0; qt < 2; ++qt)
           for (int bx = 0; bx < L::BOXES; ++bx) {
@@ -257,7 +260,7 @@ attn_tc(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensor
             row = it.b * a.N + it.j_lo + t * BNK;
           }
           for (int kv = 0; kv < 2; ++kv) {
-            if (!(ok = mbar_wait(b_empty + 8 * stage, phase ^ 1, abort_flag, status))) break;
+            if (!(ok = mbar_wait(b_empty + 8 * stage, phase ^ 1, abort_flag, status, tlim))) break;
             const uint32_t full = b_full + 8 * stage;
             mbar_expect_tx(full, L::TILE);
             for (int bx = 0; bx < L::BOXES; ++bx) {
@@ -287,7 +290,7 @@ attn_tc(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensor
       const uint32_t r_base = smem_u32(sm + L::RING);
       auto slot = [&](int item) { return r_base + (item % NSTAGE) * L::TILE; };
       auto ring_wait = [&](int item) {
-        return mbar_wait(b_full + 8 * (item % NSTAGE), (item / NSTAGE) & 1, abort_flag, status);
+        return mbar_wait(b_full + 8 * (item % NSTAGE), (item / NSTAGE) & 1, abort_flag, status, tlim);
       };
       auto issue_S = [&](int qt, uint32_t kaddr) {
 #pragma unroll
@@ -310,7 +313,7 @@ attn_tc(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensor
         const Item it = decode<LONG>(a, x);
         if (!it.valid || it.n == 0) continue;
         const int n = it.n;
-        if (!(ok = mbar_wait(b_q, qcnt & 1, abort_flag, status) && ring_wait(ri))) break;
+        if (!(ok = mbar_wait(b_q, qcnt & 1, abort_flag, status, tlim) && ring_wait(ri))) break;
         ++qcnt;
         tc_fence_after();
         issue_S(0, slot(ri));
@@ -322,7 +325,7 @@ attn_tc(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensor
         for (int t = 0; t < n; ++t) {
           const int iv = ri + 2 * t + 1, ik = ri + 2 * t + 2;
           const uint32_t par = (uint32_t)((gt + t) & 1);
-          if (!(ok = ring_wait(iv) && mbar_wait(b_p, par, abort_flag, status))) break;
+          if (!(ok = ring_wait(iv) && mbar_wait(b_p, par, abort_flag, status, tlim))) break;
           tc_fence_after();
           issue_PV(0, slot(iv), t > 0);
           umma_commit(b_o);
@@ -332,7 +335,7 @@ attn_tc(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensor
             issue_S(0, slot(ik));
             umma_commit(b_s);
           }
-          if (!(ok = mbar_wait(b_p + 8, par, abort_flag, status))) break;
+          if (!(ok = mbar_wait(b_p + 8, par, abort_flag, status, tlim))) break;
           tc_fence_after();
           issue_PV(1, slot(iv), t > 0);
           umma_commit(b_o + 8);
@@ -395,7 +398,7 @@ attn_tc(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensor
           c_hi = min(min(BNK, it.j_hi - j0), qp - j0 + 1);
           need_mask = c_lo > 0 || c_hi < BNK;
         }
-        ok = mbar_wait(b_s + 8 * qt, (uint32_t)((gt + t) & 1), abort_flag, status);
+        ok = mbar_wait(b_s + 8 * qt, (uint32_t)((gt + t) & 1), abort_flag, status, tlim);
         if (!__all_sync(0xffffffffu, ok)) {
           ok = false;
           break;
@@ -485,7 +488,7 @@ attn_tc(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensor
       if (!ok) break;
       // ---- epilogue of this item ----
       if (n > 0) {
-        ok = mbar_wait(b_o + 8 * qt, (uint32_t)((gt + n - 1) & 1), abort_flag, status);
+        ok = mbar_wait(b_o + 8 * qt, (uint32_t)((gt + n - 1) & 1), abort_flag, status, tlim);
         if (!__all_sync(0xffffffffu, ok)) {
           ok = false;
           break;
@@ -642,6 +645,8 @@ TcArgs make_args(const focus_params& p, const WsLayout& L, char* ws, float scale
   a.o_part = reinterpret_cast<float*>(ws + L.olr);
   a.lse_part = reinterpret_cast<float*>(ws + L.lselr);
   a.status = &reinterpret_cast<WsHeader*>(ws)->status;
+  a.timeout_cycles = kTimeoutCycles;
+  a.stall_producer = 0;
   return a;
 }
 
@@ -661,6 +666,34 @@ cudaError_t launch_tc(const CUtensorMap& mq, const CUtensorMap& mk, const CUtens
 }  // namespace
 
 int tc_block_rows() { return BMQ; }
+
+// Diagnostic launch: the window kernel on a tiny problem with its producer held back
+// and ~10 ms waits, so the MMA issuer's first wait runs out, the CTA aborts (nothing
+// is in flight), frees its tensor memory and exits with FOCUS_ERR_TIMEOUT raised.
+cudaError_t launch_timeout_selftest(char* ws, size_t ws_bytes, cudaStream_t s) {
+  focus_params p{};
+  p.B = 1;
+  p.N = 256;
+  p.H = p.H_kv = 1;
+  p.d_head = 64;
+  p.R = 1;
+  p.K = 1;
+  p.top_k = 1;
+  p.w = 64;
+  WsLayout L{};
+  L.nseg = 1;
+  L.olr = 4096;
+  L.lselr = 4096 + 256 * 64 * 4;
+  if (ws_bytes < L.lselr + 256 * 4) return cudaErrorInvalidValue;
+  TcArgs a = make_args(p, L, ws, 0.125f);
+  a.timeout_cycles = 20000000LL;
+  a.stall_producer = 1;
+  CUtensorMap mq, mk, mv;  // valid maps over the workspace; nothing is loaded
+  if (!make_map(&mq, ws, 64, 256, 1) || !make_map(&mk, ws, 64, 256, 1) ||
+      !make_map(&mv, ws, 64, 256, 1))
+    return cudaErrorInvalidValue;
+  return launch_tc<64, false>(mq, mk, mv, a, 1, s);
+}
 
 cudaError_t launch_attn_long_tc(const focus_params& p, const WsLayout& L, char* ws, bf16* o,
                                 float* lse, float scale, cudaStream_t s) {

@@ -78,6 +78,7 @@ cudaError_t launch_permute(const focus_params& p, const WsLayout& L, const bf16*
                            const bf16* v, char* ws, cudaStream_t s);
 // attn_tc.cu (tcgen05 engine)
 int tc_block_rows();
+cudaError_t launch_timeout_selftest(char* ws, size_t ws_bytes, cudaStream_t s);
 cudaError_t launch_attn_long_tc(const focus_params& p, const WsLayout& L, char* ws, bf16* o,
                                 float* lse, float scale, cudaStream_t s);
 cudaError_t launch_attn_window_tc(const focus_params& p, const WsLayout& L, const bf16* q,

@@ -330,6 +330,18 @@ int focus_attn_fwd_host(const focus_params* p, const uint16_t* q_h, const uint16
   return cleanup(FOCUS_OK);
 }
 
+int focus_selftest_timeout(void* ws, size_t ws_bytes, void* stream) {
+  if (!ws) return FOCUS_ERR_INVALID_ARG;
+  if (!aligned(ws, 256)) return FOCUS_ERR_ALIGNMENT;
+  if (ws_bytes < ((size_t)1 << 20)) return FOCUS_ERR_WORKSPACE;
+  cudaStream_t s = (cudaStream_t)stream;
+  char* w = (char*)ws;
+  int rc;
+  if ((rc = cuda_rc(reset_header(w, s)))) return rc;
+  if ((rc = cuda_rc(launch_timeout_selftest(w, ws_bytes, s)))) return rc;
+  return focus_get_status(ws, stream);
+}
+
 int focus_get_status(const void* ws, void* stream) {
   if (!ws) return FOCUS_ERR_INVALID_ARG;
   cudaStream_t s = (cudaStream_t)stream;

@@ -42,16 +42,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 constexpr long long kTimeoutCycles = 4000000000LL;
 
 // Bounded wait for the phase with the given parity.  Returns false if the CTA is
-// aborting (abort flag set by any thread) or if this wait ran out, in which case it
-// raises FOCUS_ERR_TIMEOUT and sets the abort flag for the rest of the CTA.
+// aborting (abort flag set by any thread) or if this wait ran out after `limit`
+// cycles, in which case it raises FOCUS_ERR_TIMEOUT and sets the abort flag for the
+// rest of the CTA.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                          int* status) {
+                                          int* status, long long limit = kTimeoutCycles) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   for (;;) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
-    if (clock64() - t0 > kTimeoutCycles) {
+    if (clock64() - t0 > limit) {
       *abort_flag = 1;
       raise_status(status, FOCUS_ERR_TIMEOUT);
       return false;
