@@ -53,7 +53,7 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target CPU time of the oracle sample")
-    ap.add_argument("--sweep", choices=["table6"], default=None,
+    ap.add_argument("--sweep", choices=["table6", "decode"], default=None,
                     help="speedup of Focus over this build's own dense causal mode (K=1) "
                          "across context lengths, K=4 and K=8 (one JSON line)")
     return ap.parse_args()
@@ -445,10 +445,66 @@ def run_table6(args):
                       "rows": rows, "pages_table6_h100": TABLE6_PAGES}), flush=True)
 
 
+# -------------------------------------------------------------- decode --
+def run_decode(args):
+    """Decode step (newest token over its cache) per workload: time, tokens/s and
+    the HBM roofline (algorithmic bytes = the allowed keys' K and V rows of every KV
+    head + the masks + q and o)."""
+    import learned_centroid_gated_gb300 as focus
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    peaks, peak_src = load_peaks()
+    rows = []
+    for name in ("mha7b_32k", "gqa_128k", "extreme_1m"):
+        wl = synth.WORKLOADS[name]
+        x = synth.make_inputs(wl, seed=args.seed, device=dev)
+        p = focus.Params.from_workload(wl)
+        mask, _ = focus.route(p, x["r"], x["C"])
+        q_new = x["q"][:, wl.N - 1].contiguous()
+        m = mask.cpu().numpy().view(np.uint32)
+        allowed_keys = 0
+        for b in range(wl.B):
+            for rho in range(wl.R):
+                mm = m[b, rho]
+                i = wl.N - 1
+                j = np.arange(wl.N)
+                ok = (i - j < wl.w) | ((mm & mm[i]) != 0)
+                allowed_keys += int(ok.sum()) * (wl.H_kv // wl.R)
+        byts = allowed_keys * 2 * wl.d_head * 2 + wl.B * wl.R * wl.N * 4 + 2 * wl.B * wl.H * wl.d_head * 2
+        ws = torch.empty(focus.decode_workspace_size(p), dtype=torch.uint8, device=dev)
+        o = torch.empty(wl.B, wl.H, wl.d_head, dtype=torch.bfloat16, device=dev)
+        for _ in range(5):
+            focus.decode(p, q_new, x["k"], x["v"], mask, out=o, want_lse=False, ws=ws, stream=stream)
+        flush = torch.empty(256 * 2**20, dtype=torch.uint8, device=dev)  # > L2, between steps
+        times = []
+        for _ in range(20):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            focus.decode(p, q_new, x["k"], x["v"], mask, out=o, want_lse=False, ws=ws, stream=stream)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            times.append(e0.elapsed_time(e1))
+        ms = statistics.median(times)
+        gbs = byts / (ms / 1e3) / 1e9
+        rows.append({"workload": name, "ms": ms, "tokens_per_s": wl.B / (ms / 1e3),
+                     "algorithmic_bytes": byts, "achieved_gbs": gbs, "hbm_frac": gbs / peaks["hbm_gbs"],
+                     "allowed_key_fraction": allowed_keys / (wl.B * wl.H_kv * wl.N)})
+        del x, ws, flush
+        torch.cuda.empty_cache()
+    print(json.dumps({"sweep": "decode", "unit": "ms per decode step", "l2": "flushed before each step",
+                      "peak_hbm_gbs": peaks["hbm_gbs"], "peak_source": peak_src, "rows": rows}), flush=True)
+
+
 def main():
     args = parse_args()
     if args.sweep == "table6":
         run_table6(args)
+        return
+    if args.sweep == "decode":
+        run_decode(args)
         return
     if args.impl == "reference":
         run_reference(args)

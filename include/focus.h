@@ -197,6 +197,26 @@ int focus_attn_fwd_host(const focus_params* p, const uint16_t* q_h, const uint16
 int focus_get_status(const void* ws, void* stream);
 
 /*
+ * Decode step: the newest token of each sequence (position N - 1) attends to its
+ * cache over the same union set as focus_attn_fwd (window keys i - j < w, plus
+ * keys whose group bitmask meets the token's).
+ *   q        [B, H, d_head] bf16: queries of the newest tokens
+ *   k_cache, v_cache  [B, N, H_kv, d_head] bf16: all N cached tokens, the newest
+ *            token's key and value included at position N - 1
+ *   mask     [B, R, N] uint32: group bitmasks of all N tokens (the newest included;
+ *            e.g. from focus_route on its routing vector)
+ *   o        [B, H, d_head] bf16 out;  lse [B, H] fp32 out or NULL
+ *   ws       focus_decode_workspace_size(p) bytes
+ * p->N is the cache length including the newest token. Split over the keys in
+ * chunks of 512 (one CTA per chunk, KV head and up to 8 of its query heads), then
+ * an LSE merge of the chunks.
+ */
+size_t focus_decode_workspace_size(const focus_params* p);
+int focus_decode(const focus_params* p, const uint16_t* q, const uint16_t* k_cache,
+                 const uint16_t* v_cache, const uint32_t* mask, uint16_t* o, float* lse,
+                 void* ws, size_t ws_bytes, void* stream);
+
+/*
  * Diagnostic of the device-side failure path (no counterpart in the paper): runs
  * the attention kernel on a tiny problem with its TMA producer held back and
  * ~10 ms wait limits, so the tensor-core issuer's first bounded wait runs out. The

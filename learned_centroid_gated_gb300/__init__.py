@@ -100,6 +100,10 @@ N_STAGE_EVENTS = 6
 STAGES = ("route", "bucket", "permute", "attn_window", "attn_long")
 _lib.focus_route_static.argtypes = [_PP, _P, _P, _P, _P, _P]
 _lib.focus_route_static.restype = ctypes.c_int
+_lib.focus_decode_workspace_size.argtypes = [_PP]
+_lib.focus_decode_workspace_size.restype = ctypes.c_size_t
+_lib.focus_decode.argtypes = [_PP, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]
+_lib.focus_decode.restype = ctypes.c_int
 _lib.focus_selftest_timeout.argtypes = [_P, ctypes.c_size_t, _P]
 _lib.focus_selftest_timeout.restype = ctypes.c_int
 _lib.focus_get_status.argtypes = [_P, _P]
@@ -297,6 +301,32 @@ def attn_fwd_host(p: Params, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, 
     Returns host (o, lse)."""
     o, lse = HostSession(p, device, n_groups)(q, k, v, r, C)
     return o.clone(), lse.clone()
+
+
+def decode_workspace_size(p: Params) -> int:
+    return int(_lib.focus_decode_workspace_size(ctypes.byref(p.c())))
+
+
+def decode(p: Params, q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+           mask: torch.Tensor, *, out=None, lse=None, want_lse: bool = True, ws=None, stream=None):
+    """Decode step for the newest token of each sequence (position p.N - 1).
+    q [B, H, d] bf16; caches [B, N, H_kv, d] bf16 (newest token included); mask
+    [B, R, N] (int32 view of uint32).  Returns (o [B, H, d] bf16, lse [B, H] fp32)."""
+    for t in (q, k_cache, v_cache):
+        _bf16_bits(t)
+    if out is None:
+        out = torch.empty(p.B, p.H, p.d_head, dtype=torch.bfloat16, device=q.device)
+    if lse is None and want_lse:
+        lse = torch.empty(p.B, p.H, dtype=torch.float32, device=q.device)
+    need = decode_workspace_size(p)
+    if need == 0:
+        raise FocusError(-1, "focus_decode_workspace_size")
+    if ws is None or ws.numel() < need:
+        ws = torch.empty(need, dtype=torch.uint8, device=q.device)
+    _check(_lib.focus_decode(ctypes.byref(p.c()), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                             _ptr(mask.contiguous()), _ptr(out), _ptr(lse), _ptr(ws), ws.numel(),
+                             _stream(stream)), "focus_decode")
+    return out, lse
 
 
 def selftest_timeout(device="cuda", stream=None) -> int:

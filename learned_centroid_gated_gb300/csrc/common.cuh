@@ -76,6 +76,12 @@ cudaError_t launch_plan(const focus_params& p, const WsLayout& L, const uint32_t
                         int block_rows, cudaStream_t s);
 cudaError_t launch_permute(const focus_params& p, const WsLayout& L, const bf16* q, const bf16* k,
                            const bf16* v, char* ws, cudaStream_t s);
+// decode.cu
+int decode_chunks(int N);
+size_t decode_workspace_bytes(const focus_params& p);
+cudaError_t launch_decode(const focus_params& p, const bf16* q, const bf16* k, const bf16* v,
+                          const uint32_t* mask, bf16* o, float* lse, char* ws, float scale,
+                          cudaStream_t s);
 // attn_tc.cu (tcgen05 engine)
 int tc_block_rows();
 cudaError_t launch_timeout_selftest(char* ws, size_t ws_bytes, cudaStream_t s);

@@ -330,6 +330,31 @@ int focus_attn_fwd_host(const focus_params* p, const uint16_t* q_h, const uint16
   return cleanup(FOCUS_OK);
 }
 
+size_t focus_decode_workspace_size(const focus_params* p) {
+  if (check_params(p) != FOCUS_OK) return 0;
+  return decode_workspace_bytes(*p);
+}
+
+int focus_decode(const focus_params* p, const uint16_t* q, const uint16_t* k_cache,
+                 const uint16_t* v_cache, const uint32_t* mask, uint16_t* o, float* lse,
+                 void* ws, size_t ws_bytes, void* stream) {
+  int rc = check_params(p);
+  if (rc) return rc;
+  if (!q || !k_cache || !v_cache || !mask || !o) return FOCUS_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(o, 16) ||
+      !aligned(mask, 4) || !aligned(lse, 4))
+    return FOCUS_ERR_ALIGNMENT;
+  if (!ws) return FOCUS_ERR_INVALID_ARG;
+  if (!aligned(ws, 256)) return FOCUS_ERR_ALIGNMENT;
+  if (ws_bytes < decode_workspace_bytes(*p)) return FOCUS_ERR_WORKSPACE;
+  const float scale = p->softmax_scale > 0.0f ? p->softmax_scale : 1.0f / sqrtf((float)p->d_head);
+  return cuda_rc(launch_decode(*p, reinterpret_cast<const bf16*>(q),
+                               reinterpret_cast<const bf16*>(k_cache),
+                               reinterpret_cast<const bf16*>(v_cache), mask,
+                               reinterpret_cast<bf16*>(o), lse, (char*)ws, scale,
+                               (cudaStream_t)stream));
+}
+
 int focus_selftest_timeout(void* ws, size_t ws_bytes, void* stream) {
   if (!ws) return FOCUS_ERR_INVALID_ARG;
   if (!aligned(ws, 256)) return FOCUS_ERR_ALIGNMENT;
