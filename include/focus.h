@@ -55,11 +55,27 @@ extern "C" {
 #define FOCUS_D_G 16            /* routing dimension */
 #define FOCUS_MAX_K 32          /* groups representable in a uint32 bitmask */
 #define FOCUS_MAX_SEGMENTS 1024 /* C(K, top_k) limit of the mask-value bucketing */
+#define FOCUS_AUTO_SEGMENTS 64  /* FOCUS_SCHEDULE_AUTO picks group lists above this */
+
+/* Long-range schedule (focus_params.schedule).
+ *   SEGMENTS: tokens sorted by their exact group set (C(K, top_k) segments); a
+ *             query segment attends to every segment its set intersects, so each
+ *             key is met once.  Needs C(K, top_k) <= FOCUS_MAX_SEGMENTS.
+ *   GROUPS:   one position-ordered list per group (each token in top_k lists); a
+ *             query in list g counts key j only when g is the LOWEST group the two
+ *             share, so each key is still counted once; the top_k partial results
+ *             of a token are merged with the window's by log-sum-exp.  Any K, top_k.
+ *   AUTO:     SEGMENTS when C(K, top_k) <= FOCUS_AUTO_SEGMENTS, else GROUPS. */
+enum focus_schedule {
+  FOCUS_SCHEDULE_AUTO = 0,
+  FOCUS_SCHEDULE_SEGMENTS = 1,
+  FOCUS_SCHEDULE_GROUPS = 2
+};
 
 enum focus_status {
   FOCUS_OK = 0,
   FOCUS_ERR_INVALID_ARG = -1, /* null pointer, bad size or inconsistent shape */
-  FOCUS_ERR_UNSUPPORTED = -2, /* valid but not implemented (d_head, C(K,top_k)) */
+  FOCUS_ERR_UNSUPPORTED = -2, /* valid but not implemented (d_head; C(K,top_k) with SEGMENTS) */
   FOCUS_ERR_WORKSPACE = -3,   /* ws_bytes < focus_workspace_size() */
   FOCUS_ERR_CUDA = -4,        /* a CUDA runtime call or launch failed */
   FOCUS_ERR_TIMEOUT = -5,     /* a bounded device-side wait ran out */
@@ -70,11 +86,12 @@ enum focus_status {
 typedef struct focus_params {
   int32_t B, N, H, H_kv, d_head; /* d_head in {64, 128} */
   int32_t R;                     /* routing heads, divides H_kv */
-  int32_t K, top_k;              /* 1 <= top_k <= K <= 32, C(K, top_k) <= 1024 */
+  int32_t K, top_k;              /* 1 <= top_k <= K <= 32 */
   int32_t w;                     /* window, >= 1 */
   int32_t sinkhorn_iters;        /* 0 = plain top-k on the scores */
   float sinkhorn_eps;            /* score temperature for Sinkhorn, > 0 (1.0 typical) */
   float softmax_scale;           /* <= 0 selects 1 / sqrt(d_head) */
+  int32_t schedule;              /* enum focus_schedule; 0 = AUTO */
 } focus_params;
 
 /* Bytes of device workspace needed by focus_route, focus_bucket and
@@ -99,13 +116,26 @@ int focus_route(const focus_params* p, const float* r, const float* C, uint32_t*
                 float* margin_out, void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * Shape of the bucketing for these parameters: the schedule that runs
+ * (FOCUS_SCHEDULE_SEGMENTS or FOCUS_SCHEDULE_GROUPS, AUTO resolved), the number
+ * of segments (C(K, top_k) or K) and the rows per (b, routing head) (N or
+ * N * top_k).  Either output pointer may be NULL.  Returns the schedule, or a
+ * negative FOCUS_ERR_* code for invalid parameters.
+ */
+int focus_bucket_shape(const focus_params* p, int32_t* n_segments, int32_t* rows);
+
+/*
  * Bucketing of tokens by group bitmask (exposed for inspection and tests).
  *   mask        [B, R, N] uint32, exactly top_k of the low K bits set per token
- *   perm_out    [B, R, N] int32: token positions, stably sorted by the colex rank
- *               of their mask's k-subset (so positions ascend inside a segment)
- *   seg_off_out [B, R, C(K,top_k)+1] int32: segment start offsets into perm_out
+ *   perm_out    [B, R, rows] int32 (rows from focus_bucket_shape):
+ *               SEGMENTS: token positions stably sorted by the colex rank of
+ *               their mask's k-subset (positions ascend inside a segment);
+ *               GROUPS: the K group lists one after another, each the ascending
+ *               positions of the tokens whose mask has that bit
+ *   seg_off_out [B, R, n_segments + 1] int32: segment start offsets into perm_out
  * Either output may be NULL (the result then stays in the workspace only).
- * A mask with the wrong number of bits sets FOCUS_ERR_BOUNDS in the status word.
+ * A mask with the wrong number of bits sets FOCUS_ERR_BOUNDS in the status word
+ * (GROUPS then files such a token under groups 0..top_k-1).
  */
 int focus_bucket(const focus_params* p, const uint32_t* mask, int32_t* perm_out,
                  int32_t* seg_off_out, void* ws, size_t ws_bytes, void* stream);
@@ -121,7 +151,8 @@ int focus_bucket(const focus_params* p, const uint32_t* mask, int32_t* perm_out,
  *   lse      [B, H, N] fp32 out (natural log of the scaled logits), may be NULL
  * Steps on `stream`: route (if mask_in is NULL), bucket, permuted copies of
  * Q/K/V, window attention, long-range attention over compatible segments with
- * the union merge.
+ * the union merge (SEGMENTS), or over the group lists followed by a merge of the
+ * window part with each token's top_k list parts (GROUPS).
  */
 int focus_attn_fwd(const focus_params* p, const uint16_t* q, const uint16_t* k,
                    const uint16_t* v, const float* r, const float* C, const uint32_t* mask_in,

@@ -46,12 +46,17 @@ class FocusError(RuntimeError):
 class _Params(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in
                 ("B", "N", "H", "H_kv", "d_head", "R", "K", "top_k", "w", "sinkhorn_iters")] + \
-               [("sinkhorn_eps", ctypes.c_float), ("softmax_scale", ctypes.c_float)]
+               [("sinkhorn_eps", ctypes.c_float), ("softmax_scale", ctypes.c_float),
+                ("schedule", ctypes.c_int32)]
+
+SCHEDULE_AUTO, SCHEDULE_SEGMENTS, SCHEDULE_GROUPS = 0, 1, 2
 
 
 @dataclasses.dataclass(frozen=True)
 class Params:
-    """Problem description (focus_params).  softmax_scale <= 0 selects 1/sqrt(d_head)."""
+    """Problem description (focus_params).  softmax_scale <= 0 selects 1/sqrt(d_head);
+    schedule: SCHEDULE_AUTO, SCHEDULE_SEGMENTS (exact group sets) or SCHEDULE_GROUPS
+    (one list per group)."""
     B: int
     N: int
     H: int
@@ -64,6 +69,7 @@ class Params:
     sinkhorn_iters: int = 0
     sinkhorn_eps: float = 1.0
     softmax_scale: float = 0.0
+    schedule: int = 0
 
     @classmethod
     def from_workload(cls, wl, **kw) -> "Params":
@@ -76,7 +82,15 @@ class Params:
 
     @property
     def nseg(self) -> int:
-        return math.comb(self.K, self.top_k)
+        """Segments of the bucketing that runs: C(K, top_k) exact sets, or K lists."""
+        return self.bucket_shape()[1]
+
+    def bucket_shape(self):
+        """(schedule that runs, segments, permuted rows per (b, routing head))."""
+        nseg, rows = ctypes.c_int32(), ctypes.c_int32()
+        rc = _lib.focus_bucket_shape(ctypes.byref(self.c()), ctypes.byref(nseg), ctypes.byref(rows))
+        _check(rc if rc < 0 else 0, "focus_bucket_shape")
+        return rc, nseg.value, rows.value
 
     @property
     def scale(self) -> float:
@@ -89,6 +103,8 @@ _lib.focus_workspace_size.argtypes = [_PP]
 _lib.focus_workspace_size.restype = ctypes.c_size_t
 _lib.focus_route.argtypes = [_PP, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]
 _lib.focus_route.restype = ctypes.c_int
+_lib.focus_bucket_shape.argtypes = [_PP, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)]
+_lib.focus_bucket_shape.restype = ctypes.c_int
 _lib.focus_bucket.argtypes = [_PP, _P, _P, _P, _P, ctypes.c_size_t, _P]
 _lib.focus_bucket.restype = ctypes.c_int
 _lib.focus_attn_fwd.argtypes = [_PP, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]
@@ -207,9 +223,11 @@ def route_static(p: Params, r: torch.Tensor, C: torch.Tensor, *, margin: bool = 
 
 
 def bucket(p: Params, mask: torch.Tensor, *, ws=None, stream=None):
-    """Stable mask-value bucketing: perm [B, R, N] int32 and seg_off [B, R, nseg+1] int32."""
-    perm = torch.empty(p.B, p.R, p.N, dtype=torch.int32, device=mask.device)
-    seg = torch.empty(p.B, p.R, p.nseg + 1, dtype=torch.int32, device=mask.device)
+    """Stable bucketing: perm [B, R, rows] int32 and seg_off [B, R, nseg+1] int32, where
+    (nseg, rows) = (C(K, top_k), N) for exact-set segments and (K, N * top_k) for group lists."""
+    _, nseg, rows = p.bucket_shape()
+    perm = torch.empty(p.B, p.R, rows, dtype=torch.int32, device=mask.device)
+    seg = torch.empty(p.B, p.R, nseg + 1, dtype=torch.int32, device=mask.device)
     w = _ws(p, ws, mask.device)
     _check(_lib.focus_bucket(ctypes.byref(p.c()), _ptr(mask.contiguous()), _ptr(perm), _ptr(seg),
                              _ptr(w), w.numel(), _stream(stream)), "focus_bucket")

@@ -28,13 +28,22 @@
 // Barrier phases run on across items; a tile's P barrier also orders the previous
 // item's reads of O before the next item's first P V.
 //
-//   attn_tc<D, false>  window part (runs first), token order, keys (i - w, i];
+//   attn_tc<D, kWin>   window part (runs first), token order, keys (i - w, i];
 //                      writes the normalised partial O_w (fp32) and LSE_w.
-//   attn_tc<D, true>   long-range part: query block of one segment x the key
+//   attn_tc<D, kSeg>   long-range part: query block of one segment x the key
 //                      tiles of every compatible segment (permuted copies),
 //                      keys with pos_j <= pos_i - w; merges with (O_w, LSE_w)
 //                      and writes O (bf16) and LSE.  Long items run ~100 key
 //                      tiles, so the merge's loads cost little there.
+//   attn_tc<D, kGrp>   long-range part over group lists: query block of list g x
+//                      the keys of list g with pos_j <= pos_i - w, a key counted
+//                      only when g is the lowest group it shares with the query
+//                      (mask_i & mask_j & (2^g - 1) == 0).  The four warps of a
+//                      softmax warpgroup turn the tile's key masks into one
+//                      128-bit column set per group bit (warp ballots, shared
+//                      memory), and each row ORs the sets of its groups below g.
+//                      Writes the normalised part of list g into the token's slot
+//                      popc(mask_i & (2^g - 1)); a separate pass merges the slots.
 #include <math.h>
 
 #include <mutex>
@@ -64,6 +73,9 @@ constexpr float kRescale = 8.0f;  // log2 units: rescale O only when the max gro
 constexpr int kRegsLow = 104;
 constexpr int kRegsHigh = 192;
 
+// Kernel modes: window part, long-range part over exact-set segments, over group lists.
+enum : int { kWin = 0, kSeg = 1, kGrp = 2 };
+
 template <int D>
 struct Layout {
   static constexpr int BOX = QT * 128;        // one TMA box: 128 rows x 128 bytes
@@ -72,21 +84,29 @@ struct Layout {
   static constexpr int Q = 0;
   static constexpr int RING = Q + 2 * TILE;
   static constexpr int BAR = RING + NSTAGE * TILE;
-  // barrier block: q, q_empty, full[NSTAGE], empty[NSTAGE], s[2], p[2], o[2], drain
-  // (8 bytes each), then the TMEM address word and the abort flag
+  // barrier block: q, q_empty, full[NSTAGE], empty[NSTAGE], s[2], p[2], o[2], drain,
+  // key-set[2] (8 bytes each), then the TMEM address word and the abort flag
   static constexpr int BAR_Q = 0, BAR_QE = 8, BAR_FULL = 16, BAR_EMPTY = BAR_FULL + 8 * NSTAGE;
   static constexpr int BAR_S = BAR_EMPTY + 8 * NSTAGE, BAR_P = BAR_S + 16, BAR_O = BAR_P + 16;
-  static constexpr int BAR_DRAIN = BAR_O + 16, TMEM_SLOT = BAR_DRAIN + 8, ABORT = TMEM_SLOT + 4;
+  static constexpr int BAR_DRAIN = BAR_O + 16, BAR_KS = BAR_DRAIN + 8;
+  static constexpr int TMEM_SLOT = BAR_KS + 16, ABORT = TMEM_SLOT + 4;
   static constexpr int BAR_BYTES = 256;
   static_assert(ABORT + 4 <= BAR_BYTES, "barrier block overflow");
-  static constexpr int SMEM = BAR + BAR_BYTES + 1024;  // + barriers, + 1 KB alignment slack
+  // group lists: per query tile, two buffers of [32 group bits][4 words] key sets
+  static constexpr int KSET = BAR + BAR_BYTES;
+  static constexpr int KSET_BYTES = 2 * 2 * 32 * 4 * 4;
+  static constexpr int SMEM = KSET + KSET_BYTES + 1024;  // + 1 KB alignment slack
   static_assert(SMEM <= 232448, "shared memory budget");
 };
 
 struct TcArgs {
   int B, N, H, H_kv, R, w, nseg, qtab_cap;
+  int NR;     // permuted rows per (b, rho): N, or N * top_k with group lists
   float sl2;  // softmax scale * log2(e)
   const int* perm;
+  const uint32_t* pmask;  // group lists: mask of each permuted row
+  float* o_slot;          // group lists: [top_k][B, N, H, d] fp32 list parts
+  float* lse_slot;        // group lists: [top_k][B, H, N]
   const QBlock* qtab;
   const int* qtab_count;
   const PlanHead* plan_head;
@@ -128,6 +148,7 @@ struct Item {
   int n;                      // key tiles
   int u;                      // long: schedule entry
   int br;                     // long: b * R + rho
+  int seg;                    // long: segment (group list g)
   int j_lo, j_hi;             // window key range
 };
 
@@ -146,6 +167,7 @@ __device__ __forceinline__ Item decode(const TcArgs& a, int x) {
     const QBlock e = a.qtab[u];
     it.u = u;
     it.br = e.br;
+    it.seg = e.seg;
     it.b = e.br / a.R;
     const int rho = e.br % a.R;
     it.kvh = rho * nkv + kvl;
@@ -170,10 +192,12 @@ __device__ __forceinline__ Item decode(const TcArgs& a, int x) {
   return it;
 }
 
-template <int D, bool LONG>
+template <int D, int MODE>
 __global__ void __launch_bounds__(NTHREADS, 1)
 attn_tc(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
         const __grid_constant__ CUtensorMap mv, const TcArgs a, const int n_items) {
+  constexpr bool LONG = MODE != kWin;
+  constexpr bool GROUP = MODE == kGrp;
   using L = Layout<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -186,6 +210,7 @@ attn_tc(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensor
   const uint32_t b_s = smem_u32(bar) + L::BAR_S, b_p = smem_u32(bar) + L::BAR_P;  // + 8 * query tile
   const uint32_t b_o = smem_u32(bar) + L::BAR_O;
   const uint32_t b_drain = smem_u32(bar) + L::BAR_DRAIN;
+  const uint32_t b_ks = smem_u32(bar) + L::BAR_KS;  // + 8 * query tile
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(bar + L::TMEM_SLOT);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bar + L::ABORT);
 
@@ -206,6 +231,7 @@ attn_tc(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensor
       mbar_init(b_o + 8 * t, 1);
     }
     mbar_init(b_drain, 1);
+    for (int t = 0; t < 2; ++t) mbar_init(b_ks + 8 * t, 4);
     *abort_flag = 0;
     fence_barrier_init();
     fence_proxy_async_smem();
@@ -238,7 +264,7 @@ attn_tc(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensor
           for (int bx = 0; bx < L::BOXES; ++bx) {
             const uint32_t dst = smem_u32(sm + L::Q + qt * L::TILE + bx * L::BOX);
             if constexpr (LONG)
-              tma_load_2d(dst, &mq, 64 * bx, (it.b * a.H + it.h) * a.N + it.row0 + qt * QT, b_q);
+              tma_load_2d(dst, &mq, 64 * bx, (it.b * a.H + it.h) * a.NR + it.row0 + qt * QT, b_q);
             else
               tma_load_3d(dst, &mq, 64 * bx, it.h, it.b * a.N + it.row0 + qt * QT, b_q);
           }
@@ -251,7 +277,7 @@ attn_tc(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensor
         for (int t = 0; t < it.n && ok; ++t) {
           int row;
           if constexpr (LONG) {
-            row = (it.b * a.H_kv + it.kvh) * a.N + pe.start + t_in * BNK;
+            row = (it.b * a.H_kv + it.kvh) * a.NR + pe.start + t_in * BNK;
             if (++t_in * BNK >= pe.cnt && ++e < a.nseg) {
               t_in = 0;
               pe = a.plan_ent[(int64_t)it.u * a.nseg + e];
@@ -364,6 +390,7 @@ attn_tc(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensor
     const uint32_t tO = tmem + lane_off + 2 * BNK + qt * D;
     const float sl2 = a.sl2;
     int gt = 0;
+    int ks_cnt = 0;  // key-set barrier uses (group lists)
     bool ok = true;
     for (int x = blockIdx.x; ok && x < n_items; x += gridDim.x) {
       const Item it = decode<LONG>(a, x);
@@ -371,7 +398,7 @@ attn_tc(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensor
       const int n = it.n;
       const int rg = qt * QT + r;  // row in the item
       const bool row_ok = rg < it.rows;
-      const int* P = LONG ? a.perm + (int64_t)it.br * a.N : nullptr;
+      const int* P = LONG ? a.perm + (int64_t)it.br * a.NR : nullptr;
       int qp;
       if constexpr (LONG) qp = __ldg(P + it.row0 + min(rg, it.rows - 1));
       else qp = it.row0 + min(rg, it.rows - 1);
@@ -381,9 +408,21 @@ attn_tc(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensor
       if constexpr (LONG) {
         if (n > 0) pe = a.plan_ent[(int64_t)it.u * a.nseg];
       }
+      // group lists: this row's groups below g (keys sharing one of them are counted
+      // in a lower list), its slot, and the next key tile's masks (one per thread)
+      const int g = GROUP ? it.seg : 0;
+      const uint32_t* PM = GROUP ? a.pmask + (int64_t)it.br * a.NR : nullptr;
+      uint32_t m_low = 0u, mj_next = 0u;
+      const int kc = (warp & 3) * 32 + lane;  // key column this thread fetches
+      if constexpr (GROUP) {
+        m_low = __ldg(PM + it.row0 + min(rg, it.rows - 1)) & ((1u << g) - 1u);
+        if (g > 0 && n > 0 && kc < pe.cnt) mj_next = __ldg(PM + pe.start + kc);
+      }
       for (int t = 0; t < n; ++t) {
         int c_lo = 0, c_hi = BNK;
         bool need_mask;
+        uint32_t mj = 0u;
+        if constexpr (GROUP) mj = mj_next;
         if constexpr (LONG) {
           const int valid = min(BNK, pe.cnt - t_in * BNK);
           need_mask = t_in >= pe.nfull;
@@ -392,11 +431,46 @@ attn_tc(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensor
             t_in = 0;
             pe = a.plan_ent[(int64_t)it.u * a.nseg + e];
           }
+          if constexpr (GROUP) {  // (pe, t_in) now describe tile t + 1
+            if (g > 0 && t + 1 < n) {
+              const int c = t_in * BNK + kc;
+              mj_next = c < pe.cnt ? __ldg(PM + pe.start + c) : 0u;
+            }
+          }
         } else {
           const int j0 = it.j_lo + t * BNK;
           c_lo = max(0, qp - a.w + 1 - j0);
           c_hi = min(min(BNK, it.j_hi - j0), qp - j0 + 1);
           need_mask = c_lo > 0 || c_hi < BNK;
+        }
+        // key columns whose key shares a group below g with this row
+        uint32_t dk0 = 0u, dk1 = 0u, dk2 = 0u, dk3 = 0u;
+        if constexpr (GROUP) {
+          if (g > 0) {
+            uint32_t* ks = reinterpret_cast<uint32_t*>(sm + L::KSET) + (qt * 2 + (ks_cnt & 1)) * 128;
+            for (int bit = 0; bit < g; ++bit) {
+              const unsigned bal = __ballot_sync(0xffffffffu, (mj >> bit) & 1u);
+              if (lane == 0) ks[bit * 4 + (warp & 3)] = bal;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(b_ks + 8 * qt);
+            ok = mbar_wait(b_ks + 8 * qt, (uint32_t)(ks_cnt & 1), abort_flag, status, tlim);
+            if (!__all_sync(0xffffffffu, ok)) {
+              ok = false;
+              break;
+            }
+            ++ks_cnt;
+            uint32_t mm = m_low;
+            while (mm) {
+              const int bit = __ffs(mm) - 1;
+              mm &= mm - 1u;
+              const uint4 v = *reinterpret_cast<const uint4*>(ks + bit * 4);
+              dk0 |= v.x;
+              dk1 |= v.y;
+              dk2 |= v.z;
+              dk3 |= v.w;
+            }
+          }
         }
         ok = mbar_wait(b_s + 8 * qt, (uint32_t)((gt + t) & 1), abort_flag, status, tlim);
         if (!__all_sync(0xffffffffu, ok)) {
@@ -425,6 +499,19 @@ attn_tc(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensor
           mask32(x1, 32);
           mask32(x2, 64);
           mask32(x3, 96);
+        }
+        if constexpr (GROUP) {
+          if (__any_sync(0xffffffffu, (dk0 | dk1 | dk2 | dk3) != 0u)) {
+            auto drop32 = [&](uint32_t(&xx)[32], uint32_t ex) {
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                if ((ex >> i) & 1u) xx[i] = 0xff800000u;  // -inf
+            };
+            drop32(x0, dk0);
+            drop32(x1, dk1);
+            drop32(x2, dk2);
+            drop32(x3, dk3);
+          }
         }
         float ma = -INFINITY, mb = -INFINITY;
         auto max32 = [&](uint32_t(&xx)[32]) {
@@ -516,6 +603,33 @@ attn_tc(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensor
           }
         }
         if (row_ok) a.lse_part[lrow] = lse;
+      } else if constexpr (GROUP) {
+        // list g's normalised part into the token's slot; a row that met no key
+        // leaves weight 0 (LSE -inf) for the merge
+        const int slot = __popc(m_low);
+        const bool any = l > 0.0f;
+        const float inv = any ? 1.0f / l : 0.0f;
+        const float lse = any ? (m_use + log2f(l)) * kLn2 : -INFINITY;
+        float* os = a.o_slot + (int64_t)slot * a.B * a.N * a.H * D + orow;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t y[32];
+          if (n > 0) {
+            tmem_ld32(tO + 32 * c, y);
+            tmem_ld_wait(y);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) y[i] = 0u;
+          }
+          if (row_ok) {
+            float4* dst = reinterpret_cast<float4*>(os + 32 * c);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              dst[i] = make_float4(__uint_as_float(y[4 * i]) * inv, __uint_as_float(y[4 * i + 1]) * inv,
+                                   __uint_as_float(y[4 * i + 2]) * inv, __uint_as_float(y[4 * i + 3]) * inv);
+          }
+        }
+        if (row_ok) a.lse_slot[(int64_t)slot * a.B * a.H * a.N + lrow] = lse;
       } else {
         // long-range pass: one softmax over the union = LSE merge of this pass with
         // the window pass (disjoint key sets); writes the final O and LSE
@@ -635,9 +749,13 @@ TcArgs make_args(const focus_params& p, const WsLayout& L, char* ws, float scale
   a.R = p.R;
   a.w = p.w;
   a.nseg = L.nseg;
-  a.qtab_cap = p.B * p.R * ((p.N + BMQ - 1) / BMQ + L.nseg);
+  a.qtab_cap = L.qtab_cap;
+  a.NR = L.NR;
   a.sl2 = scale * kLog2e;
   a.perm = reinterpret_cast<const int*>(ws + L.perm);
+  a.pmask = reinterpret_cast<const uint32_t*>(ws + L.pmask);
+  a.o_slot = reinterpret_cast<float*>(ws + L.oslot);
+  a.lse_slot = reinterpret_cast<float*>(ws + L.lseslot);
   a.qtab = reinterpret_cast<const QBlock*>(ws + L.qtab);
   a.qtab_count = &reinterpret_cast<const WsHeader*>(ws)->qtab_count;
   a.plan_head = reinterpret_cast<const PlanHead*>(ws + L.plan_head);
@@ -650,16 +768,16 @@ TcArgs make_args(const focus_params& p, const WsLayout& L, char* ws, float scale
   return a;
 }
 
-template <int D, bool LONG>
+template <int D, int MODE>
 cudaError_t launch_tc(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                       const TcArgs& a, int n_items, cudaStream_t s) {
   const int smem = Layout<D>::SMEM;
-  cudaError_t e = cudaFuncSetAttribute(attn_tc<D, LONG>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = cudaFuncSetAttribute(attn_tc<D, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int sms = num_sms();
   const int grid = n_items < sms ? n_items : sms;
   if (grid < 1) return cudaSuccess;
-  attn_tc<D, LONG><<<grid, NTHREADS, smem, s>>>(mq, mk, mv, a, n_items);
+  attn_tc<D, MODE><<<grid, NTHREADS, smem, s>>>(mq, mk, mv, a, n_items);
   return cudaGetLastError();
 }
 
@@ -692,7 +810,7 @@ cudaError_t launch_timeout_selftest(char* ws, size_t ws_bytes, cudaStream_t s) {
   if (!make_map(&mq, ws, 64, 256, 1) || !make_map(&mk, ws, 64, 256, 1) ||
       !make_map(&mv, ws, 64, 256, 1))
     return cudaErrorInvalidValue;
-  return launch_tc<64, false>(mq, mk, mv, a, 1, s);
+  return launch_tc<64, kWin>(mq, mk, mv, a, 1, s);
 }
 
 cudaError_t launch_attn_long_tc(const focus_params& p, const WsLayout& L, char* ws, bf16* o,
@@ -701,13 +819,16 @@ cudaError_t launch_attn_long_tc(const focus_params& p, const WsLayout& L, char* 
   a.o = o;
   a.lse = lse;
   CUtensorMap mq, mk, mv;
-  if (!make_map(&mq, ws + L.qp, p.d_head, (int64_t)p.B * p.H * p.N, 0) ||
-      !make_map(&mk, ws + L.kp, p.d_head, (int64_t)p.B * p.H_kv * p.N, 0) ||
-      !make_map(&mv, ws + L.vp, p.d_head, (int64_t)p.B * p.H_kv * p.N, 0))
+  if (!make_map(&mq, ws + L.qp, p.d_head, (int64_t)p.B * p.H * L.NR, 0) ||
+      !make_map(&mk, ws + L.kp, p.d_head, (int64_t)p.B * p.H_kv * L.NR, 0) ||
+      !make_map(&mv, ws + L.vp, p.d_head, (int64_t)p.B * p.H_kv * L.NR, 0))
     return cudaErrorInvalidValue;
   const int n_items = a.qtab_cap * (p.H / p.R);
-  return p.d_head == 64 ? launch_tc<64, true>(mq, mk, mv, a, n_items, s)
-                        : launch_tc<128, true>(mq, mk, mv, a, n_items, s);
+  if (L.group)
+    return p.d_head == 64 ? launch_tc<64, kGrp>(mq, mk, mv, a, n_items, s)
+                          : launch_tc<128, kGrp>(mq, mk, mv, a, n_items, s);
+  return p.d_head == 64 ? launch_tc<64, kSeg>(mq, mk, mv, a, n_items, s)
+                        : launch_tc<128, kSeg>(mq, mk, mv, a, n_items, s);
 }
 
 cudaError_t launch_attn_window_tc(const focus_params& p, const WsLayout& L, const bf16* q,
@@ -720,8 +841,8 @@ cudaError_t launch_attn_window_tc(const focus_params& p, const WsLayout& L, cons
       !make_map(&mv, v, p.d_head, (int64_t)p.B * p.N, p.H_kv))
     return cudaErrorInvalidValue;
   const int n_items = p.B * p.H * ((p.N + BMQ - 1) / BMQ);
-  return p.d_head == 64 ? launch_tc<64, false>(mq, mk, mv, a, n_items, s)
-                        : launch_tc<128, false>(mq, mk, mv, a, n_items, s);
+  return p.d_head == 64 ? launch_tc<64, kWin>(mq, mk, mv, a, n_items, s)
+                        : launch_tc<128, kWin>(mq, mk, mv, a, n_items, s);
 }
 
 }  // namespace focus

@@ -9,6 +9,13 @@
 // attends to whole key segments T with mask(S) & mask(T) != 0: every key appears
 // once in a query's candidate list, so the union softmax needs no deduplication,
 // and the tiles inside a segment are dense.
+//
+// When C(K, top_k) is large (e.g. K = 32, top_k = 4 gives 35960 sets) the
+// segments are too many and too small for dense tiles, so a second schedule keeps
+// one position-ordered list per GROUP instead (a token appears in its top_k
+// lists; rows per (b, rho) are N * top_k).  The attention kernel then counts a
+// key only in the list of the lowest group it shares with the query, which keeps
+// "each key once" without a per-set split.
 #include "common.cuh"
 
 namespace focus {
@@ -135,6 +142,65 @@ bucket_scatter(int N, int K, int top_k, int nseg, const uint32_t* __restrict__ m
   }
 }
 
+// Group-list schedule.  A mask with the wrong number of bits (or bits >= K) is
+// filed under groups 0..top_k-1 so that every token still fills top_k rows.
+__device__ __forceinline__ uint32_t group_bits(uint32_t m, int K, int top_k, int* status) {
+  if ((K < 32 && (m >> K) != 0u) || __popc(m) != top_k) {
+    if (status) raise_status(status, FOCUS_ERR_BOUNDS);
+    return top_k >= 32 ? 0xffffffffu : (1u << top_k) - 1u;
+  }
+  return m;
+}
+
+// List sizes over one chunk of kChunk tokens; one warp per chunk, lane g counts
+// group g.  grid = (nchunk, B*R); hist layout as bucket_hist with nseg = K.
+__global__ void __launch_bounds__(32)
+group_hist(int N, int K, int top_k, const uint32_t* __restrict__ mask, int* __restrict__ hist,
+           int* status) {
+  const int br = blockIdx.y, chunk = blockIdx.x, lane = threadIdx.x;
+  const uint32_t* m = mask + (int64_t)br * N;
+  const int n0 = chunk * kChunk;
+  int cnt = 0;
+  for (int it = 0; it < kChunk / 32; ++it) {
+    const int n = n0 + it * 32 + lane;
+    const uint32_t mm = n < N ? group_bits(m[n], K, top_k, status) : 0u;
+    for (int g = 0; g < K; ++g) {
+      const unsigned bal = __ballot_sync(0xffffffffu, (mm >> g) & 1u);
+      if (lane == g) cnt += __popc(bal);
+    }
+  }
+  if (lane < K) hist[((int64_t)br * gridDim.x + chunk) * K + lane] = cnt;
+}
+
+// Stable scatter into the K lists: perm[list base + rank] = n, and the token's
+// mask beside it (pmask), which the attention kernel reads for the lowest-group
+// test.  Same chunking as group_hist; lane g carries list g's cursor.
+__global__ void __launch_bounds__(32)
+group_scatter(int N, int NR, int K, int top_k, const uint32_t* __restrict__ mask,
+              const int* __restrict__ cbase, int* __restrict__ perm, uint32_t* __restrict__ pmask) {
+  const int br = blockIdx.y, chunk = blockIdx.x, lane = threadIdx.x;
+  int cur = lane < K ? cbase[((int64_t)br * gridDim.x + chunk) * K + lane] : 0;
+  const uint32_t* m = mask + (int64_t)br * N;
+  int* P = perm + (int64_t)br * NR;
+  uint32_t* PM = pmask + (int64_t)br * NR;
+  const int n0 = chunk * kChunk;
+  for (int it = 0; it < kChunk / 32; ++it) {
+    const int n = n0 + it * 32 + lane;
+    const uint32_t mm = n < N ? group_bits(m[n], K, top_k, nullptr) : 0u;
+    for (int g = 0; g < K; ++g) {
+      const bool in = (mm >> g) & 1u;
+      const unsigned bal = __ballot_sync(0xffffffffu, in);
+      const int base = __shfl_sync(0xffffffffu, cur, g);
+      if (in) {
+        const int dst = base + __popc(bal & lanemask_lt());
+        P[dst] = n;
+        PM[dst] = mm;
+      }
+      if (lane == g) cur += __popc(bal);
+    }
+  }
+}
+
 // Long-range schedule: one entry per query block of bm rows inside a segment,
 // ordered by descending position of the block's last row (the blocks with the most
 // candidate keys start first).  Single CTA.
@@ -142,7 +208,7 @@ constexpr int kTabThreads = 1024;
 constexpr int kTabBuckets = 4096;
 
 __global__ void __launch_bounds__(kTabThreads)
-build_qtab(int N, int nseg, int BR, int bm, const int* __restrict__ seg_off, const int* __restrict__ perm,
+build_qtab(int N, int NR, int nseg, int BR, int bm, const int* __restrict__ seg_off, const int* __restrict__ perm,
            int* __restrict__ entoff, QBlock* __restrict__ qtab, int* __restrict__ qtab_count) {
   __shared__ int bucket[kTabBuckets];
   __shared__ int wsum[32];
@@ -206,7 +272,7 @@ build_qtab(int N, int nseg, int BR, int bm, const int* __restrict__ seg_off, con
       const int cnt = so[s + 1] - so[s];
       const int row0 = so[s] + t * bm;
       const int rows = min(bm, cnt - t * bm);
-      const int last = perm[(int64_t)br * N + row0 + rows - 1];
+      const int last = perm[(int64_t)br * NR + row0 + rows - 1];
       const int key = (N - 1 - last) >> shift;
       if (pass == 0) {
         atomicAdd(&bucket[key], 1);
@@ -260,20 +326,21 @@ __device__ __forceinline__ int upper_bound_pos(const int* __restrict__ P, int lo
 
 // Long-range plan: for query block u (segment S, positions p_lo..p_hi), every
 // segment T with mask(S) & mask(T) != 0 and keys at pos <= p_hi - w, in segment
-// order.  One warp per block; lanes take segments in parallel.
+// order; with group lists, the block's own list only.  One warp per block; lanes
+// take segments in parallel.
 __global__ void __launch_bounds__(32)
-build_plan(int N, int w, int nseg, const int* __restrict__ seg_off, const int* __restrict__ perm,
-           const uint32_t* __restrict__ mask, const QBlock* __restrict__ qtab,
-           const int* __restrict__ qtab_count, PlanHead* __restrict__ heads,
-           PlanEnt* __restrict__ ents) {
+build_plan(int N, int NR, int w, int nseg, int group, const int* __restrict__ seg_off,
+           const int* __restrict__ perm, const uint32_t* __restrict__ mask,
+           const QBlock* __restrict__ qtab, const int* __restrict__ qtab_count,
+           PlanHead* __restrict__ heads, PlanEnt* __restrict__ ents) {
   const int u = blockIdx.x, lane = threadIdx.x;
   if (u >= *qtab_count) return;
   const QBlock e = qtab[u];
-  const int* P = perm + (int64_t)e.br * N;
+  const int* P = perm + (int64_t)e.br * NR;
   const int* SO = seg_off + (int64_t)e.br * (nseg + 1);
   const uint32_t* M = mask + (int64_t)e.br * N;
   const int p_lo = __ldg(P + e.row0), p_hi = __ldg(P + e.row0 + e.rows - 1);
-  const uint32_t mS = __ldg(M + p_lo);
+  const uint32_t mS = group ? 0u : __ldg(M + p_lo);
   PlanEnt* out = ents + (int64_t)u * nseg;
   int n_ent = 0, n_tiles = 0;
   for (int T0 = 0; T0 < nseg; T0 += 32) {
@@ -282,7 +349,8 @@ build_plan(int N, int w, int nseg, const int* __restrict__ seg_off, const int* _
     PlanEnt pe{0, 0, 0, 0};
     if (T < nseg) {
       const int s0 = __ldg(SO + T), s1 = __ldg(SO + T + 1);
-      if (s1 > s0 && (__ldg(M + __ldg(P + s0)) & mS)) {
+      const bool compatible = group ? T == e.seg : (s1 > s0 && (__ldg(M + __ldg(P + s0)) & mS));
+      if (s1 > s0 && compatible) {
         const int hi = upper_bound_pos(P, s0, s1, p_hi - w) - s0;
         if (hi > 0) {
           ok = true;
@@ -303,13 +371,14 @@ build_plan(int N, int w, int nseg, const int* __restrict__ seg_off, const int* _
 }
 
 // Permuted, head-major copies: Qp[b][h][n'][:] = q[b][perm[n']][h][:] for the heads
-// of routing head rho, and likewise K/V for its KV heads.  One CTA per permuted row.
+// of routing head rho, and likewise K/V for its KV heads; NR permuted rows per
+// (b, rho).  One CTA per permuted row.
 __global__ void __launch_bounds__(256)
-permute_qkv(int N, int H, int H_kv, int R, int d, const int* __restrict__ perm,
+permute_qkv(int N, int NR, int H, int H_kv, int R, int d, const int* __restrict__ perm,
             const uint4* __restrict__ q, const uint4* __restrict__ k, const uint4* __restrict__ v,
             uint4* __restrict__ qp, uint4* __restrict__ kp, uint4* __restrict__ vp) {
-  const int64_t row = blockIdx.x;  // (b * R + rho) * N + n'
-  const int br = (int)(row / N), np = (int)(row % N);
+  const int64_t row = blockIdx.x;  // (b * R + rho) * NR + n'
+  const int br = (int)(row / NR), np = (int)(row % NR);
   const int b = br / R, rho = br % R;
   const int n = perm[row];
   const int hq = H / R, hkv = H_kv / R;
@@ -318,12 +387,12 @@ permute_qkv(int N, int H, int H_kv, int R, int d, const int* __restrict__ perm,
   for (int i = threadIdx.x; i < nq + 2 * nk; i += blockDim.x) {
     if (i < nq) {
       const int hh = rho * hq + i / vec, c = i % vec;
-      qp[(((int64_t)b * H + hh) * N + np) * vec + c] = q[(((int64_t)b * N + n) * H + hh) * vec + c];
+      qp[(((int64_t)b * H + hh) * NR + np) * vec + c] = q[(((int64_t)b * N + n) * H + hh) * vec + c];
     } else {
       const int j = (i - nq) % nk;
       const int hh = rho * hkv + j / vec, c = j % vec;
       const int64_t src = (((int64_t)b * N + n) * H_kv + hh) * vec + c;
-      const int64_t dst = (((int64_t)b * H_kv + hh) * N + np) * vec + c;
+      const int64_t dst = (((int64_t)b * H_kv + hh) * NR + np) * vec + c;
       if (i < nq + nk) kp[dst] = k[src]; else vp[dst] = v[src];
     }
   }
@@ -339,8 +408,15 @@ cudaError_t launch_bucket(const focus_params& p, const WsLayout& L, const uint32
   int* segoff = reinterpret_cast<int*>(ws + L.segoff);
   int* cbase = reinterpret_cast<int*>(ws + L.cbase);
   int* perm = reinterpret_cast<int*>(ws + L.perm);
-  const size_t shm = sizeof(int) * L.nseg;
   dim3 grid(L.nchunk, BR);
+  if (L.group) {
+    uint32_t* pmask = reinterpret_cast<uint32_t*>(ws + L.pmask);
+    group_hist<<<grid, 32, 0, s>>>(p.N, p.K, p.top_k, mask, hist, status);
+    bucket_scan<<<BR, 1024, 0, s>>>(L.nseg, L.nchunk, hist, segoff, cbase);
+    group_scatter<<<grid, 32, 0, s>>>(p.N, L.NR, p.K, p.top_k, mask, cbase, perm, pmask);
+    return cudaGetLastError();
+  }
+  const size_t shm = sizeof(int) * L.nseg;
   bucket_hist<<<grid, 32, shm, s>>>(p.N, p.K, p.top_k, L.nseg, mask, hist, status);
   bucket_scan<<<BR, 1024, 0, s>>>(L.nseg, L.nchunk, hist, segoff, cbase);
   bucket_scatter<<<grid, 32, shm, s>>>(p.N, p.K, p.top_k, L.nseg, mask, cbase, perm);
@@ -350,7 +426,7 @@ cudaError_t launch_bucket(const focus_params& p, const WsLayout& L, const uint32
 cudaError_t launch_qtab(const focus_params& p, const WsLayout& L, char* ws, int block_rows,
                         cudaStream_t s) {
   WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
-  build_qtab<<<1, kTabThreads, 0, s>>>(p.N, L.nseg, p.B * p.R, block_rows,
+  build_qtab<<<1, kTabThreads, 0, s>>>(p.N, L.NR, L.nseg, p.B * p.R, block_rows,
                                        reinterpret_cast<int*>(ws + L.segoff),
                                        reinterpret_cast<int*>(ws + L.perm),
                                        reinterpret_cast<int*>(ws + L.entoff),
@@ -360,8 +436,9 @@ cudaError_t launch_qtab(const focus_params& p, const WsLayout& L, char* ws, int 
 
 cudaError_t launch_plan(const focus_params& p, const WsLayout& L, const uint32_t* mask, char* ws,
                         int block_rows, cudaStream_t s) {
-  const int cap = p.B * p.R * ((p.N + block_rows - 1) / block_rows + L.nseg);
-  build_plan<<<cap, 32, 0, s>>>(p.N, p.w, L.nseg, reinterpret_cast<const int*>(ws + L.segoff),
+  const int cap = p.B * p.R * ((L.NR + block_rows - 1) / block_rows + L.nseg);
+  build_plan<<<cap, 32, 0, s>>>(p.N, L.NR, p.w, L.nseg, L.group,
+                                reinterpret_cast<const int*>(ws + L.segoff),
                                 reinterpret_cast<const int*>(ws + L.perm), mask,
                                 reinterpret_cast<const QBlock*>(ws + L.qtab),
                                 &reinterpret_cast<const WsHeader*>(ws)->qtab_count,
@@ -372,9 +449,9 @@ cudaError_t launch_plan(const focus_params& p, const WsLayout& L, const uint32_t
 
 cudaError_t launch_permute(const focus_params& p, const WsLayout& L, const bf16* q, const bf16* k,
                            const bf16* v, char* ws, cudaStream_t s) {
-  const int64_t rows = (int64_t)p.B * p.R * p.N;
+  const int64_t rows = (int64_t)p.B * p.R * L.NR;
   permute_qkv<<<(unsigned)rows, 256, 0, s>>>(
-      p.N, p.H, p.H_kv, p.R, p.d_head, reinterpret_cast<const int*>(ws + L.perm),
+      p.N, L.NR, p.H, p.H_kv, p.R, p.d_head, reinterpret_cast<const int*>(ws + L.perm),
       reinterpret_cast<const uint4*>(q), reinterpret_cast<const uint4*>(k),
       reinterpret_cast<const uint4*>(v), reinterpret_cast<uint4*>(ws + L.qp),
       reinterpret_cast<uint4*>(ws + L.kp), reinterpret_cast<uint4*>(ws + L.vp));

@@ -42,11 +42,17 @@ constexpr int kSinkBlock = 256;   // tokens per Sinkhorn partial-reduction block
 constexpr int kAttnBM = 256;      // query rows per long-range work item
 constexpr int kKeySentinel = 0x7fffffff;
 
+// Workspace layout.  Segment schedule: nseg = C(K, top_k) segments over NR = N rows
+// per (b, rho).  Group schedule: nseg = K lists over NR = N * top_k rows, plus the
+// permuted masks (pmask) and top_k per-list partial results per token (oslot,
+// lseslot: [top_k][B, N, H, d] fp32 and [top_k][B, H, N]).
 struct WsLayout {
-  size_t hdr, mask, beta, skpart, hist, segoff, cbase, perm, entoff, qtab, plan_head, plan_ent, qp, kp,
-      vp, olr, lselr;
+  size_t hdr, mask, beta, skpart, hist, segoff, cbase, perm, pmask, entoff, qtab, plan_head,
+      plan_ent, qp, kp, vp, olr, lselr, oslot, lseslot;
   size_t total;
   int nseg, nchunk, nblk_sk, qtab_cap;
+  int group;  // 1: group-list schedule
+  int NR;     // permuted rows per (b, rho)
 };
 
 // Binomial coefficient C(n, r) for n <= 32 (fits uint32 for all r).
@@ -76,6 +82,9 @@ cudaError_t launch_plan(const focus_params& p, const WsLayout& L, const uint32_t
                         int block_rows, cudaStream_t s);
 cudaError_t launch_permute(const focus_params& p, const WsLayout& L, const bf16* q, const bf16* k,
                            const bf16* v, char* ws, cudaStream_t s);
+// merge.cu (group schedule)
+cudaError_t launch_merge_slots(const focus_params& p, const WsLayout& L, const char* ws, bf16* o,
+                               float* lse, cudaStream_t s);
 // decode.cu
 int decode_chunks(int N);
 size_t decode_workspace_bytes(const focus_params& p);

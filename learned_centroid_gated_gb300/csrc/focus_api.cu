@@ -10,6 +10,14 @@ namespace {
 
 bool aligned(const void* ptr, size_t a) { return ((uintptr_t)ptr % a) == 0; }
 
+// The schedule that runs: group lists when asked for, or under AUTO when the
+// exact-set segments would be more than FOCUS_AUTO_SEGMENTS.
+bool use_groups(const focus_params& p) {
+  if (p.schedule == FOCUS_SCHEDULE_GROUPS) return true;
+  if (p.schedule == FOCUS_SCHEDULE_SEGMENTS) return false;
+  return binom(p.K, p.top_k) > (uint32_t)FOCUS_AUTO_SEGMENTS;
+}
+
 // Shape checks shared by every entry point (host only, nothing launched).
 int check_params(const focus_params* p) {
   if (!p) return FOCUS_ERR_INVALID_ARG;
@@ -19,10 +27,13 @@ int check_params(const focus_params* p) {
   if (p->H % p->H_kv != 0 || p->H_kv % p->R != 0) return FOCUS_ERR_INVALID_ARG;
   if (p->K > FOCUS_MAX_K || p->top_k > p->K) return FOCUS_ERR_INVALID_ARG;
   if (p->sinkhorn_iters > 0 && !(p->sinkhorn_eps > 0.0f)) return FOCUS_ERR_INVALID_ARG;
+  if (p->schedule < FOCUS_SCHEDULE_AUTO || p->schedule > FOCUS_SCHEDULE_GROUPS)
+    return FOCUS_ERR_INVALID_ARG;
   if (p->d_head != 64 && p->d_head != 128) return FOCUS_ERR_UNSUPPORTED;
-  if (binom(p->K, p->top_k) > (uint32_t)FOCUS_MAX_SEGMENTS) return FOCUS_ERR_UNSUPPORTED;
-  // 32-bit row indices: B * max(H, R) * N rows must fit in int32
-  const int64_t rows = (int64_t)p->B * (p->H > p->R ? p->H : p->R) * p->N;
+  const bool group = use_groups(*p);
+  if (!group && binom(p->K, p->top_k) > (uint32_t)FOCUS_MAX_SEGMENTS) return FOCUS_ERR_UNSUPPORTED;
+  // 32-bit row indices: B * max(H, R) * (permuted rows per problem) must fit in int32
+  const int64_t rows = (int64_t)p->B * (p->H > p->R ? p->H : p->R) * p->N * (group ? p->top_k : 1);
   if (rows >= (int64_t)INT32_MAX) return FOCUS_ERR_UNSUPPORTED;
   return FOCUS_OK;
 }
@@ -30,10 +41,12 @@ int check_params(const focus_params* p) {
 WsLayout layout(const focus_params& p) {
   WsLayout L{};
   const int BR = p.B * p.R;
-  L.nseg = (int)binom(p.K, p.top_k);
+  L.group = use_groups(p) ? 1 : 0;
+  L.nseg = L.group ? p.K : (int)binom(p.K, p.top_k);
+  L.NR = L.group ? p.N * p.top_k : p.N;
   L.nchunk = (p.N + kChunk - 1) / kChunk;
   L.nblk_sk = (p.N + 255) / 256;
-  L.qtab_cap = BR * ((p.N + kAttnBM - 1) / kAttnBM + L.nseg);
+  L.qtab_cap = BR * ((L.NR + kAttnBM - 1) / kAttnBM + L.nseg);
   const size_t A = 256;
   size_t off = 0;
   auto take = [&](size_t bytes) {
@@ -48,16 +61,20 @@ WsLayout layout(const focus_params& p) {
   L.hist = take(sizeof(int) * (size_t)BR * L.nchunk * L.nseg);
   L.segoff = take(sizeof(int) * (size_t)BR * (L.nseg + 1));
   L.cbase = take(sizeof(int) * (size_t)BR * L.nchunk * L.nseg);
-  L.perm = take(sizeof(int) * (size_t)BR * p.N);
+  L.perm = take(sizeof(int) * (size_t)BR * L.NR);
+  L.pmask = take(L.group ? sizeof(uint32_t) * (size_t)BR * L.NR : 0);
   L.entoff = take(sizeof(int) * ((size_t)BR * L.nseg + 1));
   L.qtab = take(sizeof(QBlock) * (size_t)L.qtab_cap);
   L.plan_head = take(sizeof(PlanHead) * (size_t)L.qtab_cap);
   L.plan_ent = take(sizeof(PlanEnt) * (size_t)L.qtab_cap * L.nseg);
-  L.qp = take(sizeof(uint16_t) * (size_t)p.B * p.H * p.N * p.d_head);
-  L.kp = take(sizeof(uint16_t) * (size_t)p.B * p.H_kv * p.N * p.d_head);
-  L.vp = take(sizeof(uint16_t) * (size_t)p.B * p.H_kv * p.N * p.d_head);
+  L.qp = take(sizeof(uint16_t) * (size_t)p.B * p.H * L.NR * p.d_head);
+  L.kp = take(sizeof(uint16_t) * (size_t)p.B * p.H_kv * L.NR * p.d_head);
+  L.vp = take(sizeof(uint16_t) * (size_t)p.B * p.H_kv * L.NR * p.d_head);
   L.olr = take(sizeof(float) * (size_t)p.B * p.N * p.H * p.d_head);
   L.lselr = take(sizeof(float) * (size_t)p.B * p.H * p.N);
+  const size_t slots = L.group ? (size_t)p.top_k : 0;
+  L.oslot = take(sizeof(float) * slots * p.B * p.N * p.H * p.d_head);
+  L.lseslot = take(sizeof(float) * slots * p.B * p.H * p.N);
   L.total = off;
   return L;
 }
@@ -86,6 +103,15 @@ extern "C" {
 size_t focus_workspace_size(const focus_params* p) {
   if (check_params(p) != FOCUS_OK) return 0;
   return layout(*p).total;
+}
+
+int focus_bucket_shape(const focus_params* p, int32_t* n_segments, int32_t* rows) {
+  const int rc = check_params(p);
+  if (rc) return rc;
+  const WsLayout L = layout(*p);
+  if (n_segments) *n_segments = L.nseg;
+  if (rows) *rows = L.NR;
+  return L.group ? FOCUS_SCHEDULE_GROUPS : FOCUS_SCHEDULE_SEGMENTS;
 }
 
 int focus_route(const focus_params* p, const float* r, const float* C, uint32_t* mask_out,
@@ -118,7 +144,7 @@ int focus_bucket(const focus_params* p, const uint32_t* mask, int32_t* perm_out,
   if ((rc = cuda_rc(launch_bucket(*p, L, mask, w, s)))) return rc;
   const size_t BR = (size_t)p->B * p->R;
   if (perm_out &&
-      (rc = cuda_rc(cudaMemcpyAsync(perm_out, w + L.perm, sizeof(int) * BR * p->N,
+      (rc = cuda_rc(cudaMemcpyAsync(perm_out, w + L.perm, sizeof(int) * BR * L.NR,
                                     cudaMemcpyDeviceToDevice, s))))
     return rc;
   if (seg_off_out &&
@@ -170,6 +196,9 @@ int focus_attn_fwd_ev(const focus_params* p, const uint16_t* q, const uint16_t* 
   if ((rc = cuda_rc(launch_attn_window_tc(*p, L, qb, kb, vb, w, scale, s)))) return rc;
   if ((rc = mark(4))) return rc;
   if ((rc = cuda_rc(launch_attn_long_tc(*p, L, w, reinterpret_cast<bf16*>(o), lse, scale, s))))
+    return rc;
+  if (L.group &&
+      (rc = cuda_rc(launch_merge_slots(*p, L, w, reinterpret_cast<bf16*>(o), lse, s))))
     return rc;
   return mark(5);
 }

@@ -43,8 +43,9 @@ def test_workspace_size_valid_and_invalid():
     assert n >= 2 * 3 * p.N * p.H * p.d_head + 4 * p.N * p.H * p.d_head
     assert focus.workspace_size(_params(N=1024)) > n
     for bad in (dict(N=0), dict(H=3, H_kv=2), dict(H_kv=2, R=3), dict(top_k=5),
-                dict(K=33, top_k=1), dict(w=0), dict(d_head=96), dict(K=16, top_k=8),
-                dict(sinkhorn_iters=1, sinkhorn_eps=0.0)):
+                dict(K=33, top_k=1), dict(w=0), dict(d_head=96),
+                dict(K=16, top_k=8, schedule=focus.SCHEDULE_SEGMENTS), dict(schedule=3),
+                dict(schedule=-1), dict(sinkhorn_iters=1, sinkhorn_eps=0.0)):
         assert focus.workspace_size(_params(**bad)) == 0, bad
 
 
@@ -65,7 +66,7 @@ def test_argument_errors_are_caught_on_the_host():
     assert _call_attn(p, ws=(1 << 12) + 64) == E["FOCUS_ERR_ALIGNMENT"]
     assert _call_attn(p, ws_bytes=focus.workspace_size(p) - 1) == E["FOCUS_ERR_WORKSPACE"]
     assert _call_attn(_params(d_head=96)) == E["FOCUS_ERR_UNSUPPORTED"]
-    assert _call_attn(_params(K=16, top_k=8)) == E["FOCUS_ERR_UNSUPPORTED"]
+    assert _call_attn(_params(K=16, top_k=8, schedule=focus.SCHEDULE_SEGMENTS)) == E["FOCUS_ERR_UNSUPPORTED"]
     assert _call_attn(_params(H=4, H_kv=3)) == E["FOCUS_ERR_INVALID_ARG"]
     assert focus._lib.focus_route(None, None, None, None, None, None, 0, None) == E["FOCUS_ERR_INVALID_ARG"]
 
@@ -87,6 +88,30 @@ def test_window_pairs_closed_form():
 
 def test_nseg_is_binomial():
     assert _params(K=8, top_k=2).nseg == 28 == math.comb(8, 2)
+
+
+def test_schedule_resolution_and_bucket_shape():
+    S, G = focus.SCHEDULE_SEGMENTS, focus.SCHEDULE_GROUPS
+    N = 512
+    # AUTO: exact-set segments up to 64 sets, group lists above
+    assert _params(K=4, top_k=2).bucket_shape() == (S, 6, N)
+    assert _params(K=8, top_k=3).bucket_shape() == (S, 56, N)
+    assert _params(K=8, top_k=4).bucket_shape() == (G, 8, 4 * N)       # C(8,4) = 70
+    assert _params(K=16, top_k=2).bucket_shape() == (G, 16, 2 * N)
+    assert _params(K=32, top_k=4).bucket_shape() == (G, 32, 4 * N)     # 35960 sets
+    assert _params(K=32, top_k=1).bucket_shape() == (S, 32, N)
+    # explicit choices
+    assert _params(K=4, top_k=2, schedule=G).bucket_shape() == (G, 4, 2 * N)
+    assert _params(K=16, top_k=2, schedule=S).bucket_shape() == (S, 120, N)
+    # group lists: workspace holds top_k-fold permuted copies and top_k list parts
+    seg = focus.workspace_size(_params(K=4, top_k=2, schedule=S))
+    grp = focus.workspace_size(_params(K=4, top_k=2, schedule=G))
+    extra = 3 * 2 * N * 2 * 64 + 2 * 4 * N * 2 * 64       # one more Q/K/V copy + 2 fp32 slots
+    assert grp >= seg + extra
+    # 32-bit row limit counts the top_k-fold rows
+    big = dict(B=1, N=1 << 24, H=64, H_kv=64, K=32, top_k=4)
+    assert focus.workspace_size(_params(**big, schedule=S)) == 0       # too many sets
+    assert focus.workspace_size(_params(**big)) == 0                   # 2^24 * 64 * 4 rows
 
 
 def test_host_entry_sizes_and_argument_errors():
