@@ -53,9 +53,11 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target CPU time of the oracle sample")
-    ap.add_argument("--sweep", choices=["table6", "decode"], default=None,
-                    help="speedup of Focus over this build's own dense causal mode (K=1) "
-                         "across context lengths, K=4 and K=8 (one JSON line)")
+    ap.add_argument("--sweep", choices=["table6", "decode", "schedule"], default=None,
+                    help="table6: speedup of Focus over this build's own dense causal mode "
+                         "(K=1) across context lengths, K=4 and K=8; decode: one decode step "
+                         "per workload; schedule: exact-set segments vs group lists over "
+                         "(K, top_k) at 32K tokens (one JSON line each)")
     return ap.parse_args()
 
 
@@ -354,7 +356,10 @@ def run_focus(args):
         "executed_tflops": exec_long / t_long / 1e12,
         "launch_ms": stage_ms["attn_long"],
     }
-    launches_per_step = (1 + 2 * wl.sinkhorn_iters) + 3 + 1 + 1 + 1 + 1
+    # route (+ 2 per Sinkhorn iteration), 3 bucketing, schedule, plan, permute,
+    # window, long-range (+ the slot merge under group lists)
+    launches_per_step = (1 + 2 * wl.sinkhorn_iters) + 3 + 1 + 1 + 1 + 1 + 1 \
+        + (1 if p.bucket_shape()[0] == focus.SCHEDULE_GROUPS else 0)
     qkv_bytes = sum(x[n].numel() * x[n].element_size() for n in ("q", "k", "v"))
 
     line = {
@@ -363,7 +368,9 @@ def run_focus(args):
         "dtype": "bf16", "data": "synthetic",
         "config": dict(config_of(wl), l2=f"inputs larger than L2 (Q/K/V {qkv_bytes / 2**20:.0f} MiB "
                                           f"> {L2_BYTES / 2**20:.0f} MiB), no flush",
-                       parallelism=f"independent problem per GPU x{world}"),
+                       parallelism=f"independent problem per GPU x{world}",
+                       schedule="groups" if p.bucket_shape()[0] == focus.SCHEDULE_GROUPS
+                       else "segments"),
         "allowed_pair_tflops": tflops,
         "allowed_pair_frac_of_peak": tflops / peaks["bf16_tflops"],
         "allowed_pairs": allowed, "allowed_fraction_of_causal": allowed / causal,
@@ -498,8 +505,78 @@ def run_decode(args):
                       "peak_hbm_gbs": peaks["hbm_gbs"], "peak_source": peak_src, "rows": rows}), flush=True)
 
 
+# ------------------------------------------------------------ schedules --
+SCHEDULE_GRID = [(4, 2, 32768), (8, 2, 32768), (8, 4, 32768), (16, 2, 32768), (32, 2, 32768),
+                 (16, 4, 32768), (32, 4, 32768), (8, 2, 131072), (16, 2, 131072)]
+
+
+def run_schedule(args):
+    """Exact-set segments vs group lists on a 32-head, d=128 layer (w=512) for
+    several (K, top_k, N): step time, its stages, and allowed-pair TFLOP/s.  Segments
+    run only while C(K, top_k) <= 1024."""
+    import math
+
+    import learned_centroid_gated_gb300 as focus
+    from learned_centroid_gated_gb300 import pairs
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    base = synth.WORKLOADS["mha7b_32k"]
+    rows = []
+    x, o = None, None
+    for K, top_k, N in SCHEDULE_GRID:
+        wl = base.replace(K=K, top_k=top_k, N=N)
+        if x is None or x[0].shape[1] != N:
+            x = o = None
+            torch.cuda.empty_cache()
+            x = synth.make_qkv(wl, seed=args.seed, device=dev)
+            o = torch.empty_like(x[0])
+        r, C = synth.make_routing(wl, seed=args.seed, device=dev)
+        p0 = focus.Params.from_workload(wl)
+        mask, _ = focus.route(p0, r, C)
+        allowed = int(pairs.allowed_pairs(mask.cpu().numpy().view(np.uint32), wl.w).sum()) * wl.H
+        flops = 4.0 * wl.d_head * allowed
+        for sch in (focus.SCHEDULE_SEGMENTS, focus.SCHEDULE_GROUPS):
+            if sch == focus.SCHEDULE_SEGMENTS and math.comb(K, top_k) > 1024:
+                continue
+            p = focus.Params.from_workload(wl, schedule=sch)
+            ws = focus.Workspace(dev).get(p)
+            for _ in range(3):
+                focus.attn_fwd(p, *x, r, C, out=o, want_lse=False, ws=ws, stream=stream)
+            torch.cuda.synchronize()
+            assert focus.get_status(ws) == 0
+            steps = 5
+            evs = [[torch.cuda.Event(enable_timing=True) for _ in range(focus.N_STAGE_EVENTS)]
+                   for _ in range(steps)]
+            for e in evs:
+                focus.attn_fwd(p, *x, r, C, out=o, want_lse=False, ws=ws, stream=stream,
+                               stage_events=e)
+            torch.cuda.synchronize()
+            stage = {n: statistics.median(e[i].elapsed_time(e[i + 1]) for e in evs)
+                     for i, n in enumerate(focus.STAGES)}
+            ms = statistics.median(e[0].elapsed_time(e[-1]) for e in evs)
+            rows.append({"K": K, "top_k": top_k, "N": N, "sets": math.comb(K, top_k),
+                         "schedule": "segments" if sch == focus.SCHEDULE_SEGMENTS else "groups",
+                         "auto": p0.bucket_shape()[0] == sch, "ms": ms,
+                         "tokens_per_s": wl.B * wl.N / (ms / 1e3),
+                         "allowed_pair_tflops": flops / (ms / 1e3) / 1e12,
+                         "pairs_retained": allowed / (wl.H * wl.N * (wl.N + 1) // 2),
+                         "stages_ms": stage})
+            del ws
+            torch.cuda.empty_cache()
+    print(json.dumps({"sweep": "schedule", "unit": "ms per forward", "dtype": "bf16",
+                      "data": "synthetic",
+                      "config": config_of(base) | {"K": "varies", "top_k": "varies", "N": "varies"},
+                      "note": "attn_long includes the slot merge under group lists",
+                      "rows": rows}), flush=True)
+
+
 def main():
     args = parse_args()
+    if args.sweep == "schedule":
+        run_schedule(args)
+        return
     if args.sweep == "table6":
         run_table6(args)
         return

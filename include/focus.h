@@ -55,7 +55,6 @@ extern "C" {
 #define FOCUS_D_G 16            /* routing dimension */
 #define FOCUS_MAX_K 32          /* groups representable in a uint32 bitmask */
 #define FOCUS_MAX_SEGMENTS 1024 /* C(K, top_k) limit of the mask-value bucketing */
-#define FOCUS_AUTO_SEGMENTS 64  /* FOCUS_SCHEDULE_AUTO picks group lists above this */
 
 /* Long-range schedule (focus_params.schedule).
  *   SEGMENTS: tokens sorted by their exact group set (C(K, top_k) segments); a
@@ -65,7 +64,12 @@ extern "C" {
  *             query in list g counts key j only when g is the LOWEST group the two
  *             share, so each key is still counted once; the top_k partial results
  *             of a token are merged with the window's by log-sum-exp.  Any K, top_k.
- *   AUTO:     SEGMENTS when C(K, top_k) <= FOCUS_AUTO_SEGMENTS, else GROUPS. */
+ *   AUTO:     the one with the smaller estimated tensor-core work (fractions of
+ *             dense causal attention): SEGMENTS ~ (1 - C(K-k,k)/C(K,k)) *
+ *             (1 + 2 C(K,k) 256 / N), the chance that two sets meet times the
+ *             raggedness of C(K,k) segments over N tokens; GROUPS ~ 1.15 k^2 / K.
+ *             SEGMENTS when top_k = 1 (the same partition), GROUPS when
+ *             C(K, top_k) > FOCUS_MAX_SEGMENTS.  focus_bucket_shape reports it. */
 enum focus_schedule {
   FOCUS_SCHEDULE_AUTO = 0,
   FOCUS_SCHEDULE_SEGMENTS = 1,

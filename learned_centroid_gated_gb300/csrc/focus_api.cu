@@ -10,12 +10,24 @@ namespace {
 
 bool aligned(const void* ptr, size_t a) { return ((uintptr_t)ptr % a) == 0; }
 
-// The schedule that runs: group lists when asked for, or under AUTO when the
-// exact-set segments would be more than FOCUS_AUTO_SEGMENTS.
+// The schedule that runs.  AUTO compares estimates of the tensor-core work, as a
+// fraction of dense causal attention:
+//   segments:    P(two uniform top_k-sets of K intersect) = 1 - C(K-k, k) / C(K, k),
+//                times (1 + 2 * C(K, k) * 256 / N) for the ragged query blocks and
+//                key tiles of C(K, k) segments over N tokens;
+//   group lists: 1.15 * k^2 / K (K lists of N k / K rows, each a dense causal
+//                problem; 15 % for the lowest-group test, list imbalance, the merge).
+// top_k = 1 makes both the same partition, so segments (no merge pass).
 bool use_groups(const focus_params& p) {
   if (p.schedule == FOCUS_SCHEDULE_GROUPS) return true;
   if (p.schedule == FOCUS_SCHEDULE_SEGMENTS) return false;
-  return binom(p.K, p.top_k) > (uint32_t)FOCUS_AUTO_SEGMENTS;
+  if (p.top_k == 1) return false;
+  const double sets = (double)binom(p.K, p.top_k);
+  if (sets > (double)FOCUS_MAX_SEGMENTS) return true;
+  const double meet = 1.0 - (double)binom(p.K - p.top_k, p.top_k) / sets;
+  const double seg = meet * (1.0 + 2.0 * sets * (double)kAttnBM / (double)p.N);
+  const double grp = 1.15 * (double)p.top_k * (double)p.top_k / (double)p.K;
+  return grp < seg;
 }
 
 // Shape checks shared by every entry point (host only, nothing launched).

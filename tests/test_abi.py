@@ -87,19 +87,21 @@ def test_window_pairs_closed_form():
 
 
 def test_nseg_is_binomial():
-    assert _params(K=8, top_k=2).nseg == 28 == math.comb(8, 2)
+    assert _params(K=8, top_k=2, schedule=focus.SCHEDULE_SEGMENTS).nseg == 28 == math.comb(8, 2)
 
 
 def test_schedule_resolution_and_bucket_shape():
     S, G = focus.SCHEDULE_SEGMENTS, focus.SCHEDULE_GROUPS
+    N = 32768
+    # AUTO: smaller estimated work; on 32K tokens this is the side that measured faster
+    for K, top_k, sch, nseg in [(4, 2, S, 6), (8, 2, G, 8), (8, 4, S, 70), (16, 2, G, 16),
+                                (32, 2, G, 32), (16, 4, G, 16), (32, 4, G, 32), (32, 1, S, 32)]:
+        rows = N * top_k if sch == G else N
+        assert _params(N=N, K=K, top_k=top_k).bucket_shape() == (sch, nseg, rows), (K, top_k)
+    # fewer tokens per set tip the balance towards lists; more tokens towards segments
+    assert _params(N=512, K=4, top_k=2).bucket_shape()[0] == G
+    assert _params(N=1 << 20, K=16, top_k=2).bucket_shape()[0] == S
     N = 512
-    # AUTO: exact-set segments up to 64 sets, group lists above
-    assert _params(K=4, top_k=2).bucket_shape() == (S, 6, N)
-    assert _params(K=8, top_k=3).bucket_shape() == (S, 56, N)
-    assert _params(K=8, top_k=4).bucket_shape() == (G, 8, 4 * N)       # C(8,4) = 70
-    assert _params(K=16, top_k=2).bucket_shape() == (G, 16, 2 * N)
-    assert _params(K=32, top_k=4).bucket_shape() == (G, 32, 4 * N)     # 35960 sets
-    assert _params(K=32, top_k=1).bucket_shape() == (S, 32, N)
     # explicit choices
     assert _params(K=4, top_k=2, schedule=G).bucket_shape() == (G, 4, 2 * N)
     assert _params(K=16, top_k=2, schedule=S).bucket_shape() == (S, 120, N)

@@ -20,9 +20,9 @@ focus = pytest.importorskip("learned_centroid_gated_gb300")
 pytestmark = pytest.mark.gpu
 
 
-def _run(wl, seed=0, rows=None, heads=None, scale=0.0, use_mask_in=False):
+def _run(wl, seed=0, rows=None, heads=None, scale=0.0, use_mask_in=False, schedule=0):
     x = synth.make_inputs(wl, seed=seed, device="cuda")
-    p = focus.Params.from_workload(wl, softmax_scale=scale)
+    p = focus.Params.from_workload(wl, softmax_scale=scale, schedule=schedule)
     mask, _ = focus.route(p, x["r"], x["C"])
     if use_mask_in:
         o, lse = focus.attn_fwd(p, x["q"], x["k"], x["v"], mask=mask)
@@ -55,22 +55,28 @@ SMALL = {
 }
 
 
+SCHEDULES = {"segments": focus.SCHEDULE_SEGMENTS, "groups": focus.SCHEDULE_GROUPS}
+
+
+@pytest.mark.parametrize("schedule", list(SCHEDULES))
 @pytest.mark.parametrize("name", list(SMALL))
-def test_attention_all_rows(name):
+def test_attention_all_rows(name, schedule):
     wl = SMALL[name]
-    _, _, errs = _run(wl, seed=1)
-    print(f"{name}: max|dO|={errs[0]:.2e} max rel dLSE={errs[1]:.2e}")
+    _, _, errs = _run(wl, seed=1, schedule=SCHEDULES[schedule])
+    print(f"{name} ({schedule}): max|dO|={errs[0]:.2e} max rel dLSE={errs[1]:.2e}")
 
 
-def test_precomputed_mask_and_explicit_scale():
+@pytest.mark.parametrize("schedule", list(SCHEDULES))
+def test_precomputed_mask_and_explicit_scale(schedule):
     wl = synth.WORKLOADS["tiny"].replace(N=777, w=33)
-    _run(wl, seed=2, scale=0.05, use_mask_in=True)
+    _run(wl, seed=2, scale=0.05, use_mask_in=True, schedule=SCHEDULES[schedule])
 
 
-def test_deterministic_across_calls():
+@pytest.mark.parametrize("schedule", list(SCHEDULES))
+def test_deterministic_across_calls(schedule):
     wl = synth.WORKLOADS["gpt2_layer"]
     x = synth.make_inputs(wl, seed=3, device="cuda")
-    p = focus.Params.from_workload(wl)
+    p = focus.Params.from_workload(wl, schedule=SCHEDULES[schedule])
     o1, l1 = focus.attn_fwd(p, x["q"], x["k"], x["v"], x["r"], x["C"])
     o1, l1 = o1.clone(), l1.clone()
     o2, l2 = focus.attn_fwd(p, x["q"], x["k"], x["v"], x["r"], x["C"])

@@ -22,19 +22,19 @@ G = focus.SCHEDULE_GROUPS
 TINY = synth.WORKLOADS["tiny"]
 
 CASES = {
-    # name: (workload, schedule)
+    # name: (workload, schedule); AUTO only where C(K, top_k) > 1024 forces group lists
     "tiny_groups": (TINY, G),
-    "K16_top2_auto": (TINY.replace(N=3000, K=16, top_k=2, w=50), 0),
+    "K16_top2": (TINY.replace(N=3000, K=16, top_k=2, w=50), G),
     "K32_top4_auto": (TINY.replace(N=2500, K=32, top_k=4, w=64, d_head=128), 0),
     "K16_top3_gqa_b2": (TINY.replace(B=2, N=1500, H=8, H_kv=2, R=2, d_head=128, K=16, top_k=3,
-                                     w=100), 0),
+                                     w=100), G),
     "topk_equals_K": (TINY.replace(N=700, K=8, top_k=8), G),
     "top1_groups": (TINY.replace(N=1100, K=6, top_k=1, w=16), G),
-    "single_token": (TINY.replace(N=1, K=16, top_k=2), 0),
-    "window_covers_all": (TINY.replace(N=600, w=700, K=16, top_k=2), 0),
+    "single_token": (TINY.replace(N=1, K=16, top_k=2), G),
+    "window_covers_all": (TINY.replace(N=600, w=700, K=16, top_k=2), G),
     "sinkhorn_K16": (TINY.replace(N=2000, K=16, top_k=2, sinkhorn_iters=4, sinkhorn_eps=0.5,
-                                  w=128), 0),
-    "K32_top2_ragged": (TINY.replace(N=3001, H=3, H_kv=1, K=32, top_k=2, w=37), 0),
+                                  w=128), G),
+    "K32_top2_ragged": (TINY.replace(N=3001, H=3, H_kv=1, K=32, top_k=2, w=37), G),
 }
 
 
@@ -93,7 +93,7 @@ def test_both_schedules_agree_with_each_other():
 
 def test_group_schedule_bad_mask_raises_bounds_without_fault():
     wl = TINY.replace(K=16, top_k=2)
-    p = focus.Params.from_workload(wl)
+    p = focus.Params.from_workload(wl, schedule=G)
     x = synth.make_inputs(wl, seed=2, device="cuda")
     bad = torch.full((1, 1, wl.N), 0b0111, dtype=torch.int32, device="cuda")
     ws = focus.Workspace("cuda").get(p)

@@ -53,7 +53,7 @@ def _colex_rank_table(K, top_k):
 def test_bucketing_is_stable_sort_by_mask_value(name):
     wl = synth.WORKLOADS[name]
     r, C = synth.make_routing(wl, seed=1, device="cuda")
-    p = focus.Params.from_workload(wl)
+    p = focus.Params.from_workload(wl, schedule=focus.SCHEDULE_SEGMENTS)
     mask, _ = focus.route(p, r, C)
     perm, seg = focus.bucket(p, mask)
     m = mask_np(mask)
@@ -68,7 +68,7 @@ def test_bucketing_is_stable_sort_by_mask_value(name):
 
 def test_bad_mask_raises_bounds_status_without_fault():
     wl = synth.WORKLOADS["tiny"]
-    p = focus.Params.from_workload(wl)
+    p = focus.Params.from_workload(wl, schedule=focus.SCHEDULE_SEGMENTS)
     mask = torch.full((1, 1, wl.N), 0b0111, dtype=torch.int32, device="cuda")  # 3 bits, top_k=2
     ws = focus.Workspace("cuda").get(p)
     focus.bucket(p, mask, ws=ws)
