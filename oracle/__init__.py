@@ -1,4 +1,4 @@
-"""CPU fp64 oracle for Focus centroid-gated sparse attention (forward).
+"""CPU fp64 oracle for Focus centroid-gated sparse attention (forward and backward).
 
 TEST INFRASTRUCTURE ONLY: imported by the tests, by the smoke check and by the
 benchmark's CPU-baseline leg, never by the CUDA library or its Python binding.
@@ -10,7 +10,10 @@ and against numpy's stable sort; Sinkhorn against its marginal constraints and a
 probability-domain restatement; the attended set against a dense N x N mask built
 from the definition; values against dense causal attention in the cases that
 reduce to it (K=1, top_k=K, 2*top_k>K, w>=N) and against per-group causal
-attention for w=1, top_k=1; rows of the softmax sum to one.  The Sinkhorn step's
+attention for w=1, top_k=1; rows of the softmax sum to one.  Gradients: central
+differences of the forward between adjacent bf16 values, torch autograd of dense
+causal attention in the cases that reduce to it, per-group causal attention for
+w=1, top_k=1, and the sum rules sum_j dk_j = 0, sum_j dv_j = sum_i dO_i.  The Sinkhorn step's
 agreement with the authors' own (unpublished) formula is parity unpinned: the
 pages give no formula and no numbers for it.
 """
@@ -55,6 +58,9 @@ def _load():
         lib.oracle_attn.argtypes = [i32, i32, i32, i32, i32, i32, i32, f64, P, P, P, P, P, i64, P, i32,
                                     P, P, i32]
         lib.oracle_attn.restype = i32
+        lib.oracle_attn_bwd.argtypes = [i32, i32, i32, i32, i32, i32, i32, f64, P, P, P, P, P, P, i64,
+                                        P, i64, P, i32, P, P, P, i32]
+        lib.oracle_attn_bwd.restype = i32
         _lib = lib
     return _lib
 
@@ -138,3 +144,38 @@ def attn(q, k, v, mask, *, w: int, scale: float | None = None, rows=None, heads=
     if rc != 0:
         raise ValueError("oracle_attn: bad arguments")
     return o, lse
+
+
+def attn_bwd(q, k, v, mask, dout, *, w: int, scale: float | None = None, rows=None, keys=None,
+             heads=None, n_threads: int | None = None):
+    """Gradients of ``attn`` with the mask held fixed, for upstream gradient dout
+    [B, N, H, d] (bf16 tensor or uint16 bits).
+
+    rows: flattened query rows (b * N + i) whose dq is wanted (default all);
+    keys: flattened key rows (b * N + j) whose dk, dv are wanted (default all);
+    heads: query heads differentiated (default all); dk, dv sum over them.
+    Returns (dq [n_rows, n_heads, d], dk [n_keys, H_kv, d], dv [n_keys, H_kv, d]), f64."""
+    q16, k16, v16, g16 = (_np(t, np.uint16) for t in (q, k, v, dout))
+    mask = _np(mask, np.uint32)
+    B, N, H, d = q16.shape
+    H_kv = k16.shape[2]
+    R = mask.shape[1]
+    assert g16.shape == q16.shape and k16.shape == (B, N, H_kv, d) and v16.shape == k16.shape
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    rows_a = None if rows is None else _np(rows, np.int64)
+    keys_a = None if keys is None else _np(keys, np.int64)
+    heads_a = None if heads is None else _np(heads, np.int32)
+    n_rows = B * N if rows_a is None else rows_a.shape[0]
+    n_keys = B * N if keys_a is None else keys_a.shape[0]
+    n_heads = H if heads_a is None else heads_a.shape[0]
+    dq = np.zeros((n_rows, n_heads, d), np.float64)
+    dk = np.zeros((n_keys, H_kv, d), np.float64)
+    dv = np.zeros((n_keys, H_kv, d), np.float64)
+    rc = _load().oracle_attn_bwd(B, N, H, H_kv, R, d, w, float(scale), _ptr(q16), _ptr(k16), _ptr(v16),
+                                 _ptr(mask), _ptr(g16), _ptr(rows_a), n_rows, _ptr(keys_a), n_keys,
+                                 _ptr(heads_a), n_heads, _ptr(dq), _ptr(dk), _ptr(dv),
+                                 n_threads or n_cores())
+    if rc != 0:
+        raise ValueError("oracle_attn_bwd: bad arguments")
+    return dq, dk, dv

@@ -1,5 +1,5 @@
 /*
- * Focus centroid-gated sparse attention, forward pass: plain fp64 CPU oracle.
+ * Focus centroid-gated sparse attention, forward and backward: plain fp64 CPU oracle.
  *
  * TEST INFRASTRUCTURE ONLY. This file is the slow, obviously correct statement of
  * what the CUDA path computes. Only the tests, the smoke check and the benchmark's
@@ -299,5 +299,183 @@ int oracle_attn(int B, int N, int H, int H_kv, int R, int d, int w, double scale
   for (int t = 0; t < n_threads; ++t) pthread_create(&th[t], NULL, attn_worker, &J);
   for (int t = 0; t < n_threads; ++t) pthread_join(th[t], NULL);
   pthread_mutex_destroy(&J.mu);
+  return 0;
+}
+
+/* ------------------------------------------------------------ backward ------ */
+/*
+ * Gradients of the union-softmax attention with the hard (top-k) mask held fixed.
+ * With s_ij = scale q_i.k_j over j in A_i, P_ij = exp(s_ij - LSE_i),
+ * O_i = sum_j P_ij v_j and an upstream gradient dO:
+ *   dP_ij = dO_i . v_j,  D_i = sum_j P_ij dP_ij,  dS_ij = P_ij (dP_ij - D_i),
+ *   dq_i = scale sum_j dS_ij k_j,  dk_j = scale sum_i dS_ij q_i,  dv_j = sum_i P_ij dO_i
+ * (the chain rule through softmax; the mask is piecewise constant in r and C, so
+ * the routing inputs receive no gradient).  A KV head's gradients sum over the
+ * query heads that read it.
+ */
+typedef struct {
+  int B, N, H, H_kv, R, d, w;
+  double scale;
+  const uint16_t *q, *k, *v, *dout;
+  const uint32_t* mask;
+  const int64_t* row_slot; /* [B*N]: output slot of a query row, -1 if not wanted */
+  const int64_t* key_slot; /* [B*N]: output slot of a key row, -1 if not wanted */
+  int64_t n_keys;
+  const int32_t* heads;
+  int n_heads;
+  double *dq, *dk, *dv;
+  int64_t next, total;
+  pthread_mutex_t mu;
+} bwd_job;
+
+static void* bwd_worker(void* arg) {
+  bwd_job* J = (bwd_job*)arg;
+  const int d = J->d;
+  double* s_buf = (double*)malloc(sizeof(double) * (size_t)J->N);
+  double* dp_buf = (double*)malloc(sizeof(double) * (size_t)J->N);
+  int64_t* j_buf = (int64_t*)malloc(sizeof(int64_t) * (size_t)J->N);
+  double* qv = (double*)malloc(sizeof(double) * (size_t)d);
+  double* gv = (double*)malloc(sizeof(double) * (size_t)d);
+  const size_t acc_n = (size_t)J->n_keys * J->H_kv * d;
+  double* dk_acc = (double*)calloc(acc_n ? acc_n : 1, sizeof(double));
+  double* dv_acc = (double*)calloc(acc_n ? acc_n : 1, sizeof(double));
+  const int64_t chunk = 8;
+  for (;;) {
+    pthread_mutex_lock(&J->mu);
+    const int64_t start = J->next;
+    J->next += chunk;
+    pthread_mutex_unlock(&J->mu);
+    if (start >= J->total) break;
+    const int64_t end = start + chunk < J->total ? start + chunk : J->total;
+    for (int64_t u = start; u < end; ++u) {
+      /* u = (hs * B + b) * N + i */
+      const int64_t i = u % J->N;
+      const int b = (int)((u / J->N) % J->B);
+      const int hs = (int)(u / ((int64_t)J->N * J->B));
+      const int h = J->heads ? J->heads[hs] : hs;
+      const int kvh = h / (J->H / J->H_kv);
+      const int rho = kvh / (J->H_kv / J->R);
+      const uint32_t* m = J->mask + ((int64_t)b * J->R + rho) * J->N;
+      const int64_t bi = (int64_t)b * J->N + i;
+      const uint16_t* qi = J->q + (bi * J->H + h) * d;
+      const uint16_t* gi = J->dout + (bi * J->H + h) * d;
+      for (int t = 0; t < d; ++t) {
+        qv[t] = bf16_to_double(qi[t]);
+        gv[t] = bf16_to_double(gi[t]);
+      }
+      /* forward quantities of the row: logits, LSE, dP, D */
+      int64_t n = 0;
+      double mx = -INFINITY;
+      for (int64_t j = 0; j <= i; ++j) {
+        if (!allowed(i, j, J->w, m[i], m[j])) continue;
+        const int64_t bj = (int64_t)b * J->N + j;
+        const uint16_t* kj = J->k + (bj * J->H_kv + kvh) * d;
+        const uint16_t* vj = J->v + (bj * J->H_kv + kvh) * d;
+        double s = 0.0, dp = 0.0;
+        for (int t = 0; t < d; ++t) {
+          s += qv[t] * bf16_to_double(kj[t]);
+          dp += gv[t] * bf16_to_double(vj[t]);
+        }
+        s_buf[n] = s * J->scale;
+        dp_buf[n] = dp;
+        j_buf[n] = j;
+        if (s_buf[n] > mx) mx = s_buf[n];
+        ++n;
+      }
+      double sum = 0.0;
+      for (int64_t a = 0; a < n; ++a) sum += exp(s_buf[a] - mx);
+      const double lse = mx + log(sum);
+      double D = 0.0;
+      for (int64_t a = 0; a < n; ++a) D += exp(s_buf[a] - lse) * dp_buf[a];
+      /* scatter into the wanted outputs */
+      const int64_t rs = J->row_slot[bi];
+      double* dq = rs >= 0 ? J->dq + (rs * J->n_heads + hs) * d : NULL;
+      for (int64_t a = 0; a < n; ++a) {
+        const double p = exp(s_buf[a] - lse);
+        const double ds = p * (dp_buf[a] - D);
+        const int64_t bj = (int64_t)b * J->N + j_buf[a];
+        if (dq) {
+          const uint16_t* kj = J->k + (bj * J->H_kv + kvh) * d;
+          for (int t = 0; t < d; ++t) dq[t] += J->scale * ds * bf16_to_double(kj[t]);
+        }
+        const int64_t ks = J->key_slot[bj];
+        if (ks >= 0) {
+          double* dk = dk_acc + (ks * J->H_kv + kvh) * d;
+          double* dv = dv_acc + (ks * J->H_kv + kvh) * d;
+          for (int t = 0; t < d; ++t) {
+            dk[t] += J->scale * ds * qv[t];
+            dv[t] += p * gv[t];
+          }
+        }
+      }
+    }
+  }
+  pthread_mutex_lock(&J->mu);
+  for (size_t x = 0; x < acc_n; ++x) {
+    J->dk[x] += dk_acc[x];
+    J->dv[x] += dv_acc[x];
+  }
+  pthread_mutex_unlock(&J->mu);
+  free(s_buf); free(dp_buf); free(j_buf); free(qv); free(gv); free(dk_acc); free(dv_acc);
+  return NULL;
+}
+
+/*
+ * Backward of oracle_attn for the requested outputs.
+ *   q [B, N, H, d], k/v [B, N, H_kv, d], dout [B, N, H, d]: bf16 bit patterns
+ *   mask [B, R, N] uint32
+ *   rows (nullable) flattened query rows b*N+i for dq (NULL = all B*N rows)
+ *   keys (nullable) flattened key rows b*N+j for dk, dv (NULL = all B*N rows)
+ *   heads (nullable) query heads whose paths are differentiated (NULL = all H)
+ *   dq [n_rows, n_heads, d] double out
+ *   dk, dv [n_keys, H_kv, d] double out: sums over the selected query heads
+ * Every query row of the selected heads is visited (each one feeds the keys).
+ * Returns 0, or -1 on bad arguments.
+ */
+int oracle_attn_bwd(int B, int N, int H, int H_kv, int R, int d, int w, double scale,
+                    const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                    const uint32_t* mask, const uint16_t* dout, const int64_t* rows,
+                    int64_t n_rows, const int64_t* keys, int64_t n_keys, const int32_t* heads,
+                    int n_heads, double* dq, double* dk, double* dv, int n_threads) {
+  if (B < 1 || N < 1 || H < 1 || H_kv < 1 || R < 1 || d < 1 || w < 1 || H % H_kv ||
+      H_kv % R || n_rows < 0 || n_keys < 0)
+    return -1;
+  const int64_t BN = (int64_t)B * N;
+  if (!rows) n_rows = BN;
+  if (!keys) n_keys = BN;
+  if (!heads) n_heads = H;
+  for (int a = 0; heads && a < n_heads; ++a)
+    if (heads[a] < 0 || heads[a] >= H) return -1;
+  int64_t* row_slot = (int64_t*)malloc(sizeof(int64_t) * (size_t)BN);
+  int64_t* key_slot = (int64_t*)malloc(sizeof(int64_t) * (size_t)BN);
+  for (int64_t x = 0; x < BN; ++x) {
+    row_slot[x] = rows ? -1 : x;
+    key_slot[x] = keys ? -1 : x;
+  }
+  int bad = 0;
+  for (int64_t a = 0; rows && a < n_rows; ++a) {
+    if (rows[a] < 0 || rows[a] >= BN || row_slot[rows[a]] >= 0) bad = 1;
+    else row_slot[rows[a]] = a;
+  }
+  for (int64_t a = 0; keys && a < n_keys; ++a) {
+    if (keys[a] < 0 || keys[a] >= BN || key_slot[keys[a]] >= 0) bad = 1;
+    else key_slot[keys[a]] = a;
+  }
+  if (bad) {
+    free(row_slot); free(key_slot);
+    return -1;
+  }
+  for (int64_t x = 0; x < n_rows * n_heads * d; ++x) dq[x] = 0.0;
+  for (int64_t x = 0; x < n_keys * H_kv * d; ++x) dk[x] = dv[x] = 0.0;
+  bwd_job J = {B, N, H, H_kv, R, d, w, scale, q, k, v, dout, mask, row_slot, key_slot, n_keys,
+               heads, n_heads, dq, dk, dv, 0, (int64_t)n_heads * BN};
+  pthread_mutex_init(&J.mu, NULL);
+  if (n_threads < 1) n_threads = 1;
+  if (n_threads > 256) n_threads = 256;
+  pthread_t th[256];
+  for (int t = 0; t < n_threads; ++t) pthread_create(&th[t], NULL, bwd_worker, &J);
+  for (int t = 0; t < n_threads; ++t) pthread_join(th[t], NULL);
+  pthread_mutex_destroy(&J.mu);
+  free(row_slot); free(key_slot);
   return 0;
 }

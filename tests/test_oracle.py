@@ -318,3 +318,130 @@ def test_row_subset_equals_full_rows():
     os_, ls_ = oracle.attn(x["q"], x["k"], x["v"], mask, w=wl.w, rows=rows)
     np.testing.assert_array_equal(os_, o[rows.numpy()])
     np.testing.assert_array_equal(ls_, lse[rows.numpy()])
+
+
+# ---------------------------------------------------------------- backward ---
+
+def _loss(q, k, v, mask, G, w):
+    """L = sum O * G with the forward oracle (fp64)."""
+    o, _ = oracle.attn(q, k, v, mask, w=w)
+    return float((o * G).sum())
+
+
+def _bf16_neighbours(x: torch.Tensor):
+    """The two bf16 values adjacent to the bf16 scalar x (below, above)."""
+    bits = x.view(torch.int16).item()
+    a = torch.tensor([bits - 1], dtype=torch.int16).view(torch.bfloat16)[0]
+    b = torch.tensor([bits + 1], dtype=torch.int16).view(torch.bfloat16)[0]
+    return (a, b) if float(a) < float(b) else (b, a)
+
+
+def test_gradients_match_central_differences_between_adjacent_bf16_values():
+    """dL/dx ~ (L(x+) - L(x-)) / (x+ - x-) with x+- the bf16 neighbours of x: the
+    inputs stay exact, and the step (about 2^-8 |x|) leaves a truncation error far
+    below the tolerance.  General mask: window and shared groups, GQA."""
+    B, N, H, H_kv, d, K, top_k, w = 1, 48, 2, 1, 8, 4, 2, 5
+    q, k, v = _bf16((B, N, H, d), 21), _bf16((B, N, H_kv, d), 22), _bf16((B, N, H_kv, d), 23)
+    dout = _bf16((B, N, H, d), 24)
+    G = _f64(dout).reshape(B * N, H, d)
+    r, C = _routing(B, N, 1, K, seed=25)
+    mask, _, _, _ = oracle.route(r, C, K=K, top_k=top_k)
+    dq, dk, dv = oracle.attn_bwd(q, k, v, mask, dout, w=w)
+    dq, dk, dv = dq.reshape(B, N, H, d), dk.reshape(B, N, H_kv, d), dv.reshape(B, N, H_kv, d)
+    rng = np.random.default_rng(26)
+    checked = 0
+    for name, t, grad in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+        for _ in range(6):
+            idx = tuple(int(rng.integers(0, s)) for s in t.shape)
+            x = t[idx]
+            if not 0.25 < abs(float(x)) < 4.0:
+                continue
+            lo, hi = _bf16_neighbours(x)
+            tl, th = t.clone(), t.clone()
+            tl[idx], th[idx] = lo, hi
+            args_l = {"q": q, "k": k, "v": v} | {name: tl}
+            args_h = {"q": q, "k": k, "v": v} | {name: th}
+            fd = (_loss(args_h["q"], args_h["k"], args_h["v"], mask, G, w)
+                  - _loss(args_l["q"], args_l["k"], args_l["v"], mask, G, w)) / (float(hi) - float(lo))
+            assert fd == pytest.approx(grad[idx], rel=2e-3, abs=2e-5), (name, idx)
+            checked += 1
+    assert checked >= 8
+
+
+def _sdpa_grads(q, k, v, dout):
+    """torch autograd of dense causal attention (fp64), [B, N, H(_kv), d] layouts."""
+    H, H_kv = q.shape[2], k.shape[2]
+    qt = q.to(torch.float64).requires_grad_()
+    kt = k.to(torch.float64).requires_grad_()
+    vt = v.to(torch.float64).requires_grad_()
+    rep = lambda x: x.repeat_interleave(H // H_kv, dim=2).transpose(1, 2)
+    o = torch.nn.functional.scaled_dot_product_attention(qt.transpose(1, 2), rep(kt), rep(vt),
+                                                         is_causal=True)
+    (o.transpose(1, 2) * dout.to(torch.float64)).sum().backward()
+    return qt.grad.numpy(), kt.grad.numpy(), vt.grad.numpy()
+
+
+@pytest.mark.parametrize("case", ["K1", "topk_eq_K", "window_covers"])
+def test_gradients_reduce_to_dense_causal_autograd(case):
+    B, N, H, H_kv, d = 2, 90, 4, 2, 16
+    K, top_k, w = {"K1": (1, 1, 3), "topk_eq_K": (3, 3, 2), "window_covers": (4, 1, 90)}[case]
+    q, k, v = _bf16((B, N, H, d), 31), _bf16((B, N, H_kv, d), 32), _bf16((B, N, H_kv, d), 33)
+    dout = _bf16((B, N, H, d), 34)
+    r, C = _routing(B, N, 1, K, seed=35)
+    mask, _, _, _ = oracle.route(r, C, K=K, top_k=top_k)
+    dq, dk, dv = oracle.attn_bwd(q, k, v, mask, dout, w=w)
+    gq, gk, gv = _sdpa_grads(q, k, v, dout)
+    np.testing.assert_allclose(dq, gq.reshape(B * N, H, d), atol=1e-11, rtol=0)
+    np.testing.assert_allclose(dk, gk.reshape(B * N, H_kv, d), atol=1e-11, rtol=0)
+    np.testing.assert_allclose(dv, gv.reshape(B * N, H_kv, d), atol=1e-11, rtol=0)
+
+
+def test_unit_window_top1_gradients_are_per_group_causal_autograd():
+    B, N, H, d, K = 1, 120, 2, 16, 4
+    q, k, v = _bf16((B, N, H, d), 41), _bf16((B, N, H, d), 42), _bf16((B, N, H, d), 43)
+    dout = _bf16((B, N, H, d), 44)
+    r, C = _routing(B, N, 1, K, seed=45)
+    mask, _, _, _ = oracle.route(r, C, K=K, top_k=1)
+    dq, dk, dv = oracle.attn_bwd(q, k, v, mask, dout, w=1)
+    for g in range(K):
+        idx = np.nonzero(mask[0, 0] == (1 << g))[0]
+        if len(idx) == 0:
+            continue
+        sel = torch.from_numpy(idx)
+        gq, gk, gv = _sdpa_grads(q[:, sel], k[:, sel], v[:, sel], dout[:, sel])
+        np.testing.assert_allclose(dq[idx], gq[0], atol=1e-11, rtol=0)
+        np.testing.assert_allclose(dk[idx], gk[0], atol=1e-11, rtol=0)
+        np.testing.assert_allclose(dv[idx], gv[0], atol=1e-11, rtol=0)
+
+
+@pytest.mark.parametrize("B,N,H,H_kv,R,d,K,top_k,w", [
+    (2, 80, 4, 2, 2, 8, 5, 2, 6), (1, 130, 3, 1, 1, 16, 8, 3, 17)])
+def test_gradient_sum_rules(B, N, H, H_kv, R, d, K, top_k, w):
+    """Softmax rows: sum_j dS_ij = 0, so the dk of a KV head sum to zero over its keys;
+    sum_j P_ij = 1, so its dv sum to the dO of the queries that read it."""
+    q, k, v = _bf16((B, N, H, d), 51), _bf16((B, N, H_kv, d), 52), _bf16((B, N, H_kv, d), 53)
+    dout = _bf16((B, N, H, d), 54)
+    r, C = _routing(B, N, R, K, seed=55)
+    mask, _, _, _ = oracle.route(r, C, K=K, top_k=top_k)
+    _, dk, dv = oracle.attn_bwd(q, k, v, mask, dout, w=w)
+    dk, dv = dk.reshape(B, N, H_kv, d), dv.reshape(B, N, H_kv, d)
+    g = _f64(dout).reshape(B, N, H_kv, H // H_kv, d).sum(axis=3)
+    np.testing.assert_allclose(dk.sum(axis=1), 0.0, atol=1e-12)
+    np.testing.assert_allclose(dv.sum(axis=1), g.sum(axis=1), atol=1e-11)
+
+
+def test_gradient_subsets_equal_full_computation():
+    wl = synth.WORKLOADS["tiny"].replace(N=150, H=4, H_kv=2)
+    x = synth.make_inputs(wl, seed=3)
+    dout = _bf16((1, wl.N, wl.H, wl.d_head), 61)
+    mask, _, _, _ = oracle.route(x["r"], x["C"], K=wl.K, top_k=wl.top_k)
+    dq, dk, dv = oracle.attn_bwd(x["q"], x["k"], x["v"], mask, dout, w=wl.w)
+    rows = synth.sample_queries(wl.N, 12, wl.w, seed=4)
+    keys = synth.sample_queries(wl.N, 9, wl.w, seed=5)
+    dq_s, dk_s, dv_s = oracle.attn_bwd(x["q"], x["k"], x["v"], mask, dout, w=wl.w, rows=rows,
+                                       keys=keys, heads=[2, 3])
+    np.testing.assert_allclose(dq_s, dq[rows.numpy()][:, [2, 3]], atol=1e-12, rtol=0)
+    # KV head 1 is read by query heads 2 and 3 only
+    np.testing.assert_allclose(dk_s[:, 1], dk[keys.numpy(), 1], atol=1e-12, rtol=0)
+    np.testing.assert_allclose(dv_s[:, 1], dv[keys.numpy(), 1], atol=1e-12, rtol=0)
+    assert np.all(dk_s[:, 0] == 0) and np.all(dv_s[:, 0] == 0)
