@@ -243,13 +243,39 @@ int focus_get_status(const void* ws, void* stream);
  *   o        [B, H, d_head] bf16 out;  lse [B, H] fp32 out or NULL
  *   ws       focus_decode_workspace_size(p) bytes
  * p->N is the cache length including the newest token. Split over the keys in
- * chunks of 512 (one CTA per chunk, KV head and up to 8 of its query heads), then
+ * chunks of 256 (one CTA per chunk, KV head and up to 8 of its query heads), then
  * an LSE merge of the chunks.
  */
 size_t focus_decode_workspace_size(const focus_params* p);
 int focus_decode(const focus_params* p, const uint16_t* q, const uint16_t* k_cache,
                  const uint16_t* v_cache, const uint32_t* mask, uint16_t* o, float* lse,
                  void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Backward pass of focus_attn_fwd with the group masks held fixed (hard top-k):
+ * gradients of the loss with respect to q, k and v, given its gradient dO with
+ * respect to o.  With P_ij = exp(scale q_i.k_j - LSE_i) over the same union set
+ * A_i:  dP_ij = dO_i.v_j,  D_i = dO_i.o_i,  dS_ij = P_ij (dP_ij - D_i),
+ *   dq_i = scale sum_j dS_ij k_j,  dk_j = scale sum_i dS_ij q_i,  dv_j = sum_i P_ij dO_i,
+ * where a KV head sums over the query heads that read it.  The masks are piecewise
+ * constant in r and C, so the routing inputs get no gradient (none is returned).
+ *   q, o, d_o  [B, N, H, d_head] bf16 (o: the forward output)
+ *   k, v       [B, N, H_kv, d_head] bf16
+ *   mask       [B, R, N] uint32: the masks the forward used (e.g. focus_route's)
+ *   lse        [B, H, N] fp32: the forward's LSE
+ *   dq         [B, N, H, d_head] bf16 out;  dk, dv [B, N, H_kv, d_head] bf16 out
+ *   ws         focus_bwd_workspace_size(p) bytes
+ * Runs over exact-set segments whatever p->schedule says (so C(K, top_k) <=
+ * FOCUS_MAX_SEGMENTS, else FOCUS_ERR_UNSUPPORTED).  Steps on `stream`: bucket,
+ * block schedule and backward plans, permuted copies of Q/K/V/dO, D, then per
+ * pass (window, long-range) a query-major dQ kernel and a key-major dK/dV kernel
+ * on the tensor cores.  Deterministic: no atomics.
+ */
+size_t focus_bwd_workspace_size(const focus_params* p);
+int focus_attn_bwd(const focus_params* p, const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                   const uint32_t* mask, const uint16_t* o, const float* lse, const uint16_t* d_o,
+                   uint16_t* dq, uint16_t* dk, uint16_t* dv, void* ws, size_t ws_bytes,
+                   void* stream);
 
 /*
  * Diagnostic of the device-side failure path (no counterpart in the paper): runs

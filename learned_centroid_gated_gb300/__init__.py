@@ -116,6 +116,10 @@ N_STAGE_EVENTS = 6
 STAGES = ("route", "bucket", "permute", "attn_window", "attn_long")
 _lib.focus_route_static.argtypes = [_PP, _P, _P, _P, _P, _P]
 _lib.focus_route_static.restype = ctypes.c_int
+_lib.focus_bwd_workspace_size.argtypes = [_PP]
+_lib.focus_bwd_workspace_size.restype = ctypes.c_size_t
+_lib.focus_attn_bwd.argtypes = [_PP, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]
+_lib.focus_attn_bwd.restype = ctypes.c_int
 _lib.focus_decode_workspace_size.argtypes = [_PP]
 _lib.focus_decode_workspace_size.restype = ctypes.c_size_t
 _lib.focus_decode.argtypes = [_PP, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]
@@ -345,6 +349,32 @@ def decode(p: Params, q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Ten
                              _ptr(mask.contiguous()), _ptr(out), _ptr(lse), _ptr(ws), ws.numel(),
                              _stream(stream)), "focus_decode")
     return out, lse
+
+
+def bwd_workspace_size(p: Params) -> int:
+    return int(_lib.focus_bwd_workspace_size(ctypes.byref(p.c())))
+
+
+def attn_bwd(p: Params, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, mask: torch.Tensor,
+             o: torch.Tensor, lse: torch.Tensor, d_o: torch.Tensor, *, dq=None, dk=None, dv=None,
+             ws=None, stream=None):
+    """Backward of attn_fwd with the masks held fixed.  q, o, d_o [B, N, H, d] bf16;
+    k, v [B, N, H_kv, d] bf16; mask [B, R, N] (the forward's); lse [B, H, N] fp32 (the
+    forward's).  Returns (dq, dk, dv) bf16 in the layouts of q, k, v."""
+    for t in (q, k, v, o, d_o):
+        _bf16_bits(t)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    need = bwd_workspace_size(p)
+    if need == 0:
+        raise FocusError(-2, "focus_bwd_workspace_size")
+    if ws is None or ws.numel() < need:
+        ws = torch.empty(need, dtype=torch.uint8, device=q.device)
+    _check(_lib.focus_attn_bwd(ctypes.byref(p.c()), _ptr(q), _ptr(k), _ptr(v), _ptr(mask.contiguous()),
+                               _ptr(o), _ptr(lse.contiguous()), _ptr(d_o), _ptr(dq), _ptr(dk), _ptr(dv),
+                               _ptr(ws), ws.numel(), _stream(stream)), "focus_attn_bwd")
+    return dq, dk, dv
 
 
 def selftest_timeout(device="cuda", stream=None) -> int:

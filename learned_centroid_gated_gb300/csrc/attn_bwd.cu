@@ -1,0 +1,1062 @@
+// Focus attention backward on the 5th-generation tensor cores (tcgen05, TMEM, TMA).
+//
+// "Why Attend to Everything? Focus is the Key", gist.science technical summary,
+// section 2 "Core Architecture" and "Inference Efficiency (Top-k)": one exact
+// softmax over the window keys and the distant keys that share a group.  With the
+// hard mask held fixed, the gradients of that softmax are (s = scale q.k over the
+// attended set A_i, P = exp(s - LSE)):
+//   dP_ij = dO_i . v_j,  D_i = dO_i . O_i,  dS_ij = P_ij (dP_ij - D_i),
+//   dQ_i = scale sum_j dS_ij k_j,  dK_j = scale sum_i dS_ij q_i,  dV_j = sum_i P_ij dO_i.
+// (Section 5 "Significance and Implications" of the same summary notes that
+// training with the soft gate still visits all pairs; this is the hard-mask form.)
+//
+// Two persistent kernels, each in a window pass (token order, keys (i - w, i])
+// and a long-range pass (compatible exact-set segments, permuted copies); no
+// atomics, so the result is deterministic:
+//   bwd_dq<D, LONG>    query-major: 128 query rows of one head per item.  Their Q
+//                      and dO rows are staged in TMEM as the A operands; for each
+//                      64-key tile: S = Q K^T and dP = dO V^T into one of two TMEM
+//                      buffers, dS (bf16) written over S by the elementwise warps,
+//                      dQ += dS K.  The tensor core computes tile t+1 while the
+//                      warps work on tile t.
+//   bwd_dkdv<D, LONG>  key-major: 128 key rows of one KV head per item, every
+//                      query head of its group.  K and V rows staged in TMEM; for
+//                      each 32-query tile: S^T = K Q^T, dP^T = V dO^T, P^T and dS^T
+//                      (bf16) written over them, dV += P^T dO, dK += dS^T Q.
+// The window pass writes fp32 partials; the long-range pass adds them and writes
+// the bf16 gradients (the two key sets are disjoint, so the sums are the totals).
+//
+// Warps: 0-7 elementwise (two warpgroups, each a column half of every tile, lane =
+// TMEM row), 8 producer (TMA; in bwd_dkdv the whole warp also stages the tile's
+// per-query LSE, D and position), 9 MMA issuer, 10-11 idle.
+#include <math.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "tc_ptx.cuh"
+
+namespace focus {
+namespace {
+
+using namespace ptx;
+
+constexpr int NTHREADS = 384;
+constexpr int PRODUCER_WARP = 8;
+constexpr int MMA_WARP = 9;
+constexpr int BM = kBwdBlock;       // rows per item
+constexpr int NK = kBwdKeyTile;     // keys per dQ tile
+constexpr int NQ = kBwdQryTile;     // queries per dK/dV tile
+constexpr uint32_t TMEM_COLS = 512;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kMinSmem = 116 * 1024;  // > half the SM's shared memory: one CTA per SM
+
+// Barrier block shared by both kernels: full[NST], empty[NST], sdp[2], ds[2], a,
+// fin, drain (8 bytes each), the TMEM address word and the abort flag.
+template <int NST>
+struct Bars {
+  static constexpr int FULL = 0, EMPTY = 8 * NST, SDP = 16 * NST, DS = SDP + 16, A = DS + 16;
+  static constexpr int FIN = A + 8, DRAIN = FIN + 8, TMEM_SLOT = DRAIN + 8, ABORT = TMEM_SLOT + 4;
+  static constexpr int BYTES = 256;
+  static_assert(ABORT + 4 <= BYTES, "barrier block overflow");
+};
+
+template <int D>
+struct DqLayout {
+  static constexpr int NST = 4;
+  static constexpr int BOX = NK * 128;           // 64 rows x 128 bytes
+  static constexpr int TILE = (D / 64) * BOX;    // one 64-key tile of K or V
+  static constexpr int RING = 0;                 // [NST][K tile, V tile]
+  static constexpr int BAR = RING + NST * 2 * TILE;
+  static constexpr int SMEM = BAR + Bars<NST>::BYTES + 1024;
+  // TMEM columns
+  static constexpr int COL_Q = 0, COL_DO = D / 2, COL_S = D, COL_DP = D + 2 * NK, COL_DQ = D + 4 * NK;
+  static_assert(COL_DQ + D <= (int)TMEM_COLS, "tensor memory budget");
+};
+
+template <int D>
+struct DkvLayout {
+  static constexpr int NST = 8;
+  static constexpr int BOX = NQ * 128;           // 32 rows x 128 bytes
+  static constexpr int TILE = (D / 64) * BOX;    // one 32-query tile of Q or dO
+  static constexpr int RING = 0;                 // [NST][Q tile, dO tile]
+  static constexpr int SCAL = RING + NST * 2 * TILE;  // [NST][lse2, D, pos][32]
+  static constexpr int BAR = SCAL + NST * 3 * NQ * 4;
+  static constexpr int SMEM = BAR + Bars<NST>::BYTES + 1024;
+  static constexpr int COL_K = 0, COL_V = D / 2, COL_ST = D, COL_DPT = D + 2 * NQ;
+  static constexpr int COL_DK = D + 4 * NQ, COL_DV = COL_DK + D;
+  static_assert(COL_DV + D <= (int)TMEM_COLS, "tensor memory budget");
+};
+
+struct BwdArgs {
+  int B, N, H, H_kv, R, w, nseg, qtab_cap, NR;
+  float sl2;    // softmax scale * log2(e)
+  float scale;  // softmax scale
+  const int* perm;
+  const QBlock* qtab;
+  const int* qtab_count;
+  const PlanHead* qhead;
+  const PlanEnt* qent;
+  const PlanHead* rhead;
+  const PlanEnt* rent;
+  const bf16* q;
+  const bf16* k;
+  const bf16* v;
+  const bf16* dout;
+  const float* lse;   // [B, H, N]
+  const float* dvec;  // [B, H, N]: D = dO . O
+  float* dq_w;        // window partials, fp32, token order
+  float* dk_w;
+  float* dv_w;
+  bf16* dq;           // gradients, bf16, token order
+  bf16* dk;
+  bf16* dv;
+  int* status;
+  long long timeout_cycles;
+};
+
+struct BItem {
+  bool valid;
+  int b, h, kvh, br, u, row0, rows;
+  int n;     // tiles
+  int nsub;  // dK/dV: tiles per query head
+  int lo, hi;
+};
+
+// dQ items: (query head, 128-row block).  Long: heads sharing a KV head adjacent.
+template <bool LONG>
+__device__ __forceinline__ BItem dq_item(const BwdArgs& a, int x) {
+  BItem it{};
+  const int gq = a.H / a.H_kv;
+  if constexpr (LONG) {
+    const int nkv = a.H_kv / a.R;
+    const int jq = x % gq;
+    const int rest = x / gq;
+    const int u = rest % a.qtab_cap, kvl = rest / a.qtab_cap;
+    it.valid = u < *a.qtab_count;
+    if (!it.valid) return it;
+    const QBlock e = a.qtab[u];
+    it.u = u;
+    it.br = e.br;
+    it.b = e.br / a.R;
+    it.kvh = (e.br % a.R) * nkv + kvl;
+    it.h = it.kvh * gq + jq;
+    it.row0 = e.row0;
+    it.rows = e.rows;
+    it.n = a.qhead[u].n_tiles;
+  } else {
+    const int nqb = (a.N + BM - 1) / BM;
+    const int bh = x / nqb;
+    it.valid = true;
+    it.h = bh % a.H;
+    it.b = bh / a.H;
+    it.kvh = it.h / gq;
+    it.row0 = (x % nqb) * BM;
+    it.rows = min(BM, a.N - it.row0);
+    it.lo = max(0, it.row0 - a.w + 1);
+    it.hi = it.row0 + it.rows;
+    it.n = (it.hi - it.lo + NK - 1) / NK;
+  }
+  return it;
+}
+
+// dK/dV items: (KV head, 128-row key block).  Long: key blocks of early positions
+// (the most queries) first.
+template <bool LONG>
+__device__ __forceinline__ BItem dkv_item(const BwdArgs& a, int x) {
+  BItem it{};
+  const int gq = a.H / a.H_kv;
+  if constexpr (LONG) {
+    const int nkv = a.H_kv / a.R;
+    const int ur = x % a.qtab_cap, kvl = x / a.qtab_cap;
+    const int cnt = *a.qtab_count;
+    it.valid = ur < cnt;
+    if (!it.valid) return it;
+    const int u = cnt - 1 - ur;
+    const QBlock e = a.qtab[u];
+    it.u = u;
+    it.br = e.br;
+    it.b = e.br / a.R;
+    it.kvh = (e.br % a.R) * nkv + kvl;
+    it.row0 = e.row0;
+    it.rows = e.rows;
+    it.nsub = a.rhead[u].n_tiles;
+    it.n = gq * it.nsub;
+  } else {
+    const int nkb = (a.N + BM - 1) / BM;
+    const int bk = x / nkb;
+    it.valid = true;
+    it.kvh = bk % a.H_kv;
+    it.b = bk / a.H_kv;
+    it.row0 = (x % nkb) * BM;
+    it.rows = min(BM, a.N - it.row0);
+    it.lo = it.row0;
+    it.hi = min(a.N, it.row0 + it.rows + a.w - 1);
+    it.nsub = (it.hi - it.lo + NQ - 1) / NQ;
+    it.n = gq * it.nsub;
+  }
+  return it;
+}
+
+// Walks the key tiles of a dQ item: first key row (permuted row in the long pass,
+// token in the window pass), keys in the tile, and whether every key of the tile
+// is allowed for every row of the block (long pass).
+struct DqWalk {
+  int e, t_in;
+  PlanEnt pe;
+  __device__ __forceinline__ void init(const BwdArgs& a, const BItem& it, bool LONG) {
+    e = 0;
+    t_in = 0;
+    pe = PlanEnt{0, 0, 0, 0};
+    if (LONG && it.n > 0) pe = a.qent[(int64_t)it.u * a.nseg];
+  }
+  // fills (start, cnt, full) of tile t and moves on
+  __device__ __forceinline__ void next(const BwdArgs& a, const BItem& it, bool LONG, int t,
+                                       int& start, int& cnt, bool& full) {
+    if (LONG) {
+      start = pe.start + t_in * NK;
+      cnt = min(NK, pe.cnt - t_in * NK);
+      full = t_in * NK + cnt <= pe.nfull;
+      if (++t_in * NK >= pe.cnt && ++e < a.nseg) {
+        t_in = 0;
+        pe = a.qent[(int64_t)it.u * a.nseg + e];
+      }
+    } else {
+      start = it.lo + t * NK;
+      cnt = min(NK, it.hi - start);
+      full = false;
+    }
+  }
+};
+
+// Walks the query tiles of a dK/dV item: query head, first query row, count.
+struct DkvWalk {
+  int jq, e, t_in, n_ent;
+  PlanEnt pe;
+  __device__ __forceinline__ void init(const BwdArgs& a, const BItem& it, bool LONG) {
+    jq = e = t_in = 0;
+    n_ent = 0;
+    pe = PlanEnt{0, 0, 0, 0};
+    if (LONG && it.n > 0) {
+      n_ent = a.rhead[it.u].n_ent;
+      pe = a.rent[(int64_t)it.u * a.nseg];
+    }
+  }
+  __device__ __forceinline__ void next(const BwdArgs& a, const BItem& it, bool LONG, int t,
+                                       int& h, int& start, int& cnt) {
+    const int gq = a.H / a.H_kv;
+    if (LONG) {
+      h = it.kvh * gq + jq;
+      start = pe.start + t_in * NQ;
+      cnt = min(NQ, pe.cnt - t_in * NQ);
+      if (++t_in * NQ >= pe.cnt) {
+        t_in = 0;
+        if (++e >= n_ent) {
+          e = 0;
+          ++jq;
+        }
+        pe = a.rent[(int64_t)it.u * a.nseg + e];
+      }
+    } else {
+      const int s = t % it.nsub;
+      h = it.kvh * gq + t / it.nsub;
+      start = it.lo + s * NQ;
+      cnt = min(NQ, it.hi - start);
+    }
+  }
+};
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// First index in [lo, hi) with P[index] > x (P ascending), or hi.
+__device__ __forceinline__ int upper_bound_g(const int* __restrict__ P, int lo, int hi, int x) {
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(P + mid) <= x) lo = mid + 1; else hi = mid;
+  }
+  return lo;
+}
+
+// Stages one bf16 row of D values (src, 16-byte aligned; zeros when src is null)
+// into TMEM columns [col, col + D/2) of this thread's lane as bf16 pairs.
+template <int D>
+__device__ __forceinline__ void stage_row(uint32_t taddr, const bf16* src) {
+#pragma unroll
+  for (int c = 0; c < D / 64; ++c) {
+    uint32_t r[32];
+    if (src) {
+      const uint4* s4 = reinterpret_cast<const uint4*>(src) + c * 8;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint4 x = __ldg(s4 + i);
+        r[4 * i] = x.x;
+        r[4 * i + 1] = x.y;
+        r[4 * i + 2] = x.z;
+        r[4 * i + 3] = x.w;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) r[i] = 0u;
+    }
+    tmem_st32(taddr + 32 * c, r);
+  }
+}
+
+// Epilogue helper: 32 fp32 accumulator columns of this lane -> window partial
+// (fp32) or, in the long pass, partial + these -> bf16 gradient.
+template <bool LONG>
+__device__ __forceinline__ void emit32(const uint32_t (&y)[32], float mul, float* part,
+                                       bf16* out) {
+  if constexpr (!LONG) {
+    float4* dst = reinterpret_cast<float4*>(part);
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      dst[i] = make_float4(__uint_as_float(y[4 * i]) * mul, __uint_as_float(y[4 * i + 1]) * mul,
+                           __uint_as_float(y[4 * i + 2]) * mul, __uint_as_float(y[4 * i + 3]) * mul);
+  } else {
+    const float4* src = reinterpret_cast<const float4*>(part);
+    uint32_t pk[16];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float4 w = src[i];
+      pk[2 * i] = pack_bf16(w.x + __uint_as_float(y[4 * i]) * mul, w.y + __uint_as_float(y[4 * i + 1]) * mul);
+      pk[2 * i + 1] =
+          pack_bf16(w.z + __uint_as_float(y[4 * i + 2]) * mul, w.w + __uint_as_float(y[4 * i + 3]) * mul);
+    }
+    uint4* dst = reinterpret_cast<uint4*>(out);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+  }
+}
+
+// Common prologue: TMEM allocation, barrier initialisation.
+template <int NST>
+__device__ __forceinline__ void init_cta(uint8_t* bar, int warp, uint32_t full_count) {
+  using BB = Bars<NST>;
+  const uint32_t base = smem_u32(bar);
+  if (warp == MMA_WARP) {
+    tmem_alloc(base + BB::TMEM_SLOT, TMEM_COLS);
+    tmem_relinquish();
+  }
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NST; ++s) {
+      mbar_init(base + BB::FULL + 8 * s, full_count);
+      mbar_init(base + BB::EMPTY + 8 * s, 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(base + BB::SDP + 8 * t, 1);
+      mbar_init(base + BB::DS + 8 * t, 256);
+    }
+    mbar_init(base + BB::A, 256);
+    mbar_init(base + BB::FIN, 1);
+    mbar_init(base + BB::DRAIN, 1);
+    *reinterpret_cast<volatile int*>(bar + BB::ABORT) = 0;
+    fence_barrier_init();
+    fence_proxy_async_smem();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+}
+
+// ================================================================ dQ kernel ==
+template <int D, bool LONG>
+__global__ void __launch_bounds__(NTHREADS, 1)
+bwd_dq(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv,
+       const BwdArgs a, const int n_items) {
+  using L = DqLayout<D>;
+  using BB = Bars<L::NST>;
+  constexpr int NST = L::NST;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  uint8_t* bar = sm + L::BAR;
+  const uint32_t bb = smem_u32(bar);
+  const uint32_t b_full = bb + BB::FULL, b_empty = bb + BB::EMPTY, b_sdp = bb + BB::SDP;
+  const uint32_t b_ds = bb + BB::DS, b_a = bb + BB::A, b_fin = bb + BB::FIN, b_drain = bb + BB::DRAIN;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bar + BB::ABORT);
+  init_cta<NST>(bar, warp, 1);
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(bar + BB::TMEM_SLOT);
+  int* status = a.status;
+  const long long tlim = a.timeout_cycles;
+
+  if (warp == PRODUCER_WARP) {
+    if (lane == 0) {
+      tma_prefetch(&mk);
+      tma_prefetch(&mv);
+      int last_par[NST];
+      for (int s = 0; s < NST; ++s) last_par[s] = -1;
+      int g = 0;
+      bool ok = true;
+      for (int x = blockIdx.x; ok && x < n_items; x += gridDim.x) {
+        const BItem it = dq_item<LONG>(a, x);
+        if (!it.valid || it.n == 0) continue;
+        DqWalk wk;
+        wk.init(a, it, LONG);
+        for (int t = 0; t < it.n && ok; ++t, ++g) {
+          int start, cnt;
+          bool full;
+          wk.next(a, it, LONG, t, start, cnt, full);
+          const int slot = g % NST;
+          const uint32_t par = (uint32_t)((g / NST) & 1);
+          if (!(ok = mbar_wait(b_empty + 8 * slot, par ^ 1, abort_flag, status, tlim))) break;
+          const uint32_t fb = b_full + 8 * slot;
+          mbar_expect_tx(fb, 2 * L::TILE);
+          for (int kv = 0; kv < 2; ++kv)
+            for (int bx = 0; bx < D / 64; ++bx) {
+              const uint32_t dst = smem_u32(sm + L::RING + (slot * 2 + kv) * L::TILE + bx * L::BOX);
+              const CUtensorMap* m = kv ? &mv : &mk;
+              if constexpr (LONG)
+                tma_load_2d(dst, m, 64 * bx, (it.b * a.H_kv + it.kvh) * a.NR + start, fb);
+              else
+                tma_load_3d(dst, m, 64 * bx, it.kvh, it.b * a.N + start, fb);
+            }
+          last_par[slot] = (int)par;
+        }
+      }
+      if (*abort_flag)
+        for (int s = 0; s < NST; ++s)
+          if (last_par[s] >= 0) mbar_drain(b_full + 8 * s, (uint32_t)last_par[s]);
+    }
+    __syncwarp();
+  } else if (warp == MMA_WARP) {
+    if (lane == 0) {
+      constexpr uint32_t ISD = idesc_bf16(128, NK, 0);  // S = Q K^T, dP = dO V^T
+      constexpr uint32_t IDQ = idesc_bf16(128, D, 1);   // dQ += dS K (K MN-major)
+      const uint32_t r_base = smem_u32(sm + L::RING);
+      auto kaddr = [&](int g) { return r_base + (g % NST) * 2 * L::TILE; };
+      auto ring_wait = [&](int g) {
+        return mbar_wait(b_full + 8 * (g % NST), (uint32_t)((g / NST) & 1), abort_flag, status, tlim);
+      };
+      auto issue_sdp = [&](int g) {
+        const int buf = g & 1;
+        const uint32_t ka = kaddr(g), va = ka + L::TILE;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk / 4) * L::BOX + (kk % 4) * 32;
+          umma_ts(tmem + L::COL_S + NK * buf, tmem + L::COL_Q + 8 * kk, sw128_desc(ka + off, 16, 1024),
+                  ISD, kk > 0);
+        }
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk / 4) * L::BOX + (kk % 4) * 32;
+          umma_ts(tmem + L::COL_DP + NK * buf, tmem + L::COL_DO + 8 * kk,
+                  sw128_desc(va + off, 16, 1024), ISD, kk > 0);
+        }
+        umma_commit(b_sdp + 8 * buf);
+      };
+      int g = 0, ac = 0;
+      bool ok = true;
+      for (int x = blockIdx.x; ok && x < n_items; x += gridDim.x) {
+        const BItem it = dq_item<LONG>(a, x);
+        if (!it.valid || it.n == 0) continue;
+        if (!(ok = mbar_wait(b_a, (uint32_t)(ac & 1), abort_flag, status, tlim))) break;
+        ++ac;
+        if (!(ok = ring_wait(g))) break;
+        tc_fence_after();
+        issue_sdp(g);
+        for (int t = 0; t < it.n; ++t) {
+          const int gc = g + t;
+          if (t + 1 < it.n) {
+            if (!(ok = ring_wait(gc + 1))) break;
+            tc_fence_after();
+            issue_sdp(gc + 1);
+          }
+          if (!(ok = mbar_wait(b_ds + 8 * (gc & 1), (uint32_t)((gc >> 1) & 1), abort_flag, status, tlim)))
+            break;
+          tc_fence_after();
+          const uint32_t ka = kaddr(gc);
+          const uint32_t sc = tmem + L::COL_S + NK * (gc & 1);
+#pragma unroll
+          for (int kk = 0; kk < NK / 16; ++kk)
+            umma_ts(tmem + L::COL_DQ, sc + 32 * (kk >> 1) + 8 * (kk & 1),
+                    sw128_desc(ka + kk * 2048, L::BOX, 1024), IDQ, (t > 0 || kk > 0) ? 1u : 0u);
+          umma_commit(b_empty + 8 * (gc % NST));
+        }
+        if (!ok) break;
+        umma_commit(b_fin);
+        g += it.n;
+      }
+      umma_commit(b_drain);
+      mbar_drain(b_drain, 0);
+    }
+    __syncwarp();
+  } else if (warp < 8) {
+    // ---------------------------------------------------------- elementwise --
+    const int wg = warp >> 2;
+    const int r = (warp & 3) * 32 + lane;
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t tl = tmem + lane_off;
+    const float sl2 = a.sl2;
+    int g = 0, ac = 0;
+    bool ok = true;
+    for (int x = blockIdx.x; ok && x < n_items; x += gridDim.x) {
+      const BItem it = dq_item<LONG>(a, x);
+      if (!it.valid) continue;
+      const bool row_ok = r < it.rows;
+      const int rr = min(r, it.rows - 1);
+      const int* P = LONG ? a.perm + (int64_t)it.br * a.NR : nullptr;
+      const int qp = LONG ? __ldg(P + it.row0 + rr) : it.row0 + rr;
+      const int64_t grow = ((int64_t)it.b * a.N + qp) * a.H + it.h;  // [B, N, H] row
+      if (it.n > 0) {
+        const bf16* src = (wg == 0 ? a.q : a.dout) + grow * D;
+        stage_row<D>(tl + (wg == 0 ? L::COL_Q : L::COL_DO), row_ok ? src : nullptr);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(b_a);
+        ++ac;
+      }
+      const int64_t li = ((int64_t)it.b * a.H + it.h) * a.N + qp;
+      const float lse2 = __ldg(a.lse + li) * kLog2e;
+      const float Dr = __ldg(a.dvec + li);
+      DqWalk wk;
+      wk.init(a, it, LONG);
+      for (int t = 0; t < it.n; ++t) {
+        const int gc = g + t, buf = gc & 1;
+        int start, cnt;
+        bool full;
+        wk.next(a, it, LONG, t, start, cnt, full);
+        int c_lo = 0, c_hi;
+        if constexpr (LONG) c_hi = full ? cnt : upper_bound_g(P + start, 0, cnt, qp - a.w);
+        else {
+          c_lo = max(0, qp - a.w + 1 - start);
+          c_hi = min(cnt, qp - start + 1);
+        }
+        if (!row_ok) c_hi = c_lo;
+        const uint32_t width = (uint32_t)max(c_hi - c_lo, 0);
+        ok = mbar_wait(b_sdp + 8 * buf, (uint32_t)((gc >> 1) & 1), abort_flag, status, tlim);
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t s[32], dp[32];
+        tmem_ld32(tl + L::COL_S + NK * buf + 32 * wg, s);
+        tmem_ld32(tl + L::COL_DP + NK * buf + 32 * wg, dp);
+        tmem_ld_wait(s);
+        tie32(dp);
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int c0 = 32 * wg + 2 * i;
+          float ds[2];
+#pragma unroll
+          for (int h2 = 0; h2 < 2; ++h2) {
+            const float pr = ex2(fmaf(__uint_as_float(s[2 * i + h2]), sl2, -lse2));
+            const float p = ((uint32_t)(c0 + h2 - c_lo) < width) ? pr : 0.0f;
+            ds[h2] = p * (__uint_as_float(dp[2 * i + h2]) - Dr);
+          }
+          pk[i] = pack_bf16(ds[0], ds[1]);
+        }
+        tmem_st16(tl + L::COL_S + NK * buf + 32 * wg, pk);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(b_ds + 8 * buf);
+      }
+      if (!ok) break;
+      // ---- epilogue: dQ = scale * (dS K), window partial or final ----
+      if (it.n > 0) {
+        ok = mbar_wait(b_fin, (uint32_t)((ac - 1) & 1), abort_flag, status, tlim);
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+      }
+      g += it.n;
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c) {
+        const int col = wg * (D / 2) + 32 * c;
+        uint32_t y[32];
+        if (it.n > 0) {
+          tmem_ld32(tl + L::COL_DQ + col, y);
+          tmem_ld_wait(y);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) y[i] = 0u;
+        }
+        if (row_ok) emit32<LONG>(y, a.scale, a.dq_w + grow * D + col, a.dq + grow * D + col);
+      }
+      tc_fence_before();
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == MMA_WARP) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+// ============================================================= dK/dV kernel ==
+template <int D, bool LONG>
+__global__ void __launch_bounds__(NTHREADS, 1)
+bwd_dkdv(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mdo,
+         const BwdArgs a, const int n_items) {
+  using L = DkvLayout<D>;
+  using BB = Bars<L::NST>;
+  constexpr int NST = L::NST;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  uint8_t* bar = sm + L::BAR;
+  const uint32_t bb = smem_u32(bar);
+  const uint32_t b_full = bb + BB::FULL, b_empty = bb + BB::EMPTY, b_sdp = bb + BB::SDP;
+  const uint32_t b_ds = bb + BB::DS, b_a = bb + BB::A, b_fin = bb + BB::FIN, b_drain = bb + BB::DRAIN;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bar + BB::ABORT);
+  float* scal = reinterpret_cast<float*>(sm + L::SCAL);  // [NST][3][NQ]
+  init_cta<NST>(bar, warp, 2);
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(bar + BB::TMEM_SLOT);
+  int* status = a.status;
+  const long long tlim = a.timeout_cycles;
+
+  if (warp == PRODUCER_WARP) {
+    // whole warp: lane 0 issues the copies, every lane stages one query's scalars
+    if (lane == 0) {
+      tma_prefetch(&mq);
+      tma_prefetch(&mdo);
+    }
+    int last_par[NST];
+    for (int s = 0; s < NST; ++s) last_par[s] = -1;
+    int g = 0;
+    bool ok = true;
+    for (int x = blockIdx.x; ok && x < n_items; x += gridDim.x) {
+      const BItem it = dkv_item<LONG>(a, x);
+      if (!it.valid || it.n == 0) continue;
+      DkvWalk wk;
+      wk.init(a, it, LONG);
+      const int* P = LONG ? a.perm + (int64_t)it.br * a.NR : nullptr;
+      for (int t = 0; t < it.n; ++t, ++g) {
+        int h, start, cnt;
+        wk.next(a, it, LONG, t, h, start, cnt);
+        const int slot = g % NST;
+        const uint32_t par = (uint32_t)((g / NST) & 1);
+        if (lane == 0) ok = mbar_wait(b_empty + 8 * slot, par ^ 1, abort_flag, status, tlim);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        const uint32_t fb = b_full + 8 * slot;
+        if (lane == 0) {
+          mbar_expect_tx(fb, 2 * L::TILE);
+          for (int kv = 0; kv < 2; ++kv)
+            for (int bx = 0; bx < D / 64; ++bx) {
+              const uint32_t dst = smem_u32(sm + L::RING + (slot * 2 + kv) * L::TILE + bx * L::BOX);
+              const CUtensorMap* m = kv ? &mdo : &mq;
+              if constexpr (LONG)
+                tma_load_2d(dst, m, 64 * bx, (it.b * a.H + h) * a.NR + start, fb);
+              else
+                tma_load_3d(dst, m, 64 * bx, h, it.b * a.N + start, fb);
+            }
+        }
+        // query scalars: LSE * log2(e) (+inf marks "no query"), D, position
+        float lse2 = INFINITY, dd = 0.0f;
+        int pos = 0;
+        if (lane < cnt) {
+          pos = LONG ? __ldg(P + start + lane) : start + lane;
+          const int64_t li = ((int64_t)it.b * a.H + h) * a.N + pos;
+          lse2 = __ldg(a.lse + li) * kLog2e;
+          dd = __ldg(a.dvec + li);
+        }
+        float* sc = scal + slot * 3 * NQ;
+        sc[lane] = lse2;
+        sc[NQ + lane] = dd;
+        reinterpret_cast<int*>(sc)[2 * NQ + lane] = pos;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(fb);
+        last_par[slot] = (int)par;
+      }
+    }
+    if (lane == 0 && *abort_flag)
+      for (int s = 0; s < NST; ++s)
+        if (last_par[s] >= 0) mbar_drain(b_full + 8 * s, (uint32_t)last_par[s]);
+    __syncwarp();
+  } else if (warp == MMA_WARP) {
+    if (lane == 0) {
+      constexpr uint32_t IST = idesc_bf16(128, NQ, 0);  // S^T = K Q^T, dP^T = V dO^T
+      constexpr uint32_t IKV = idesc_bf16(128, D, 1);   // dV += P^T dO, dK += dS^T Q
+      const uint32_t r_base = smem_u32(sm + L::RING);
+      auto qaddr = [&](int g) { return r_base + (g % NST) * 2 * L::TILE; };
+      auto ring_wait = [&](int g) {
+        return mbar_wait(b_full + 8 * (g % NST), (uint32_t)((g / NST) & 1), abort_flag, status, tlim);
+      };
+      auto issue_st = [&](int g) {
+        const int buf = g & 1;
+        const uint32_t qa = qaddr(g), da = qa + L::TILE;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk / 4) * L::BOX + (kk % 4) * 32;
+          umma_ts(tmem + L::COL_ST + NQ * buf, tmem + L::COL_K + 8 * kk, sw128_desc(qa + off, 16, 1024),
+                  IST, kk > 0);
+        }
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk / 4) * L::BOX + (kk % 4) * 32;
+          umma_ts(tmem + L::COL_DPT + NQ * buf, tmem + L::COL_V + 8 * kk,
+                  sw128_desc(da + off, 16, 1024), IST, kk > 0);
+        }
+        umma_commit(b_sdp + 8 * buf);
+      };
+      int g = 0, ac = 0;
+      bool ok = true;
+      for (int x = blockIdx.x; ok && x < n_items; x += gridDim.x) {
+        const BItem it = dkv_item<LONG>(a, x);
+        if (!it.valid || it.n == 0) continue;
+        if (!(ok = mbar_wait(b_a, (uint32_t)(ac & 1), abort_flag, status, tlim))) break;
+        ++ac;
+        if (!(ok = ring_wait(g))) break;
+        tc_fence_after();
+        issue_st(g);
+        for (int t = 0; t < it.n; ++t) {
+          const int gc = g + t, buf = gc & 1;
+          if (t + 1 < it.n) {
+            if (!(ok = ring_wait(gc + 1))) break;
+            tc_fence_after();
+            issue_st(gc + 1);
+          }
+          if (!(ok = mbar_wait(b_ds + 8 * buf, (uint32_t)((gc >> 1) & 1), abort_flag, status, tlim)))
+            break;
+          tc_fence_after();
+          const uint32_t qa = qaddr(gc), da = qa + L::TILE;
+#pragma unroll
+          for (int kk = 0; kk < NQ / 16; ++kk) {
+            const uint32_t acc = (t > 0 || kk > 0) ? 1u : 0u;
+            umma_ts(tmem + L::COL_DV, tmem + L::COL_ST + NQ * buf + 16 * kk,
+                    sw128_desc(da + kk * 2048, L::BOX, 1024), IKV, acc);
+            umma_ts(tmem + L::COL_DK, tmem + L::COL_DPT + NQ * buf + 16 * kk,
+                    sw128_desc(qa + kk * 2048, L::BOX, 1024), IKV, acc);
+          }
+          umma_commit(b_empty + 8 * (gc % NST));
+        }
+        if (!ok) break;
+        umma_commit(b_fin);
+        g += it.n;
+      }
+      umma_commit(b_drain);
+      mbar_drain(b_drain, 0);
+    }
+    __syncwarp();
+  } else if (warp < 8) {
+    // ---------------------------------------------------------- elementwise --
+    const int wg = warp >> 2;
+    const int r = (warp & 3) * 32 + lane;
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t tl = tmem + lane_off;
+    const float sl2 = a.sl2;
+    const int w = a.w;
+    int g = 0, ac = 0;
+    bool ok = true;
+    for (int x = blockIdx.x; ok && x < n_items; x += gridDim.x) {
+      const BItem it = dkv_item<LONG>(a, x);
+      if (!it.valid) continue;
+      const bool row_ok = r < it.rows;
+      const int rr = min(r, it.rows - 1);
+      const int pj = LONG ? __ldg(a.perm + (int64_t)it.br * a.NR + it.row0 + rr) : it.row0 + rr;
+      const int64_t grow = ((int64_t)it.b * a.N + pj) * a.H_kv + it.kvh;  // [B, N, H_kv] row
+      if (it.n > 0) {
+        const bf16* src = (wg == 0 ? a.k : a.v) + grow * D;
+        stage_row<D>(tl + (wg == 0 ? L::COL_K : L::COL_V), row_ok ? src : nullptr);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(b_a);
+        ++ac;
+      }
+      for (int t = 0; t < it.n; ++t) {
+        const int gc = g + t, buf = gc & 1, slot = gc % NST;
+        ok = mbar_wait(b_full + 8 * slot, (uint32_t)((gc / NST) & 1), abort_flag, status, tlim) &&
+             mbar_wait(b_sdp + 8 * buf, (uint32_t)((gc >> 1) & 1), abort_flag, status, tlim);
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t st[16], dpt[16];
+        tmem_ld16(tl + L::COL_ST + NQ * buf + 16 * wg, st);
+        tmem_ld16(tl + L::COL_DPT + NQ * buf + 16 * wg, dpt);
+        const float* sc = scal + slot * 3 * NQ + 16 * wg;
+        float ls[16], dd[16];
+        int pq[16];
+#pragma unroll
+        for (int i = 0; i < 16; i += 4) {
+          const float4 l4 = *reinterpret_cast<const float4*>(sc + i);
+          const float4 d4 = *reinterpret_cast<const float4*>(sc + NQ + i);
+          const int4 p4 = *reinterpret_cast<const int4*>(reinterpret_cast<const int*>(sc) + 2 * NQ + i);
+          ls[i] = l4.x; ls[i + 1] = l4.y; ls[i + 2] = l4.z; ls[i + 3] = l4.w;
+          dd[i] = d4.x; dd[i + 1] = d4.y; dd[i + 2] = d4.z; dd[i + 3] = d4.w;
+          pq[i] = p4.x; pq[i + 1] = p4.y; pq[i + 2] = p4.z; pq[i + 3] = p4.w;
+        }
+        tmem_ld_wait(st);
+        tie16(dpt);
+        uint32_t pp[8], pd[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          float p2[2], d2[2];
+#pragma unroll
+          for (int h2 = 0; h2 < 2; ++h2) {
+            const int c = 2 * i + h2;
+            const int dpos = pq[c] - pj;
+            const bool allowed = LONG ? dpos >= w : (uint32_t)dpos < (uint32_t)w;
+            const float pr = ex2(fmaf(__uint_as_float(st[c]), sl2, -ls[c]));
+            const float p = (row_ok && allowed) ? pr : 0.0f;
+            p2[h2] = p;
+            d2[h2] = p * (__uint_as_float(dpt[c]) - dd[c]);
+          }
+          pp[i] = pack_bf16(p2[0], p2[1]);
+          pd[i] = pack_bf16(d2[0], d2[1]);
+        }
+        tmem_st8(tl + L::COL_ST + NQ * buf + 16 * wg, pp);
+        tmem_st8(tl + L::COL_DPT + NQ * buf + 16 * wg, pd);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(b_ds + 8 * buf);
+      }
+      if (!ok) break;
+      // ---- epilogue: dK = scale * (dS^T Q) (warpgroup 0), dV = P^T dO (warpgroup 1) ----
+      if (it.n > 0) {
+        ok = mbar_wait(b_fin, (uint32_t)((ac - 1) & 1), abort_flag, status, tlim);
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+      }
+      g += it.n;
+      const int col_acc = wg == 0 ? L::COL_DK : L::COL_DV;
+      const float mul = wg == 0 ? a.scale : 1.0f;
+      float* part = (wg == 0 ? a.dk_w : a.dv_w) + grow * D;
+      bf16* out = (wg == 0 ? a.dk : a.dv) + grow * D;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t y[32];
+        if (it.n > 0) {
+          tmem_ld32(tl + col_acc + 32 * c, y);
+          tmem_ld_wait(y);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) y[i] = 0u;
+        }
+        if (row_ok) emit32<LONG>(y, mul, part + 32 * c, out + 32 * c);
+      }
+      tc_fence_before();
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == MMA_WARP) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------- preparation kernels --
+// D[b, h, i] = dO[b, i, h, :] . O[b, i, h, :] (fp32 sums of bf16 products); one
+// thread per (b, i, h).
+template <int D>
+__global__ void __launch_bounds__(256)
+bwd_rowdot(int64_t rows, int N, int H, const uint4* __restrict__ o, const uint4* __restrict__ d_o,
+           float* __restrict__ dvec) {
+  const int64_t x = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (x >= rows) return;
+  const uint4* a = o + x * (D / 8);
+  const uint4* b = d_o + x * (D / 8);
+  float acc = 0.0f;
+#pragma unroll 4
+  for (int c = 0; c < D / 8; ++c) {
+    const uint4 va = __ldg(a + c), vb = __ldg(b + c);
+    const uint32_t wa[4] = {va.x, va.y, va.z, va.w}, wb[4] = {vb.x, vb.y, vb.z, vb.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 fa = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wa[i]));
+      const float2 fb = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wb[i]));
+      acc = fmaf(fa.x, fb.x, acc);
+      acc = fmaf(fa.y, fb.y, acc);
+    }
+  }
+  const int h = (int)(x % H);
+  const int64_t bn = x / H;
+  dvec[((bn / N) * H + h) * N + bn % N] = acc;
+}
+
+// Permuted, head-major copy of dO: dOp[b][h][n'][:] = dO[b][perm[n']][h][:] for the
+// heads of routing head rho.  One CTA per permuted row.
+__global__ void __launch_bounds__(256)
+permute_rows(int N, int NR, int H, int R, int d, const int* __restrict__ perm,
+             const uint4* __restrict__ src, uint4* __restrict__ dst) {
+  const int64_t row = blockIdx.x;  // (b * R + rho) * NR + n'
+  const int br = (int)(row / NR), np = (int)(row % NR);
+  const int b = br / R, rho = br % R;
+  const int n = perm[row];
+  const int hq = H / R, vec = d / 8;
+  for (int i = threadIdx.x; i < hq * vec; i += blockDim.x) {
+    const int hh = rho * hq + i / vec, c = i % vec;
+    dst[(((int64_t)b * H + hh) * NR + np) * vec + c] = src[(((int64_t)b * N + n) * H + hh) * vec + c];
+  }
+}
+
+// ------------------------------------------------------------- host side --
+using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                 const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                 const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                 CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiled encode_fn() {
+  static EncodeTiled fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiled>(p);
+  });
+  return fn;
+}
+
+// Tensor map over rows of D bf16 values, box 64 columns x box_rows rows (x 1 head
+// when heads > 0: 3-D d, head, token), 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* base, int D, int64_t rows, int heads, int box_rows) {
+  EncodeTiled fn = encode_fn();
+  if (!fn) return false;
+  const cuuint32_t es[3] = {1, 1, 1};
+  CUresult r;
+  if (heads > 0) {
+    const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)heads, (cuuint64_t)rows};
+    const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)heads * D * 2};
+    const cuuint32_t box[3] = {64, 1, (cuuint32_t)box_rows};
+    r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  } else {
+    const cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)D * 2};
+    const cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+    r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  }
+  return r == CUDA_SUCCESS;
+}
+
+int num_sms() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+    return 148;
+  return n;
+}
+
+template <typename Kernel>
+cudaError_t launch_persistent(Kernel kernel, int smem, const CUtensorMap& m0, const CUtensorMap& m1,
+                              const BwdArgs& a, int n_items, cudaStream_t s) {
+  smem = smem < kMinSmem ? kMinSmem : smem;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  const int sms = num_sms();
+  const int grid = n_items < sms ? n_items : sms;
+  if (grid < 1) return cudaSuccess;
+  kernel<<<grid, NTHREADS, smem, s>>>(m0, m1, a, n_items);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_rowdot(const focus_params& p, const bf16* o, const bf16* d_o, float* dvec,
+                              cudaStream_t s) {
+  const int64_t rows = (int64_t)p.B * p.N * p.H;
+  const unsigned grid = (unsigned)((rows + 255) / 256);
+  if (p.d_head == 64)
+    bwd_rowdot<64><<<grid, 256, 0, s>>>(rows, p.N, p.H, reinterpret_cast<const uint4*>(o),
+                                        reinterpret_cast<const uint4*>(d_o), dvec);
+  else
+    bwd_rowdot<128><<<grid, 256, 0, s>>>(rows, p.N, p.H, reinterpret_cast<const uint4*>(o),
+                                         reinterpret_cast<const uint4*>(d_o), dvec);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_permute_rows(const focus_params& p, const WsLayout& L, const bf16* src, bf16* dst,
+                                const char* ws, cudaStream_t s) {
+  const int64_t rows = (int64_t)p.B * p.R * L.NR;
+  permute_rows<<<(unsigned)rows, 256, 0, s>>>(p.N, L.NR, p.H, p.R, p.d_head,
+                                              reinterpret_cast<const int*>(ws + L.perm),
+                                              reinterpret_cast<const uint4*>(src),
+                                              reinterpret_cast<uint4*>(dst));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_attn_bwd(const focus_params& p, const BwdPlan& bp, const bf16* q, const bf16* k,
+                            const bf16* v, const bf16* d_o, const float* lse, bf16* dq, bf16* dk,
+                            bf16* dv, char* ws, float scale, bool long_pass, cudaStream_t s) {
+  const WsLayout& L = bp.L;
+  BwdArgs a{};
+  a.B = p.B;
+  a.N = p.N;
+  a.H = p.H;
+  a.H_kv = p.H_kv;
+  a.R = p.R;
+  a.w = p.w;
+  a.nseg = L.nseg;
+  a.qtab_cap = L.qtab_cap;
+  a.NR = L.NR;
+  a.sl2 = scale * kLog2e;
+  a.scale = scale;
+  a.perm = reinterpret_cast<const int*>(ws + L.perm);
+  a.qtab = reinterpret_cast<const QBlock*>(ws + L.qtab);
+  a.qtab_count = &reinterpret_cast<const WsHeader*>(ws)->qtab_count;
+  a.qhead = reinterpret_cast<const PlanHead*>(ws + bp.qhead);
+  a.qent = reinterpret_cast<const PlanEnt*>(ws + bp.qent);
+  a.rhead = reinterpret_cast<const PlanHead*>(ws + bp.rhead);
+  a.rent = reinterpret_cast<const PlanEnt*>(ws + bp.rent);
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.dout = d_o;
+  a.lse = lse;
+  a.dvec = reinterpret_cast<const float*>(ws + bp.dvec);
+  a.dq_w = reinterpret_cast<float*>(ws + bp.dqw);
+  a.dk_w = reinterpret_cast<float*>(ws + bp.dkw);
+  a.dv_w = reinterpret_cast<float*>(ws + bp.dvw);
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.status = &reinterpret_cast<WsHeader*>(ws)->status;
+  a.timeout_cycles = kTimeoutCycles;
+  const int D = p.d_head;
+  const int gq = p.H / p.H_kv;
+  CUtensorMap m0, m1, m2, m3;
+  cudaError_t e;
+  if (!long_pass) {
+    // window: token-order maps over K, V (dQ) and Q, dO (dK, dV)
+    if (!make_map(&m0, k, D, (int64_t)p.B * p.N, p.H_kv, NK) ||
+        !make_map(&m1, v, D, (int64_t)p.B * p.N, p.H_kv, NK) ||
+        !make_map(&m2, q, D, (int64_t)p.B * p.N, p.H, NQ) ||
+        !make_map(&m3, d_o, D, (int64_t)p.B * p.N, p.H, NQ))
+      return cudaErrorInvalidValue;
+    const int nb = (p.N + BM - 1) / BM;
+    const int nq_items = p.B * p.H * nb, nk_items = p.B * p.H_kv * nb;
+    if (D == 64) {
+      if ((e = launch_persistent(bwd_dq<64, false>, DqLayout<64>::SMEM, m0, m1, a, nq_items, s))) return e;
+      return launch_persistent(bwd_dkdv<64, false>, DkvLayout<64>::SMEM, m2, m3, a, nk_items, s);
+    }
+    if ((e = launch_persistent(bwd_dq<128, false>, DqLayout<128>::SMEM, m0, m1, a, nq_items, s))) return e;
+    return launch_persistent(bwd_dkdv<128, false>, DkvLayout<128>::SMEM, m2, m3, a, nk_items, s);
+  }
+  // long range: maps over the permuted head-major copies
+  if (!make_map(&m0, ws + L.kp, D, (int64_t)p.B * p.H_kv * L.NR, 0, NK) ||
+      !make_map(&m1, ws + L.vp, D, (int64_t)p.B * p.H_kv * L.NR, 0, NK) ||
+      !make_map(&m2, ws + L.qp, D, (int64_t)p.B * p.H * L.NR, 0, NQ) ||
+      !make_map(&m3, ws + bp.dop, D, (int64_t)p.B * p.H * L.NR, 0, NQ))
+    return cudaErrorInvalidValue;
+  const int nq_items = L.qtab_cap * (p.H / p.R);
+  const int nk_items = L.qtab_cap * (p.H_kv / p.R);
+  (void)gq;
+  if (D == 64) {
+    if ((e = launch_persistent(bwd_dq<64, true>, DqLayout<64>::SMEM, m0, m1, a, nq_items, s))) return e;
+    return launch_persistent(bwd_dkdv<64, true>, DkvLayout<64>::SMEM, m2, m3, a, nk_items, s);
+  }
+  if ((e = launch_persistent(bwd_dq<128, true>, DqLayout<128>::SMEM, m0, m1, a, nq_items, s))) return e;
+  return launch_persistent(bwd_dkdv<128, true>, DkvLayout<128>::SMEM, m2, m3, a, nk_items, s);
+}
+
+}  // namespace focus

@@ -370,6 +370,72 @@ build_plan(int N, int NR, int w, int nseg, int group, const int* __restrict__ se
   if (lane == 0) heads[u] = PlanHead{n_ent, n_tiles, 0, 0};
 }
 
+// Backward plans of 128-row block u (segment S, positions p_lo..p_hi), over the
+// compatible segments T in segment order (exact-set schedule):
+//   query-major (dQ):  keys of T with pos <= p_hi - w, in tiles of kBwdKeyTile;
+//                      PlanEnt.nfull = keys with pos <= p_lo - w (need no mask);
+//   key-major (dK, dV): queries of T with pos >= p_lo + w, in tiles of kBwdQryTile.
+// One warp per block; lanes take segments in parallel.
+__global__ void __launch_bounds__(32)
+build_plan_bwd(int N, int w, int nseg, const int* __restrict__ seg_off, const int* __restrict__ perm,
+               const uint32_t* __restrict__ mask, const QBlock* __restrict__ qtab,
+               const int* __restrict__ qtab_count, PlanHead* __restrict__ qheads,
+               PlanEnt* __restrict__ qents, PlanHead* __restrict__ rheads,
+               PlanEnt* __restrict__ rents) {
+  const int u = blockIdx.x, lane = threadIdx.x;
+  if (u >= *qtab_count) return;
+  const QBlock e = qtab[u];
+  const int* P = perm + (int64_t)e.br * N;
+  const int* SO = seg_off + (int64_t)e.br * (nseg + 1);
+  const uint32_t* M = mask + (int64_t)e.br * N;
+  const int p_lo = __ldg(P + e.row0), p_hi = __ldg(P + e.row0 + e.rows - 1);
+  const uint32_t mS = __ldg(M + p_lo);
+  PlanEnt* qo = qents + (int64_t)u * nseg;
+  PlanEnt* ro = rents + (int64_t)u * nseg;
+  int nq = 0, nr = 0, tq = 0, tr = 0;
+  for (int T0 = 0; T0 < nseg; T0 += 32) {
+    const int T = T0 + lane;
+    PlanEnt qe{0, 0, 0, 0}, re{0, 0, 0, 0};
+    bool qok = false, rok = false;
+    if (T < nseg) {
+      const int s0 = __ldg(SO + T), s1 = __ldg(SO + T + 1);
+      if (s1 > s0 && (__ldg(M + __ldg(P + s0)) & mS)) {
+        const int hi = upper_bound_pos(P, s0, s1, p_hi - w) - s0;
+        if (hi > 0) {
+          qok = true;
+          qe.start = s0;
+          qe.cnt = hi;
+          qe.nfull = upper_bound_pos(P, s0, s1, p_lo - w) - s0;
+        }
+        const int lo = upper_bound_pos(P, s0, s1, p_lo + w - 1);
+        if (lo < s1) {
+          rok = true;
+          re.start = lo;
+          re.cnt = s1 - lo;
+        }
+      }
+    }
+    unsigned bal = __ballot_sync(0xffffffffu, qok);
+    if (qok) qo[nq + __popc(bal & lanemask_lt())] = qe;
+    nq += __popc(bal);
+    bal = __ballot_sync(0xffffffffu, rok);
+    if (rok) ro[nr + __popc(bal & lanemask_lt())] = re;
+    nr += __popc(bal);
+    int a = qok ? (qe.cnt + kBwdKeyTile - 1) / kBwdKeyTile : 0;
+    int c = rok ? (re.cnt + kBwdQryTile - 1) / kBwdQryTile : 0;
+    for (int o = 16; o > 0; o >>= 1) {
+      a += __shfl_xor_sync(0xffffffffu, a, o);
+      c += __shfl_xor_sync(0xffffffffu, c, o);
+    }
+    tq += a;
+    tr += c;
+  }
+  if (lane == 0) {
+    qheads[u] = PlanHead{nq, tq, 0, 0};
+    rheads[u] = PlanHead{nr, tr, 0, 0};
+  }
+}
+
 // Permuted, head-major copies: Qp[b][h][n'][:] = q[b][perm[n']][h][:] for the heads
 // of routing head rho, and likewise K/V for its KV heads; NR permuted rows per
 // (b, rho).  One CTA per permuted row.
@@ -455,6 +521,17 @@ cudaError_t launch_permute(const focus_params& p, const WsLayout& L, const bf16*
       reinterpret_cast<const uint4*>(q), reinterpret_cast<const uint4*>(k),
       reinterpret_cast<const uint4*>(v), reinterpret_cast<uint4*>(ws + L.qp),
       reinterpret_cast<uint4*>(ws + L.kp), reinterpret_cast<uint4*>(ws + L.vp));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_plan_bwd(const focus_params& p, const WsLayout& L, const uint32_t* mask, char* ws,
+                            PlanHead* qheads, PlanEnt* qents, PlanHead* rheads, PlanEnt* rents,
+                            cudaStream_t s) {
+  build_plan_bwd<<<L.qtab_cap, 32, 0, s>>>(p.N, p.w, L.nseg, reinterpret_cast<const int*>(ws + L.segoff),
+                                           reinterpret_cast<const int*>(ws + L.perm), mask,
+                                           reinterpret_cast<const QBlock*>(ws + L.qtab),
+                                           &reinterpret_cast<const WsHeader*>(ws)->qtab_count,
+                                           qheads, qents, rheads, rents);
   return cudaGetLastError();
 }
 

@@ -41,6 +41,9 @@ constexpr int kChunk = 1024;      // tokens per bucketing chunk (one warp)
 constexpr int kSinkBlock = 256;   // tokens per Sinkhorn partial-reduction block
 constexpr int kAttnBM = 256;      // query rows per long-range work item
 constexpr int kKeySentinel = 0x7fffffff;
+constexpr int kBwdBlock = 128;    // backward: query rows (dQ) or key rows (dK, dV) per item
+constexpr int kBwdKeyTile = 64;   // backward dQ: keys per tile
+constexpr int kBwdQryTile = 32;   // backward dK, dV: queries per tile
 
 // Workspace layout.  Segment schedule: nseg = C(K, top_k) segments over NR = N rows
 // per (b, rho).  Group schedule: nseg = K lists over NR = N * top_k rows, plus the
@@ -53,6 +56,14 @@ struct WsLayout {
   int nseg, nchunk, nblk_sk, qtab_cap;
   int group;  // 1: group-list schedule
   int NR;     // permuted rows per (b, rho)
+};
+
+// Backward workspace: the exact-set bucketing and the 128-row block schedule (in
+// L), the backward plans (query-major and key-major), the permuted dO, D = dO . O
+// and the window pass's fp32 partial gradients.
+struct BwdPlan {
+  WsLayout L;
+  size_t qhead, qent, rhead, rent, dop, dvec, dqw, dkw, dvw;
 };
 
 // Binomial coefficient C(n, r) for n <= 32 (fits uint32 for all r).
@@ -82,9 +93,20 @@ cudaError_t launch_plan(const focus_params& p, const WsLayout& L, const uint32_t
                         int block_rows, cudaStream_t s);
 cudaError_t launch_permute(const focus_params& p, const WsLayout& L, const bf16* q, const bf16* k,
                            const bf16* v, char* ws, cudaStream_t s);
+cudaError_t launch_plan_bwd(const focus_params& p, const WsLayout& L, const uint32_t* mask, char* ws,
+                            PlanHead* qheads, PlanEnt* qents, PlanHead* rheads, PlanEnt* rents,
+                            cudaStream_t s);
 // merge.cu (group schedule)
 cudaError_t launch_merge_slots(const focus_params& p, const WsLayout& L, const char* ws, bf16* o,
                                float* lse, cudaStream_t s);
+// attn_bwd.cu (backward)
+cudaError_t launch_bwd_rowdot(const focus_params& p, const bf16* o, const bf16* d_o, float* dvec,
+                              cudaStream_t s);
+cudaError_t launch_permute_rows(const focus_params& p, const WsLayout& L, const bf16* src, bf16* dst,
+                                const char* ws, cudaStream_t s);
+cudaError_t launch_attn_bwd(const focus_params& p, const BwdPlan& bp, const bf16* q, const bf16* k,
+                            const bf16* v, const bf16* d_o, const float* lse, bf16* dq, bf16* dk,
+                            bf16* dv, char* ws, float scale, bool long_pass, cudaStream_t s);
 // decode.cu
 int decode_chunks(int N);
 size_t decode_workspace_bytes(const focus_params& p);

@@ -91,6 +91,58 @@ WsLayout layout(const focus_params& p) {
   return L;
 }
 
+// Backward: exact-set segments over 128-row blocks (the gradients do not depend on
+// the schedule; the group-list form is not built for the backward).
+int check_bwd_params(const focus_params* p) {
+  const int rc = check_params(p);
+  if (rc) return rc;
+  if (binom(p->K, p->top_k) > (uint32_t)FOCUS_MAX_SEGMENTS) return FOCUS_ERR_UNSUPPORTED;
+  const int64_t rows = (int64_t)p->B * (p->H > p->R ? p->H : p->R) * p->N;
+  if (rows >= (int64_t)INT32_MAX) return FOCUS_ERR_UNSUPPORTED;
+  return FOCUS_OK;
+}
+
+BwdPlan bwd_layout(const focus_params& p) {
+  BwdPlan bp{};
+  WsLayout& L = bp.L;
+  const int BR = p.B * p.R;
+  L.group = 0;
+  L.nseg = (int)binom(p.K, p.top_k);
+  L.NR = p.N;
+  L.nchunk = (p.N + kChunk - 1) / kChunk;
+  L.nblk_sk = (p.N + 255) / 256;
+  L.qtab_cap = BR * ((p.N + kBwdBlock - 1) / kBwdBlock + L.nseg);
+  const size_t A = 256;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off = align_up(off + bytes, A);
+    return at;
+  };
+  const size_t BHN = (size_t)p.B * p.H * p.N, BKN = (size_t)p.B * p.H_kv * p.N;
+  L.hdr = take(sizeof(WsHeader));
+  L.hist = take(sizeof(int) * (size_t)BR * L.nchunk * L.nseg);
+  L.segoff = take(sizeof(int) * (size_t)BR * (L.nseg + 1));
+  L.cbase = take(sizeof(int) * (size_t)BR * L.nchunk * L.nseg);
+  L.perm = take(sizeof(int) * (size_t)BR * L.NR);
+  L.entoff = take(sizeof(int) * ((size_t)BR * L.nseg + 1));
+  L.qtab = take(sizeof(QBlock) * (size_t)L.qtab_cap);
+  L.qp = take(sizeof(uint16_t) * BHN * p.d_head);
+  L.kp = take(sizeof(uint16_t) * BKN * p.d_head);
+  L.vp = take(sizeof(uint16_t) * BKN * p.d_head);
+  bp.qhead = take(sizeof(PlanHead) * (size_t)L.qtab_cap);
+  bp.qent = take(sizeof(PlanEnt) * (size_t)L.qtab_cap * L.nseg);
+  bp.rhead = take(sizeof(PlanHead) * (size_t)L.qtab_cap);
+  bp.rent = take(sizeof(PlanEnt) * (size_t)L.qtab_cap * L.nseg);
+  bp.dop = take(sizeof(uint16_t) * BHN * p.d_head);
+  bp.dvec = take(sizeof(float) * BHN);
+  bp.dqw = take(sizeof(float) * BHN * p.d_head);
+  bp.dkw = take(sizeof(float) * BKN * p.d_head);
+  bp.dvw = take(sizeof(float) * BKN * p.d_head);
+  L.total = off;
+  return bp;
+}
+
 int check_ws(const WsLayout& L, const void* ws, size_t ws_bytes) {
   if (!ws) return FOCUS_ERR_INVALID_ARG;
   if (!aligned(ws, 256)) return FOCUS_ERR_ALIGNMENT;
@@ -369,6 +421,55 @@ int focus_attn_fwd_host(const focus_params* p, const uint16_t* q_h, const uint16
     if ((rc = cuda_rc(copy_out(g)))) return cleanup(rc);
   }
   return cleanup(FOCUS_OK);
+}
+
+size_t focus_bwd_workspace_size(const focus_params* p) {
+  if (check_bwd_params(p) != FOCUS_OK) return 0;
+  return bwd_layout(*p).L.total;
+}
+
+int focus_attn_bwd(const focus_params* p, const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                   const uint32_t* mask, const uint16_t* o, const float* lse, const uint16_t* d_o,
+                   uint16_t* dq, uint16_t* dk, uint16_t* dv, void* ws, size_t ws_bytes,
+                   void* stream) {
+  int rc = check_bwd_params(p);
+  if (rc) return rc;
+  if (!q || !k || !v || !mask || !o || !lse || !d_o || !dq || !dk || !dv)
+    return FOCUS_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
+      !aligned(d_o, 16) || !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) ||
+      !aligned(mask, 4) || !aligned(lse, 4))
+    return FOCUS_ERR_ALIGNMENT;
+  const BwdPlan bp = bwd_layout(*p);
+  const WsLayout& L = bp.L;
+  if ((rc = check_ws(L, ws, ws_bytes))) return rc;
+  cudaStream_t s = (cudaStream_t)stream;
+  char* w = (char*)ws;
+  const float scale = p->softmax_scale > 0.0f ? p->softmax_scale : 1.0f / sqrtf((float)p->d_head);
+  const bf16* qb = reinterpret_cast<const bf16*>(q);
+  const bf16* kb = reinterpret_cast<const bf16*>(k);
+  const bf16* vb = reinterpret_cast<const bf16*>(v);
+  const bf16* gb = reinterpret_cast<const bf16*>(d_o);
+  if ((rc = cuda_rc(reset_header(w, s)))) return rc;
+  if ((rc = cuda_rc(launch_bucket(*p, L, mask, w, s)))) return rc;
+  if ((rc = cuda_rc(launch_qtab(*p, L, w, kBwdBlock, s)))) return rc;
+  if ((rc = cuda_rc(launch_plan_bwd(*p, L, mask, w, reinterpret_cast<PlanHead*>(w + bp.qhead),
+                                    reinterpret_cast<PlanEnt*>(w + bp.qent),
+                                    reinterpret_cast<PlanHead*>(w + bp.rhead),
+                                    reinterpret_cast<PlanEnt*>(w + bp.rent), s))))
+    return rc;
+  if ((rc = cuda_rc(launch_permute(*p, L, qb, kb, vb, w, s)))) return rc;
+  if ((rc = cuda_rc(launch_permute_rows(*p, L, gb, reinterpret_cast<bf16*>(w + bp.dop), w, s))))
+    return rc;
+  if ((rc = cuda_rc(launch_bwd_rowdot(*p, reinterpret_cast<const bf16*>(o), gb,
+                                      reinterpret_cast<float*>(w + bp.dvec), s))))
+    return rc;
+  bf16* dqb = reinterpret_cast<bf16*>(dq);
+  bf16* dkb = reinterpret_cast<bf16*>(dk);
+  bf16* dvb = reinterpret_cast<bf16*>(dv);
+  if ((rc = cuda_rc(launch_attn_bwd(*p, bp, qb, kb, vb, gb, lse, dqb, dkb, dvb, w, scale, false, s))))
+    return rc;
+  return cuda_rc(launch_attn_bwd(*p, bp, qb, kb, vb, gb, lse, dqb, dkb, dvb, w, scale, true, s));
 }
 
 size_t focus_decode_workspace_size(const focus_params* p) {

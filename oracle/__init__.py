@@ -58,8 +58,8 @@ def _load():
         lib.oracle_attn.argtypes = [i32, i32, i32, i32, i32, i32, i32, f64, P, P, P, P, P, i64, P, i32,
                                     P, P, i32]
         lib.oracle_attn.restype = i32
-        lib.oracle_attn_bwd.argtypes = [i32, i32, i32, i32, i32, i32, i32, f64, P, P, P, P, P, P, i64,
-                                        P, i64, P, i32, P, P, P, i32]
+        lib.oracle_attn_bwd.argtypes = [i32, i32, i32, i32, i32, i32, i32, f64, P, P, P, P, P, P, P,
+                                        i64, P, i64, P, i32, P, P, P, P, P, P, f64, i32]
         lib.oracle_attn_bwd.restype = i32
         _lib = lib
     return _lib
@@ -147,20 +147,31 @@ def attn(q, k, v, mask, *, w: int, scale: float | None = None, rows=None, heads=
 
 
 def attn_bwd(q, k, v, mask, dout, *, w: int, scale: float | None = None, rows=None, keys=None,
-             heads=None, n_threads: int | None = None):
+             heads=None, o_for_D=None, magnitudes: bool = False, d_rel: float = 0.0,
+             n_threads: int | None = None):
     """Gradients of ``attn`` with the mask held fixed, for upstream gradient dout
     [B, N, H, d] (bf16 tensor or uint16 bits).
 
     rows: flattened query rows (b * N + i) whose dq is wanted (default all);
     keys: flattened key rows (b * N + j) whose dk, dv are wanted (default all);
     heads: query heads differentiated (default all); dk, dv sum over them.
+    o_for_D: optional bf16 forward output [B, N, H, d]; D_i = dO_i . o_i is then taken
+    from it (as an implementation that receives o in bf16 does) instead of the exact
+    sum_j P_ij dP_ij.
+    magnitudes: also return (mq, mk, mv), first-order error scales: the sums of the
+    absolute values of the gradient's terms, where each dS_ij (and P_ij for dv) is
+    widened by d_rel times the absolute sums that form its logit, dP_ij and D_i (see
+    oracle_attn_bwd in focus_oracle.c); a relative error u in those steps moves a
+    gradient by about u times its scale.
     Returns (dq [n_rows, n_heads, d], dk [n_keys, H_kv, d], dv [n_keys, H_kv, d]), f64."""
     q16, k16, v16, g16 = (_np(t, np.uint16) for t in (q, k, v, dout))
+    o16 = None if o_for_D is None else _np(o_for_D, np.uint16)
     mask = _np(mask, np.uint32)
     B, N, H, d = q16.shape
     H_kv = k16.shape[2]
     R = mask.shape[1]
     assert g16.shape == q16.shape and k16.shape == (B, N, H_kv, d) and v16.shape == k16.shape
+    assert o16 is None or o16.shape == q16.shape
     if scale is None:
         scale = 1.0 / np.sqrt(d)
     rows_a = None if rows is None else _np(rows, np.int64)
@@ -172,10 +183,15 @@ def attn_bwd(q, k, v, mask, dout, *, w: int, scale: float | None = None, rows=No
     dq = np.zeros((n_rows, n_heads, d), np.float64)
     dk = np.zeros((n_keys, H_kv, d), np.float64)
     dv = np.zeros((n_keys, H_kv, d), np.float64)
+    mq = np.zeros_like(dq) if magnitudes else None
+    mk = np.zeros_like(dk) if magnitudes else None
+    mv = np.zeros_like(dv) if magnitudes else None
     rc = _load().oracle_attn_bwd(B, N, H, H_kv, R, d, w, float(scale), _ptr(q16), _ptr(k16), _ptr(v16),
-                                 _ptr(mask), _ptr(g16), _ptr(rows_a), n_rows, _ptr(keys_a), n_keys,
-                                 _ptr(heads_a), n_heads, _ptr(dq), _ptr(dk), _ptr(dv),
-                                 n_threads or n_cores())
+                                 _ptr(mask), _ptr(g16), _ptr(o16), _ptr(rows_a), n_rows, _ptr(keys_a), n_keys,
+                                 _ptr(heads_a), n_heads, _ptr(dq), _ptr(dk), _ptr(dv), _ptr(mq),
+                                 _ptr(mk), _ptr(mv), float(d_rel), n_threads or n_cores())
     if rc != 0:
         raise ValueError("oracle_attn_bwd: bad arguments")
+    if magnitudes:
+        return dq, dk, dv, mq, mk, mv
     return dq, dk, dv

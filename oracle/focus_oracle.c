@@ -317,6 +317,7 @@ typedef struct {
   int B, N, H, H_kv, R, d, w;
   double scale;
   const uint16_t *q, *k, *v, *dout;
+  const uint16_t* o_for_D; /* [B, N, H, d] bf16 or NULL: D_i = dO_i . o_i instead of sum P dP */
   const uint32_t* mask;
   const int64_t* row_slot; /* [B*N]: output slot of a query row, -1 if not wanted */
   const int64_t* key_slot; /* [B*N]: output slot of a key row, -1 if not wanted */
@@ -324,6 +325,8 @@ typedef struct {
   const int32_t* heads;
   int n_heads;
   double *dq, *dk, *dv;
+  double *mq, *mk, *mv; /* nullable: magnitudes of the terms (error scales) */
+  double d_rel;         /* weight of D's own error in mq, mk (see oracle_attn_bwd) */
   int64_t next, total;
   pthread_mutex_t mu;
 } bwd_job;
@@ -333,12 +336,18 @@ static void* bwd_worker(void* arg) {
   const int d = J->d;
   double* s_buf = (double*)malloc(sizeof(double) * (size_t)J->N);
   double* dp_buf = (double*)malloc(sizeof(double) * (size_t)J->N);
+  double* sa_buf = (double*)malloc(sizeof(double) * (size_t)J->N); /* scale sum_t |q_t k_t| */
+  double* pa_buf = (double*)malloc(sizeof(double) * (size_t)J->N); /* sum_t |dO_t v_t| */
   int64_t* j_buf = (int64_t*)malloc(sizeof(int64_t) * (size_t)J->N);
   double* qv = (double*)malloc(sizeof(double) * (size_t)d);
   double* gv = (double*)malloc(sizeof(double) * (size_t)d);
   const size_t acc_n = (size_t)J->n_keys * J->H_kv * d;
   double* dk_acc = (double*)calloc(acc_n ? acc_n : 1, sizeof(double));
   double* dv_acc = (double*)calloc(acc_n ? acc_n : 1, sizeof(double));
+  const size_t macc_n = J->mk ? acc_n : 0;
+  double* mk_acc = (double*)calloc(macc_n ? macc_n : 1, sizeof(double));
+  double* mv_acc = (double*)calloc(macc_n ? macc_n : 1, sizeof(double));
+
   const int64_t chunk = 8;
   for (;;) {
     pthread_mutex_lock(&J->mu);
@@ -371,13 +380,18 @@ static void* bwd_worker(void* arg) {
         const int64_t bj = (int64_t)b * J->N + j;
         const uint16_t* kj = J->k + (bj * J->H_kv + kvh) * d;
         const uint16_t* vj = J->v + (bj * J->H_kv + kvh) * d;
-        double s = 0.0, dp = 0.0;
+        double s = 0.0, dp = 0.0, sa = 0.0, pa = 0.0;
         for (int t = 0; t < d; ++t) {
-          s += qv[t] * bf16_to_double(kj[t]);
-          dp += gv[t] * bf16_to_double(vj[t]);
+          const double kt = bf16_to_double(kj[t]), vt = bf16_to_double(vj[t]);
+          s += qv[t] * kt;
+          dp += gv[t] * vt;
+          sa += fabs(qv[t] * kt);
+          pa += fabs(gv[t] * vt);
         }
         s_buf[n] = s * J->scale;
         dp_buf[n] = dp;
+        sa_buf[n] = sa * J->scale;
+        pa_buf[n] = pa;
         j_buf[n] = j;
         if (s_buf[n] > mx) mx = s_buf[n];
         ++n;
@@ -386,17 +400,31 @@ static void* bwd_worker(void* arg) {
       for (int64_t a = 0; a < n; ++a) sum += exp(s_buf[a] - mx);
       const double lse = mx + log(sum);
       double D = 0.0;
-      for (int64_t a = 0; a < n; ++a) D += exp(s_buf[a] - lse) * dp_buf[a];
+      if (J->o_for_D) {
+        const uint16_t* oi = J->o_for_D + (bi * J->H + h) * d;
+        for (int t = 0; t < d; ++t) D += gv[t] * bf16_to_double(oi[t]);
+      } else {
+        for (int64_t a = 0; a < n; ++a) D += exp(s_buf[a] - lse) * dp_buf[a];
+      }
+      /* e_i = sum_j P_ij sum_t |dO_it v_jt|: scale of D's error when each O_it carries
+         an error relative to the magnitude of its terms, sum_j P_ij |v_jt| */
+      double e = 0.0;
+      for (int64_t a = 0; a < n; ++a) e += exp(s_buf[a] - lse) * pa_buf[a];
       /* scatter into the wanted outputs */
       const int64_t rs = J->row_slot[bi];
       double* dq = rs >= 0 ? J->dq + (rs * J->n_heads + hs) * d : NULL;
+      double* mq = (rs >= 0 && J->mq) ? J->mq + (rs * J->n_heads + hs) * d : NULL;
       for (int64_t a = 0; a < n; ++a) {
         const double p = exp(s_buf[a] - lse);
         const double ds = p * (dp_buf[a] - D);
+        /* first-order error scale of dS: its rounding, the logit's and dP's sums, D */
+        const double ads = fabs(ds) * (1.0 + J->d_rel * sa_buf[a]) + J->d_rel * p * (pa_buf[a] + e);
         const int64_t bj = (int64_t)b * J->N + j_buf[a];
         if (dq) {
           const uint16_t* kj = J->k + (bj * J->H_kv + kvh) * d;
           for (int t = 0; t < d; ++t) dq[t] += J->scale * ds * bf16_to_double(kj[t]);
+          if (mq)
+            for (int t = 0; t < d; ++t) mq[t] += J->scale * ads * fabs(bf16_to_double(kj[t]));
         }
         const int64_t ks = J->key_slot[bj];
         if (ks >= 0) {
@@ -405,6 +433,14 @@ static void* bwd_worker(void* arg) {
           for (int t = 0; t < d; ++t) {
             dk[t] += J->scale * ds * qv[t];
             dv[t] += p * gv[t];
+          }
+          if (macc_n) {
+            double* mk = mk_acc + (ks * J->H_kv + kvh) * d;
+            double* mv = mv_acc + (ks * J->H_kv + kvh) * d;
+            for (int t = 0; t < d; ++t) {
+              mk[t] += J->scale * ads * fabs(qv[t]);
+              mv[t] += p * (1.0 + J->d_rel * sa_buf[a]) * fabs(gv[t]);
+            }
           }
         }
       }
@@ -415,8 +451,13 @@ static void* bwd_worker(void* arg) {
     J->dk[x] += dk_acc[x];
     J->dv[x] += dv_acc[x];
   }
+  for (size_t x = 0; x < macc_n; ++x) {
+    J->mk[x] += mk_acc[x];
+    J->mv[x] += mv_acc[x];
+  }
   pthread_mutex_unlock(&J->mu);
-  free(s_buf); free(dp_buf); free(j_buf); free(qv); free(gv); free(dk_acc); free(dv_acc);
+  free(s_buf); free(dp_buf); free(sa_buf); free(pa_buf); free(j_buf); free(qv); free(gv); free(dk_acc); free(dv_acc);
+  free(mk_acc); free(mv_acc);
   return NULL;
 }
 
@@ -429,14 +470,27 @@ static void* bwd_worker(void* arg) {
  *   heads (nullable) query heads whose paths are differentiated (NULL = all H)
  *   dq [n_rows, n_heads, d] double out
  *   dk, dv [n_keys, H_kv, d] double out: sums over the selected query heads
+ *   o_for_D (nullable) [B, N, H, d] bf16: when given, D_i = dO_i . o_i with this
+ *           (rounded) forward output, the form an implementation that receives the
+ *           forward output in bf16 uses; when NULL, D_i = sum_j P_ij dP_ij exactly
+ *   mq [n_rows, n_heads, d], mk, mv [n_keys, H_kv, d] (nullable, all or none):
+ *           first-order error scales: with a_ij = scale sum_t |q_it k_jt| (the logit's
+ *           terms), b_ij = sum_t |dO_it v_jt| (dP's terms), e_i = sum_j P_ij b_ij (D's
+ *           terms, with O's) and m_ij = |dS_ij| (1 + d_rel a_ij) + d_rel P_ij (b_ij + e_i),
+ *           mq_i = scale sum_j m_ij |k_j|,  mk_j = scale sum_i m_ij |q_i|,
+ *           mv_j = sum_i P_ij (1 + d_rel a_ij) |dO_i|: a relative error u on dS (or P)
+ *           and u d_rel on the sums that form s, dP and D moves a gradient by at most
+ *           about u times its scale
  * Every query row of the selected heads is visited (each one feeds the keys).
  * Returns 0, or -1 on bad arguments.
  */
 int oracle_attn_bwd(int B, int N, int H, int H_kv, int R, int d, int w, double scale,
                     const uint16_t* q, const uint16_t* k, const uint16_t* v,
-                    const uint32_t* mask, const uint16_t* dout, const int64_t* rows,
+                    const uint32_t* mask, const uint16_t* dout, const uint16_t* o_for_D,
+                    const int64_t* rows,
                     int64_t n_rows, const int64_t* keys, int64_t n_keys, const int32_t* heads,
-                    int n_heads, double* dq, double* dk, double* dv, int n_threads) {
+                    int n_heads, double* dq, double* dk, double* dv, double* mq, double* mk,
+                    double* mv, double d_rel, int n_threads) {
   if (B < 1 || N < 1 || H < 1 || H_kv < 1 || R < 1 || d < 1 || w < 1 || H % H_kv ||
       H_kv % R || n_rows < 0 || n_keys < 0)
     return -1;
@@ -467,8 +521,11 @@ int oracle_attn_bwd(int B, int N, int H, int H_kv, int R, int d, int w, double s
   }
   for (int64_t x = 0; x < n_rows * n_heads * d; ++x) dq[x] = 0.0;
   for (int64_t x = 0; x < n_keys * H_kv * d; ++x) dk[x] = dv[x] = 0.0;
-  bwd_job J = {B, N, H, H_kv, R, d, w, scale, q, k, v, dout, mask, row_slot, key_slot, n_keys,
-               heads, n_heads, dq, dk, dv, 0, (int64_t)n_heads * BN};
+  if (!mq || !mk || !mv) mq = mk = mv = NULL;
+  for (int64_t x = 0; mq && x < n_rows * n_heads * d; ++x) mq[x] = 0.0;
+  for (int64_t x = 0; mk && x < n_keys * H_kv * d; ++x) mk[x] = mv[x] = 0.0;
+  bwd_job J = {B, N, H, H_kv, R, d, w, scale, q, k, v, dout, o_for_D, mask, row_slot, key_slot, n_keys,
+               heads, n_heads, dq, dk, dv, mq, mk, mv, d_rel, 0, (int64_t)n_heads * BN};
   pthread_mutex_init(&J.mu, NULL);
   if (n_threads < 1) n_threads = 1;
   if (n_threads > 256) n_threads = 256;

@@ -133,3 +133,26 @@ def test_host_entry_sizes_and_argument_errors():
     assert rc == E["FOCUS_ERR_INVALID_ARG"]               # routing inputs are required
     rc = focus._lib.focus_attn_fwd_host(ctypes.byref(p.c()), h, h, h, h, h, h, None, 0, P(1 << 12), n - 1, None, same)
     assert rc == E["FOCUS_ERR_WORKSPACE"]
+
+
+def test_backward_sizes_and_argument_errors():
+    p = _params()
+    n = focus.bwd_workspace_size(p)
+    # permuted Q, K, V, dO (bf16) + fp32 window partials of dq, dk, dv + D
+    assert n >= (4 * 2 + 3 * 4) * p.N * p.H * p.d_head + 4 * p.N * p.H
+    assert focus.bwd_workspace_size(_params(K=32, top_k=4)) == 0      # 35960 sets: no segments
+    assert focus.bwd_workspace_size(_params(d_head=96)) == 0
+    E = {v: k for k, v in focus.ERRORS.items()}
+    P = ctypes.c_void_p
+    h = P(1 << 12)
+    args = [h] * 10
+    bad = list(args)
+    bad[3] = None                                                      # no mask
+    assert focus._lib.focus_attn_bwd(ctypes.byref(p.c()), *bad, h, n, None) == E["FOCUS_ERR_INVALID_ARG"]
+    bad = list(args)
+    bad[5] = None                                                      # no lse
+    assert focus._lib.focus_attn_bwd(ctypes.byref(p.c()), *bad, h, n, None) == E["FOCUS_ERR_INVALID_ARG"]
+    bad = list(args)
+    bad[0] = P((1 << 12) + 8)                                          # misaligned q
+    assert focus._lib.focus_attn_bwd(ctypes.byref(p.c()), *bad, h, n, None) == E["FOCUS_ERR_ALIGNMENT"]
+    assert focus._lib.focus_attn_bwd(ctypes.byref(p.c()), *args, h, n - 1, None) == E["FOCUS_ERR_WORKSPACE"]

@@ -445,3 +445,46 @@ def test_gradient_subsets_equal_full_computation():
     np.testing.assert_allclose(dk_s[:, 1], dk[keys.numpy(), 1], atol=1e-12, rtol=0)
     np.testing.assert_allclose(dv_s[:, 1], dv[keys.numpy(), 1], atol=1e-12, rtol=0)
     assert np.all(dk_s[:, 0] == 0) and np.all(dv_s[:, 0] == 0)
+
+
+def test_gradients_with_given_forward_output_shift_as_the_d_term_predicts():
+    """dq_i = scale sum_j P_ij (dP_ij - D_i) k_j is affine in D_i: taking D'_i = dO_i . R_i
+    from a given array R moves dq_i by -scale (D'_i - D_i) (P k)_i, where (P k)_i is the
+    forward with v := k, and leaves dv unchanged.  R varies per row and head, so a
+    wrong index into it shows."""
+    B, N, H, H_kv, d, K, top_k, w = 2, 60, 4, 2, 16, 4, 2, 7
+    q, k, v = _bf16((B, N, H, d), 71), _bf16((B, N, H_kv, d), 72), _bf16((B, N, H_kv, d), 73)
+    dout = _bf16((B, N, H, d), 74)
+    R = _bf16((B, N, H, d), 75)
+    r, C = _routing(B, N, 1, K, seed=76)
+    mask, _, _, _ = oracle.route(r, C, K=K, top_k=top_k)
+    dq0, dk0, dv0 = oracle.attn_bwd(q, k, v, mask, dout, w=w)
+    dq1, _, dv1 = oracle.attn_bwd(q, k, v, mask, dout, w=w, o_for_D=R)
+    o, _ = oracle.attn(q, k, v, mask, w=w)
+    pk, _ = oracle.attn(q, k, k, mask, w=w)
+    g = _f64(dout).reshape(B * N, H, d)
+    D = (g * o).sum(axis=2)
+    D1 = (g * _f64(R).reshape(B * N, H, d)).sum(axis=2)
+    scale = 1.0 / math.sqrt(d)
+    np.testing.assert_allclose(dq1 - dq0, -scale * (D1 - D)[:, :, None] * pk, atol=1e-11, rtol=0)
+    np.testing.assert_allclose(dv1, dv0, atol=1e-13, rtol=0)
+
+
+def test_gradient_magnitudes_bound_the_gradients_and_reduce_without_d_term():
+    """mq, mk, mv sum the absolute values of the terms of dq, dk, dv, so they bound
+    them; with d_rel = 0 and a single allowed key per row (w = 1, one group per
+    token in its own group) dS = 0 and mq = mk = 0, mv_j = |dO_j|."""
+    B, N, H, H_kv, d, K, top_k, w = 1, 70, 2, 1, 16, 4, 2, 6
+    q, k, v = _bf16((B, N, H, d), 81), _bf16((B, N, H_kv, d), 82), _bf16((B, N, H_kv, d), 83)
+    dout = _bf16((B, N, H, d), 84)
+    r, C = _routing(B, N, 1, K, seed=85)
+    mask, _, _, _ = oracle.route(r, C, K=K, top_k=top_k)
+    dq, dk, dv, mq, mk, mv = oracle.attn_bwd(q, k, v, mask, dout, w=w, magnitudes=True, d_rel=1.0)
+    assert np.all(np.abs(dq) <= mq + 1e-12) and np.all(np.abs(dk) <= mk + 1e-12)
+    assert np.all(np.abs(dv) <= mv + 1e-12)
+    n = 30
+    lone = (1 << np.arange(n)).astype(np.uint32)[None, None, :]   # every token its own group
+    q, k, v, dout = q[:, :n].contiguous(), k[:, :n].contiguous(), v[:, :n].contiguous(), dout[:, :n].contiguous()
+    dq, dk, dv, mq, mk, mv = oracle.attn_bwd(q, k, v, lone, dout, w=1, magnitudes=True)
+    assert np.all(mq == 0) and np.all(mk == 0)
+    np.testing.assert_allclose(mv[:, 0], np.abs(_f64(dout)[0]).sum(axis=1), atol=1e-14, rtol=0)
