@@ -12,21 +12,23 @@
 //
 // Two persistent kernels, each in a window pass (token order, keys (i - w, i])
 // and a long-range pass (compatible exact-set segments, permuted copies); no
-// atomics, so the result is deterministic:
+// atomics, so the result is deterministic.  Every tensor-core product has N = 128
+// (narrower products ran at a fraction of the rate), so each kernel keeps one
+// 128 x 128 tile of S and dP in TMEM at a time:
 //   bwd_dq<D, LONG>    query-major: 128 query rows of one head per item.  Their Q
-//                      and dO rows are staged in TMEM as the A operands; for each
-//                      64-key tile: S = Q K^T and dP = dO V^T into one of two TMEM
-//                      buffers, dS (bf16) written over S by the elementwise warps,
-//                      dQ += dS K.  The tensor core computes tile t+1 while the
-//                      warps work on tile t.
-//   bwd_dkdv<D, LONG>  key-major: 128 key rows of one KV head per item, every
-//                      query head of its group.  K and V rows staged in TMEM; for
-//                      each 32-query tile: S^T = K Q^T, dP^T = V dO^T, P^T and dS^T
+//                      and dO rows are staged in TMEM as the A operands; per
+//                      128-key tile: S = Q K^T and dP = dO V^T, dS (bf16) written
+//                      over S by the elementwise warps, dQ += dS K; the tensor
+//                      core runs dQ(t), S(t+1), dP(t+1) back to back.
+//   bwd_dkdv<D, LONG>  key-major: 128 key rows of one KV head per item (K and V
+//                      resident in shared memory), every query head of its group;
+//                      per 128-query tile: S^T = K Q^T, dP^T = V dO^T, P^T and dS^T
 //                      (bf16) written over them, dV += P^T dO, dK += dS^T Q.
+// TMEM (512 columns): dQ kernel Q | dO | S | dP | dQ, dK/dV kernel S^T | dP^T | dK | dV.
 // The window pass writes fp32 partials; the long-range pass adds them and writes
 // the bf16 gradients (the two key sets are disjoint, so the sums are the totals).
 //
-// Warps: 0-7 elementwise (two warpgroups, each a column half of every tile, lane =
+// Warps: 0-7 elementwise (two warpgroups, each 64 columns of every tile, lane =
 // TMEM row), 8 producer (TMA; in bwd_dkdv the whole warp also stages the tile's
 // per-query LSE, D and position), 9 MMA issuer, 10-11 idle.
 #include <math.h>
@@ -51,40 +53,43 @@ constexpr uint32_t TMEM_COLS = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kMinSmem = 116 * 1024;  // > half the SM's shared memory: one CTA per SM
 
-// Barrier block shared by both kernels: full[NST], empty[NST], sdp[2], ds[2], a,
-// fin, drain (8 bytes each), the TMEM address word and the abort flag.
+// Barrier block shared by both kernels: full[NST], empty[NST], then sdp, ds, a,
+// fin, drain, kv_full, kv_empty (8 bytes each), the TMEM address word and the
+// abort flag.
 template <int NST>
 struct Bars {
-  static constexpr int FULL = 0, EMPTY = 8 * NST, SDP = 16 * NST, DS = SDP + 16, A = DS + 16;
-  static constexpr int FIN = A + 8, DRAIN = FIN + 8, TMEM_SLOT = DRAIN + 8, ABORT = TMEM_SLOT + 4;
+  static constexpr int FULL = 0, EMPTY = 8 * NST, SDP = 16 * NST, DS = SDP + 8, A = DS + 8;
+  static constexpr int FIN = A + 8, DRAIN = FIN + 8, KVF = DRAIN + 8, KVE = KVF + 8;
+  static constexpr int TMEM_SLOT = KVE + 8, ABORT = TMEM_SLOT + 4;
   static constexpr int BYTES = 256;
   static_assert(ABORT + 4 <= BYTES, "barrier block overflow");
 };
 
+constexpr int BOX = 128 * 128;  // one TMA box: 128 rows x 128 bytes (64 bf16)
+
 template <int D>
 struct DqLayout {
-  static constexpr int NST = 4;
-  static constexpr int BOX = NK * 128;           // 64 rows x 128 bytes
-  static constexpr int TILE = (D / 64) * BOX;    // one 64-key tile of K or V
+  static constexpr int NST = 3;
+  static constexpr int TILE = (D / 64) * BOX;    // one 128-key tile of K or V
   static constexpr int RING = 0;                 // [NST][K tile, V tile]
   static constexpr int BAR = RING + NST * 2 * TILE;
   static constexpr int SMEM = BAR + Bars<NST>::BYTES + 1024;
-  // TMEM columns
-  static constexpr int COL_Q = 0, COL_DO = D / 2, COL_S = D, COL_DP = D + 2 * NK, COL_DQ = D + 4 * NK;
+  static_assert(SMEM <= 232448, "shared memory budget");
+  static constexpr int COL_Q = 0, COL_DO = D / 2, COL_S = D, COL_DP = D + NK, COL_DQ = D + 2 * NK;
   static_assert(COL_DQ + D <= (int)TMEM_COLS, "tensor memory budget");
 };
 
 template <int D>
 struct DkvLayout {
-  static constexpr int NST = 8;
-  static constexpr int BOX = NQ * 128;           // 32 rows x 128 bytes
-  static constexpr int TILE = (D / 64) * BOX;    // one 32-query tile of Q or dO
-  static constexpr int RING = 0;                 // [NST][Q tile, dO tile]
-  static constexpr int SCAL = RING + NST * 2 * TILE;  // [NST][lse2, D, pos][32]
+  static constexpr int NST = 2;
+  static constexpr int TILE = (D / 64) * BOX;    // one 128-row tile of K, V, Q or dO
+  static constexpr int KV = 0;                   // K tile, V tile of the item
+  static constexpr int RING = KV + 2 * TILE;     // [NST][Q tile, dO tile]
+  static constexpr int SCAL = RING + NST * 2 * TILE;  // [NST][lse2, D, pos][NQ]
   static constexpr int BAR = SCAL + NST * 3 * NQ * 4;
   static constexpr int SMEM = BAR + Bars<NST>::BYTES + 1024;
-  static constexpr int COL_K = 0, COL_V = D / 2, COL_ST = D, COL_DPT = D + 2 * NQ;
-  static constexpr int COL_DK = D + 4 * NQ, COL_DV = COL_DK + D;
+  static_assert(SMEM <= 232448, "shared memory budget");
+  static constexpr int COL_ST = 0, COL_DPT = NQ, COL_DK = 2 * NQ, COL_DV = 2 * NQ + D;
   static_assert(COL_DV + D <= (int)TMEM_COLS, "tensor memory budget");
 };
 
@@ -346,13 +351,13 @@ __device__ __forceinline__ void init_cta(uint8_t* bar, int warp, uint32_t full_c
       mbar_init(base + BB::FULL + 8 * s, full_count);
       mbar_init(base + BB::EMPTY + 8 * s, 1);
     }
-    for (int t = 0; t < 2; ++t) {
-      mbar_init(base + BB::SDP + 8 * t, 1);
-      mbar_init(base + BB::DS + 8 * t, 256);
-    }
+    mbar_init(base + BB::SDP, 1);
+    mbar_init(base + BB::DS, 256);
     mbar_init(base + BB::A, 256);
     mbar_init(base + BB::FIN, 1);
     mbar_init(base + BB::DRAIN, 1);
+    mbar_init(base + BB::KVF, 1);
+    mbar_init(base + BB::KVE, 1);
     *reinterpret_cast<volatile int*>(bar + BB::ABORT) = 0;
     fence_barrier_init();
     fence_proxy_async_smem();
@@ -360,6 +365,13 @@ __device__ __forceinline__ void init_cta(uint8_t* bar, int warp, uint32_t full_c
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+}
+
+// Elementwise step on 32 columns of one row: P = 2^(s sl2 - lse2) where allowed,
+// dS = P (dP - D); returns dS (or P) packed as bf16 pairs.
+__device__ __forceinline__ float p_of(float s, float sl2, float lse2, bool allowed) {
+  const float pr = ex2(fmaf(s, sl2, -lse2));
+  return allowed ? pr : 0.0f;
 }
 
 // ================================================================ dQ kernel ==
@@ -407,7 +419,7 @@ bwd_dq(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorM
           mbar_expect_tx(fb, 2 * L::TILE);
           for (int kv = 0; kv < 2; ++kv)
             for (int bx = 0; bx < D / 64; ++bx) {
-              const uint32_t dst = smem_u32(sm + L::RING + (slot * 2 + kv) * L::TILE + bx * L::BOX);
+              const uint32_t dst = smem_u32(sm + L::RING + (slot * 2 + kv) * L::TILE + bx * BOX);
               const CUtensorMap* m = kv ? &mv : &mk;
               if constexpr (LONG)
                 tma_load_2d(dst, m, 64 * bx, (it.b * a.H_kv + it.kvh) * a.NR + start, fb);
@@ -432,49 +444,45 @@ bwd_dq(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorM
         return mbar_wait(b_full + 8 * (g % NST), (uint32_t)((g / NST) & 1), abort_flag, status, tlim);
       };
       auto issue_sdp = [&](int g) {
-        const int buf = g & 1;
         const uint32_t ka = kaddr(g), va = ka + L::TILE;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk / 4) * L::BOX + (kk % 4) * 32;
-          umma_ts(tmem + L::COL_S + NK * buf, tmem + L::COL_Q + 8 * kk, sw128_desc(ka + off, 16, 1024),
-                  ISD, kk > 0);
+          const uint32_t off = (kk / 4) * BOX + (kk % 4) * 32;
+          umma_ts(tmem + L::COL_S, tmem + L::COL_Q + 8 * kk, sw128_desc(ka + off, 16, 1024), ISD, kk > 0);
         }
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk / 4) * L::BOX + (kk % 4) * 32;
-          umma_ts(tmem + L::COL_DP + NK * buf, tmem + L::COL_DO + 8 * kk,
-                  sw128_desc(va + off, 16, 1024), ISD, kk > 0);
+          const uint32_t off = (kk / 4) * BOX + (kk % 4) * 32;
+          umma_ts(tmem + L::COL_DP, tmem + L::COL_DO + 8 * kk, sw128_desc(va + off, 16, 1024), ISD,
+                  kk > 0);
         }
-        umma_commit(b_sdp + 8 * buf);
+        umma_commit(b_sdp);
       };
       int g = 0, ac = 0;
       bool ok = true;
       for (int x = blockIdx.x; ok && x < n_items; x += gridDim.x) {
         const BItem it = dq_item<LONG>(a, x);
         if (!it.valid || it.n == 0) continue;
-        if (!(ok = mbar_wait(b_a, (uint32_t)(ac & 1), abort_flag, status, tlim))) break;
+        if (!(ok = mbar_wait(b_a, (uint32_t)(ac & 1), abort_flag, status, tlim) && ring_wait(g))) break;
         ++ac;
-        if (!(ok = ring_wait(g))) break;
         tc_fence_after();
         issue_sdp(g);
         for (int t = 0; t < it.n; ++t) {
           const int gc = g + t;
+          if (!(ok = mbar_wait(b_ds, (uint32_t)(gc & 1), abort_flag, status, tlim))) break;
+          tc_fence_after();
+          const uint32_t ka = kaddr(gc);
+          // dS of keys 64w + 2i, 64w + 2i + 1 sits in column 64w + i of the S region
+#pragma unroll
+          for (int kk = 0; kk < NK / 16; ++kk)
+            umma_ts(tmem + L::COL_DQ, tmem + L::COL_S + 64 * (kk >> 2) + 8 * (kk & 3),
+                    sw128_desc(ka + kk * 2048, BOX, 1024), IDQ, (t > 0 || kk > 0) ? 1u : 0u);
+          umma_commit(b_empty + 8 * (gc % NST));
           if (t + 1 < it.n) {
             if (!(ok = ring_wait(gc + 1))) break;
             tc_fence_after();
             issue_sdp(gc + 1);
           }
-          if (!(ok = mbar_wait(b_ds + 8 * (gc & 1), (uint32_t)((gc >> 1) & 1), abort_flag, status, tlim)))
-            break;
-          tc_fence_after();
-          const uint32_t ka = kaddr(gc);
-          const uint32_t sc = tmem + L::COL_S + NK * (gc & 1);
-#pragma unroll
-          for (int kk = 0; kk < NK / 16; ++kk)
-            umma_ts(tmem + L::COL_DQ, sc + 32 * (kk >> 1) + 8 * (kk & 1),
-                    sw128_desc(ka + kk * 2048, L::BOX, 1024), IDQ, (t > 0 || kk > 0) ? 1u : 0u);
-          umma_commit(b_empty + 8 * (gc % NST));
         }
         if (!ok) break;
         umma_commit(b_fin);
@@ -515,7 +523,7 @@ bwd_dq(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorM
       DqWalk wk;
       wk.init(a, it, LONG);
       for (int t = 0; t < it.n; ++t) {
-        const int gc = g + t, buf = gc & 1;
+        const int gc = g + t;
         int start, cnt;
         bool full;
         wk.next(a, it, LONG, t, start, cnt, full);
@@ -527,34 +535,33 @@ bwd_dq(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorM
         }
         if (!row_ok) c_hi = c_lo;
         const uint32_t width = (uint32_t)max(c_hi - c_lo, 0);
-        ok = mbar_wait(b_sdp + 8 * buf, (uint32_t)((gc >> 1) & 1), abort_flag, status, tlim);
+        ok = mbar_wait(b_sdp, (uint32_t)(gc & 1), abort_flag, status, tlim);
         if (!__all_sync(0xffffffffu, ok)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        uint32_t s[32], dp[32];
-        tmem_ld32(tl + L::COL_S + NK * buf + 32 * wg, s);
-        tmem_ld32(tl + L::COL_DP + NK * buf + 32 * wg, dp);
-        tmem_ld_wait(s);
-        tie32(dp);
-        uint32_t pk[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int c0 = 32 * wg + 2 * i;
-          float ds[2];
+        for (int hh = 0; hh < 2; ++hh) {
+          const int c = 64 * wg + 32 * hh;  // first key column of this half
+          uint32_t s[32], dp[32];
+          tmem_ld32(tl + L::COL_S + c, s);
+          tmem_ld32(tl + L::COL_DP + c, dp);
+          tmem_ld_wait(s);
+          tie32(dp);
+          uint32_t pk[16];
 #pragma unroll
-          for (int h2 = 0; h2 < 2; ++h2) {
-            const float pr = ex2(fmaf(__uint_as_float(s[2 * i + h2]), sl2, -lse2));
-            const float p = ((uint32_t)(c0 + h2 - c_lo) < width) ? pr : 0.0f;
-            ds[h2] = p * (__uint_as_float(dp[2 * i + h2]) - Dr);
+          for (int i = 0; i < 16; ++i) {
+            const float p0 = p_of(__uint_as_float(s[2 * i]), sl2, lse2, (uint32_t)(c + 2 * i - c_lo) < width);
+            const float p1 =
+                p_of(__uint_as_float(s[2 * i + 1]), sl2, lse2, (uint32_t)(c + 2 * i + 1 - c_lo) < width);
+            pk[i] = pack_bf16(p0 * (__uint_as_float(dp[2 * i]) - Dr), p1 * (__uint_as_float(dp[2 * i + 1]) - Dr));
           }
-          pk[i] = pack_bf16(ds[0], ds[1]);
+          tmem_st16(tl + L::COL_S + 64 * wg + 16 * hh, pk);  // over columns already read
         }
-        tmem_st16(tl + L::COL_S + NK * buf + 32 * wg, pk);
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(b_ds + 8 * buf);
+        mbar_arrive(b_ds);
       }
       if (!ok) break;
       // ---- epilogue: dQ = scale * (dS K), window partial or final ----
@@ -594,7 +601,8 @@ bwd_dq(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorM
 // ============================================================= dK/dV kernel ==
 template <int D, bool LONG>
 __global__ void __launch_bounds__(NTHREADS, 1)
-bwd_dkdv(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mdo,
+bwd_dkdv(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv,
+         const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mdo,
          const BwdArgs a, const int n_items) {
   using L = DkvLayout<D>;
   using BB = Bars<L::NST>;
@@ -606,6 +614,7 @@ bwd_dkdv(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtenso
   const uint32_t bb = smem_u32(bar);
   const uint32_t b_full = bb + BB::FULL, b_empty = bb + BB::EMPTY, b_sdp = bb + BB::SDP;
   const uint32_t b_ds = bb + BB::DS, b_a = bb + BB::A, b_fin = bb + BB::FIN, b_drain = bb + BB::DRAIN;
+  const uint32_t b_kvf = bb + BB::KVF, b_kve = bb + BB::KVE;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bar + BB::ABORT);
   float* scal = reinterpret_cast<float*>(sm + L::SCAL);  // [NST][3][NQ]
   init_cta<NST>(bar, warp, 2);
@@ -614,18 +623,40 @@ bwd_dkdv(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtenso
   const long long tlim = a.timeout_cycles;
 
   if (warp == PRODUCER_WARP) {
-    // whole warp: lane 0 issues the copies, every lane stages one query's scalars
+    // whole warp: lane 0 issues the copies, every lane stages four queries' scalars
     if (lane == 0) {
+      tma_prefetch(&mk);
+      tma_prefetch(&mv);
       tma_prefetch(&mq);
       tma_prefetch(&mdo);
     }
     int last_par[NST];
     for (int s = 0; s < NST; ++s) last_par[s] = -1;
-    int g = 0;
+    int g = 0, kc = 0, kv_par = -1;
     bool ok = true;
     for (int x = blockIdx.x; ok && x < n_items; x += gridDim.x) {
       const BItem it = dkv_item<LONG>(a, x);
       if (!it.valid || it.n == 0) continue;
+      // the item's K and V rows, once the previous item's products are done
+      if (lane == 0) {
+        ok = mbar_wait(b_kve, (uint32_t)((kc & 1) ^ 1), abort_flag, status, tlim);
+        if (ok) {
+          mbar_expect_tx(b_kvf, 2 * L::TILE);
+          for (int kv = 0; kv < 2; ++kv)
+            for (int bx = 0; bx < D / 64; ++bx) {
+              const uint32_t dst = smem_u32(sm + L::KV + kv * L::TILE + bx * BOX);
+              const CUtensorMap* m = kv ? &mv : &mk;
+              if constexpr (LONG)
+                tma_load_2d(dst, m, 64 * bx, (it.b * a.H_kv + it.kvh) * a.NR + it.row0, b_kvf);
+              else
+                tma_load_3d(dst, m, 64 * bx, it.kvh, it.b * a.N + it.row0, b_kvf);
+            }
+          kv_par = kc & 1;
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      ++kc;
       DkvWalk wk;
       wk.init(a, it, LONG);
       const int* P = LONG ? a.perm + (int64_t)it.br * a.NR : nullptr;
@@ -642,7 +673,7 @@ bwd_dkdv(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtenso
           mbar_expect_tx(fb, 2 * L::TILE);
           for (int kv = 0; kv < 2; ++kv)
             for (int bx = 0; bx < D / 64; ++bx) {
-              const uint32_t dst = smem_u32(sm + L::RING + (slot * 2 + kv) * L::TILE + bx * L::BOX);
+              const uint32_t dst = smem_u32(sm + L::RING + (slot * 2 + kv) * L::TILE + bx * BOX);
               const CUtensorMap* m = kv ? &mdo : &mq;
               if constexpr (LONG)
                 tma_load_2d(dst, m, 64 * bx, (it.b * a.H + h) * a.NR + start, fb);
@@ -651,86 +682,96 @@ bwd_dkdv(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtenso
             }
         }
         // query scalars: LSE * log2(e) (+inf marks "no query"), D, position
-        float lse2 = INFINITY, dd = 0.0f;
-        int pos = 0;
-        if (lane < cnt) {
-          pos = LONG ? __ldg(P + start + lane) : start + lane;
-          const int64_t li = ((int64_t)it.b * a.H + h) * a.N + pos;
-          lse2 = __ldg(a.lse + li) * kLog2e;
-          dd = __ldg(a.dvec + li);
-        }
         float* sc = scal + slot * 3 * NQ;
-        sc[lane] = lse2;
-        sc[NQ + lane] = dd;
-        reinterpret_cast<int*>(sc)[2 * NQ + lane] = pos;
+#pragma unroll
+        for (int i = 0; i < NQ / 32; ++i) {
+          const int qc = 32 * i + lane;
+          float lse2 = INFINITY, dd = 0.0f;
+          int pos = 0;
+          if (qc < cnt) {
+            pos = LONG ? __ldg(P + start + qc) : start + qc;
+            const int64_t li = ((int64_t)it.b * a.H + h) * a.N + pos;
+            lse2 = __ldg(a.lse + li) * kLog2e;
+            dd = __ldg(a.dvec + li);
+          }
+          sc[qc] = lse2;
+          sc[NQ + qc] = dd;
+          reinterpret_cast<int*>(sc)[2 * NQ + qc] = pos;
+        }
         __syncwarp();
         if (lane == 0) mbar_arrive(fb);
         last_par[slot] = (int)par;
       }
     }
-    if (lane == 0 && *abort_flag)
+    if (lane == 0 && *abort_flag) {
+      if (kv_par >= 0) mbar_drain(b_kvf, (uint32_t)kv_par);
       for (int s = 0; s < NST; ++s)
         if (last_par[s] >= 0) mbar_drain(b_full + 8 * s, (uint32_t)last_par[s]);
+    }
     __syncwarp();
   } else if (warp == MMA_WARP) {
     if (lane == 0) {
       constexpr uint32_t IST = idesc_bf16(128, NQ, 0);  // S^T = K Q^T, dP^T = V dO^T
       constexpr uint32_t IKV = idesc_bf16(128, D, 1);   // dV += P^T dO, dK += dS^T Q
+      const uint32_t k_base = smem_u32(sm + L::KV), v_base = k_base + L::TILE;
       const uint32_t r_base = smem_u32(sm + L::RING);
       auto qaddr = [&](int g) { return r_base + (g % NST) * 2 * L::TILE; };
       auto ring_wait = [&](int g) {
         return mbar_wait(b_full + 8 * (g % NST), (uint32_t)((g / NST) & 1), abort_flag, status, tlim);
       };
       auto issue_st = [&](int g) {
-        const int buf = g & 1;
         const uint32_t qa = qaddr(g), da = qa + L::TILE;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk / 4) * L::BOX + (kk % 4) * 32;
-          umma_ts(tmem + L::COL_ST + NQ * buf, tmem + L::COL_K + 8 * kk, sw128_desc(qa + off, 16, 1024),
+          const uint32_t off = (kk / 4) * BOX + (kk % 4) * 32;
+          umma_ss(tmem + L::COL_ST, sw128_desc(k_base + off, 16, 1024), sw128_desc(qa + off, 16, 1024),
                   IST, kk > 0);
         }
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk / 4) * L::BOX + (kk % 4) * 32;
-          umma_ts(tmem + L::COL_DPT + NQ * buf, tmem + L::COL_V + 8 * kk,
-                  sw128_desc(da + off, 16, 1024), IST, kk > 0);
+          const uint32_t off = (kk / 4) * BOX + (kk % 4) * 32;
+          umma_ss(tmem + L::COL_DPT, sw128_desc(v_base + off, 16, 1024), sw128_desc(da + off, 16, 1024),
+                  IST, kk > 0);
         }
-        umma_commit(b_sdp + 8 * buf);
+        umma_commit(b_sdp);
       };
-      int g = 0, ac = 0;
+      int g = 0, ac = 0, kc = 0;
       bool ok = true;
       for (int x = blockIdx.x; ok && x < n_items; x += gridDim.x) {
         const BItem it = dkv_item<LONG>(a, x);
         if (!it.valid || it.n == 0) continue;
-        if (!(ok = mbar_wait(b_a, (uint32_t)(ac & 1), abort_flag, status, tlim))) break;
-        ++ac;
-        if (!(ok = ring_wait(g))) break;
+        if (!(ok = mbar_wait(b_kvf, (uint32_t)(kc & 1), abort_flag, status, tlim) && ring_wait(g))) break;
+        ++kc;
         tc_fence_after();
         issue_st(g);
+        // the previous item's epilogue has read dK and dV before they restart
+        if (!(ok = mbar_wait(b_a, (uint32_t)(ac & 1), abort_flag, status, tlim))) break;
+        ++ac;
         for (int t = 0; t < it.n; ++t) {
-          const int gc = g + t, buf = gc & 1;
+          const int gc = g + t;
+          if (!(ok = mbar_wait(b_ds, (uint32_t)(gc & 1), abort_flag, status, tlim))) break;
+          tc_fence_after();
+          const uint32_t qa = qaddr(gc), da = qa + L::TILE;
+          // P^T (dS^T) of queries 64w + 2i, 64w + 2i + 1 sits in column 64w + i
+#pragma unroll
+          for (int kk = 0; kk < NQ / 16; ++kk) {
+            const uint32_t acc = (t > 0 || kk > 0) ? 1u : 0u;
+            const uint32_t col = 64 * (kk >> 2) + 8 * (kk & 3);
+            umma_ts(tmem + L::COL_DV, tmem + L::COL_ST + col, sw128_desc(da + kk * 2048, BOX, 1024), IKV,
+                    acc);
+            umma_ts(tmem + L::COL_DK, tmem + L::COL_DPT + col, sw128_desc(qa + kk * 2048, BOX, 1024), IKV,
+                    acc);
+          }
+          umma_commit(b_empty + 8 * (gc % NST));
           if (t + 1 < it.n) {
             if (!(ok = ring_wait(gc + 1))) break;
             tc_fence_after();
             issue_st(gc + 1);
           }
-          if (!(ok = mbar_wait(b_ds + 8 * buf, (uint32_t)((gc >> 1) & 1), abort_flag, status, tlim)))
-            break;
-          tc_fence_after();
-          const uint32_t qa = qaddr(gc), da = qa + L::TILE;
-#pragma unroll
-          for (int kk = 0; kk < NQ / 16; ++kk) {
-            const uint32_t acc = (t > 0 || kk > 0) ? 1u : 0u;
-            umma_ts(tmem + L::COL_DV, tmem + L::COL_ST + NQ * buf + 16 * kk,
-                    sw128_desc(da + kk * 2048, L::BOX, 1024), IKV, acc);
-            umma_ts(tmem + L::COL_DK, tmem + L::COL_DPT + NQ * buf + 16 * kk,
-                    sw128_desc(qa + kk * 2048, L::BOX, 1024), IKV, acc);
-          }
-          umma_commit(b_empty + 8 * (gc % NST));
         }
         if (!ok) break;
         umma_commit(b_fin);
+        umma_commit(b_kve);
         g += it.n;
       }
       umma_commit(b_drain);
@@ -755,61 +796,55 @@ bwd_dkdv(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtenso
       const int pj = LONG ? __ldg(a.perm + (int64_t)it.br * a.NR + it.row0 + rr) : it.row0 + rr;
       const int64_t grow = ((int64_t)it.b * a.N + pj) * a.H_kv + it.kvh;  // [B, N, H_kv] row
       if (it.n > 0) {
-        const bf16* src = (wg == 0 ? a.k : a.v) + grow * D;
-        stage_row<D>(tl + (wg == 0 ? L::COL_K : L::COL_V), row_ok ? src : nullptr);
-        tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(b_a);
+        mbar_arrive(b_a);  // the previous item's dK, dV have been read
         ++ac;
       }
       for (int t = 0; t < it.n; ++t) {
-        const int gc = g + t, buf = gc & 1, slot = gc % NST;
+        const int gc = g + t, slot = gc % NST;
         ok = mbar_wait(b_full + 8 * slot, (uint32_t)((gc / NST) & 1), abort_flag, status, tlim) &&
-             mbar_wait(b_sdp + 8 * buf, (uint32_t)((gc >> 1) & 1), abort_flag, status, tlim);
+             mbar_wait(b_sdp, (uint32_t)(gc & 1), abort_flag, status, tlim);
         if (!__all_sync(0xffffffffu, ok)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        uint32_t st[16], dpt[16];
-        tmem_ld16(tl + L::COL_ST + NQ * buf + 16 * wg, st);
-        tmem_ld16(tl + L::COL_DPT + NQ * buf + 16 * wg, dpt);
-        const float* sc = scal + slot * 3 * NQ + 16 * wg;
-        float ls[16], dd[16];
-        int pq[16];
+        const float* sc = scal + slot * 3 * NQ;
 #pragma unroll
-        for (int i = 0; i < 16; i += 4) {
-          const float4 l4 = *reinterpret_cast<const float4*>(sc + i);
-          const float4 d4 = *reinterpret_cast<const float4*>(sc + NQ + i);
-          const int4 p4 = *reinterpret_cast<const int4*>(reinterpret_cast<const int*>(sc) + 2 * NQ + i);
-          ls[i] = l4.x; ls[i + 1] = l4.y; ls[i + 2] = l4.z; ls[i + 3] = l4.w;
-          dd[i] = d4.x; dd[i + 1] = d4.y; dd[i + 2] = d4.z; dd[i + 3] = d4.w;
-          pq[i] = p4.x; pq[i + 1] = p4.y; pq[i + 2] = p4.z; pq[i + 3] = p4.w;
-        }
-        tmem_ld_wait(st);
-        tie16(dpt);
-        uint32_t pp[8], pd[8];
+        for (int hh = 0; hh < 2; ++hh) {
+          const int c = 64 * wg + 32 * hh;  // first query column of this half
+          uint32_t st[32], dpt[32];
+          tmem_ld32(tl + L::COL_ST + c, st);
+          tmem_ld32(tl + L::COL_DPT + c, dpt);
+          tmem_ld_wait(st);
+          tie32(dpt);
+          uint32_t pp[16], pd[16];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          float p2[2], d2[2];
+          for (int i = 0; i < 32; i += 4) {
+            const float4 l4 = *reinterpret_cast<const float4*>(sc + c + i);
+            const float4 d4 = *reinterpret_cast<const float4*>(sc + NQ + c + i);
+            const int4 q4 = *reinterpret_cast<const int4*>(reinterpret_cast<const int*>(sc) + 2 * NQ + c + i);
+            const float ls[4] = {l4.x, l4.y, l4.z, l4.w}, dd[4] = {d4.x, d4.y, d4.z, d4.w};
+            const int pq[4] = {q4.x, q4.y, q4.z, q4.w};
+            float pv[4], dv4[4];
 #pragma unroll
-          for (int h2 = 0; h2 < 2; ++h2) {
-            const int c = 2 * i + h2;
-            const int dpos = pq[c] - pj;
-            const bool allowed = LONG ? dpos >= w : (uint32_t)dpos < (uint32_t)w;
-            const float pr = ex2(fmaf(__uint_as_float(st[c]), sl2, -ls[c]));
-            const float p = (row_ok && allowed) ? pr : 0.0f;
-            p2[h2] = p;
-            d2[h2] = p * (__uint_as_float(dpt[c]) - dd[c]);
+            for (int e = 0; e < 4; ++e) {
+              const int dpos = pq[e] - pj;
+              const bool allowed = row_ok && (LONG ? dpos >= w : (uint32_t)dpos < (uint32_t)w);
+              pv[e] = p_of(__uint_as_float(st[i + e]), sl2, ls[e], allowed);
+              dv4[e] = pv[e] * (__uint_as_float(dpt[i + e]) - dd[e]);
+            }
+            pp[i / 2] = pack_bf16(pv[0], pv[1]);
+            pp[i / 2 + 1] = pack_bf16(pv[2], pv[3]);
+            pd[i / 2] = pack_bf16(dv4[0], dv4[1]);
+            pd[i / 2 + 1] = pack_bf16(dv4[2], dv4[3]);
           }
-          pp[i] = pack_bf16(p2[0], p2[1]);
-          pd[i] = pack_bf16(d2[0], d2[1]);
+          tmem_st16(tl + L::COL_ST + 64 * wg + 16 * hh, pp);   // over columns already read
+          tmem_st16(tl + L::COL_DPT + 64 * wg + 16 * hh, pd);
         }
-        tmem_st8(tl + L::COL_ST + NQ * buf + 16 * wg, pp);
-        tmem_st8(tl + L::COL_DPT + NQ * buf + 16 * wg, pd);
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(b_ds + 8 * buf);
+        mbar_arrive(b_ds);
       }
       if (!ok) break;
       // ---- epilogue: dK = scale * (dS^T Q) (warpgroup 0), dV = P^T dO (warpgroup 1) ----
@@ -947,17 +982,30 @@ int num_sms() {
   return n;
 }
 
-template <typename Kernel>
-cudaError_t launch_persistent(Kernel kernel, int smem, const CUtensorMap& m0, const CUtensorMap& m1,
-                              const BwdArgs& a, int n_items, cudaStream_t s) {
+template <typename Kernel, typename... Maps>
+cudaError_t launch_persistent(Kernel kernel, int smem, const BwdArgs& a, int n_items, cudaStream_t s,
+                              const Maps&... maps) {
   smem = smem < kMinSmem ? kMinSmem : smem;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int sms = num_sms();
   const int grid = n_items < sms ? n_items : sms;
   if (grid < 1) return cudaSuccess;
-  kernel<<<grid, NTHREADS, smem, s>>>(m0, m1, a, n_items);
+  kernel<<<grid, NTHREADS, smem, s>>>(maps..., a, n_items);
   return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_pass(const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mq,
+                        const CUtensorMap& mdo, const BwdArgs& a, int nq_items, int nk_items,
+                        bool long_pass, cudaStream_t s) {
+  cudaError_t e;
+  if (long_pass) {
+    if ((e = launch_persistent(bwd_dq<D, true>, DqLayout<D>::SMEM, a, nq_items, s, mk, mv))) return e;
+    return launch_persistent(bwd_dkdv<D, true>, DkvLayout<D>::SMEM, a, nk_items, s, mk, mv, mq, mdo);
+  }
+  if ((e = launch_persistent(bwd_dq<D, false>, DqLayout<D>::SMEM, a, nq_items, s, mk, mv))) return e;
+  return launch_persistent(bwd_dkdv<D, false>, DkvLayout<D>::SMEM, a, nk_items, s, mk, mv, mq, mdo);
 }
 
 }  // namespace
@@ -1023,40 +1071,30 @@ cudaError_t launch_attn_bwd(const focus_params& p, const BwdPlan& bp, const bf16
   a.status = &reinterpret_cast<WsHeader*>(ws)->status;
   a.timeout_cycles = kTimeoutCycles;
   const int D = p.d_head;
-  const int gq = p.H / p.H_kv;
-  CUtensorMap m0, m1, m2, m3;
-  cudaError_t e;
+  CUtensorMap mk, mv, mq, mdo;
+  int nq_items, nk_items;
   if (!long_pass) {
-    // window: token-order maps over K, V (dQ) and Q, dO (dK, dV)
-    if (!make_map(&m0, k, D, (int64_t)p.B * p.N, p.H_kv, NK) ||
-        !make_map(&m1, v, D, (int64_t)p.B * p.N, p.H_kv, NK) ||
-        !make_map(&m2, q, D, (int64_t)p.B * p.N, p.H, NQ) ||
-        !make_map(&m3, d_o, D, (int64_t)p.B * p.N, p.H, NQ))
+    // window: token-order maps over K, V, Q, dO
+    if (!make_map(&mk, k, D, (int64_t)p.B * p.N, p.H_kv, NK) ||
+        !make_map(&mv, v, D, (int64_t)p.B * p.N, p.H_kv, NK) ||
+        !make_map(&mq, q, D, (int64_t)p.B * p.N, p.H, NQ) ||
+        !make_map(&mdo, d_o, D, (int64_t)p.B * p.N, p.H, NQ))
       return cudaErrorInvalidValue;
     const int nb = (p.N + BM - 1) / BM;
-    const int nq_items = p.B * p.H * nb, nk_items = p.B * p.H_kv * nb;
-    if (D == 64) {
-      if ((e = launch_persistent(bwd_dq<64, false>, DqLayout<64>::SMEM, m0, m1, a, nq_items, s))) return e;
-      return launch_persistent(bwd_dkdv<64, false>, DkvLayout<64>::SMEM, m2, m3, a, nk_items, s);
-    }
-    if ((e = launch_persistent(bwd_dq<128, false>, DqLayout<128>::SMEM, m0, m1, a, nq_items, s))) return e;
-    return launch_persistent(bwd_dkdv<128, false>, DkvLayout<128>::SMEM, m2, m3, a, nk_items, s);
+    nq_items = p.B * p.H * nb;
+    nk_items = p.B * p.H_kv * nb;
+  } else {
+    // long range: maps over the permuted head-major copies
+    if (!make_map(&mk, ws + L.kp, D, (int64_t)p.B * p.H_kv * L.NR, 0, NK) ||
+        !make_map(&mv, ws + L.vp, D, (int64_t)p.B * p.H_kv * L.NR, 0, NK) ||
+        !make_map(&mq, ws + L.qp, D, (int64_t)p.B * p.H * L.NR, 0, NQ) ||
+        !make_map(&mdo, ws + bp.dop, D, (int64_t)p.B * p.H * L.NR, 0, NQ))
+      return cudaErrorInvalidValue;
+    nq_items = L.qtab_cap * (p.H / p.R);
+    nk_items = L.qtab_cap * (p.H_kv / p.R);
   }
-  // long range: maps over the permuted head-major copies
-  if (!make_map(&m0, ws + L.kp, D, (int64_t)p.B * p.H_kv * L.NR, 0, NK) ||
-      !make_map(&m1, ws + L.vp, D, (int64_t)p.B * p.H_kv * L.NR, 0, NK) ||
-      !make_map(&m2, ws + L.qp, D, (int64_t)p.B * p.H * L.NR, 0, NQ) ||
-      !make_map(&m3, ws + bp.dop, D, (int64_t)p.B * p.H * L.NR, 0, NQ))
-    return cudaErrorInvalidValue;
-  const int nq_items = L.qtab_cap * (p.H / p.R);
-  const int nk_items = L.qtab_cap * (p.H_kv / p.R);
-  (void)gq;
-  if (D == 64) {
-    if ((e = launch_persistent(bwd_dq<64, true>, DqLayout<64>::SMEM, m0, m1, a, nq_items, s))) return e;
-    return launch_persistent(bwd_dkdv<64, true>, DkvLayout<64>::SMEM, m2, m3, a, nk_items, s);
-  }
-  if ((e = launch_persistent(bwd_dq<128, true>, DqLayout<128>::SMEM, m0, m1, a, nq_items, s))) return e;
-  return launch_persistent(bwd_dkdv<128, true>, DkvLayout<128>::SMEM, m2, m3, a, nk_items, s);
+  return D == 64 ? launch_pass<64>(mk, mv, mq, mdo, a, nq_items, nk_items, long_pass, s)
+                 : launch_pass<128>(mk, mv, mq, mdo, a, nq_items, nk_items, long_pass, s);
 }
 
 }  // namespace focus

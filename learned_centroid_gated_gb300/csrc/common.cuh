@@ -42,8 +42,8 @@ constexpr int kSinkBlock = 256;   // tokens per Sinkhorn partial-reduction block
 constexpr int kAttnBM = 256;      // query rows per long-range work item
 constexpr int kKeySentinel = 0x7fffffff;
 constexpr int kBwdBlock = 128;    // backward: query rows (dQ) or key rows (dK, dV) per item
-constexpr int kBwdKeyTile = 64;   // backward dQ: keys per tile
-constexpr int kBwdQryTile = 32;   // backward dK, dV: queries per tile
+constexpr int kBwdKeyTile = 128;  // backward dQ: keys per tile
+constexpr int kBwdQryTile = 128;  // backward dK, dV: queries per tile
 
 // Workspace layout.  Segment schedule: nseg = C(K, top_k) segments over NR = N rows
 // per (b, rho).  Group schedule: nseg = K lists over NR = N * top_k rows, plus the
