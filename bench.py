@@ -53,11 +53,12 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target CPU time of the oracle sample")
-    ap.add_argument("--sweep", choices=["table6", "decode", "schedule"], default=None,
+    ap.add_argument("--sweep", choices=["table6", "decode", "schedule", "backward"], default=None,
                     help="table6: speedup of Focus over this build's own dense causal mode "
                          "(K=1) across context lengths, K=4 and K=8; decode: one decode step "
                          "per workload; schedule: exact-set segments vs group lists over "
-                         "(K, top_k) at 32K tokens (one JSON line each)")
+                         "(K, top_k) at 32K tokens; backward: dq, dk, dv with the masks held "
+                         "fixed, per kernel (one JSON line each)")
     return ap.parse_args()
 
 
@@ -572,8 +573,84 @@ def run_schedule(args):
                       "rows": rows}), flush=True)
 
 
+# ------------------------------------------------------------- backward --
+def run_backward(args):
+    """Backward pass (hard mask held fixed) per workload: the forward for reference,
+    the backward's stages, and tensor-core rates.  Work is counted on allowed pairs:
+    the forward's 2 products (4 d flops per pair), the backward's 5 (10 d: S, dP, dQ,
+    dK, dV); its kernels execute 7 (dQ recomputes S and dP: the long-range dQ kernel
+    runs 3 products, the dK/dV kernel 4)."""
+    import learned_centroid_gated_gb300 as focus
+    from learned_centroid_gated_gb300 import pairs
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    peaks, peak_src = load_peaks()
+    rows = []
+    for name in ("mha7b_32k", "gqa_128k"):
+        wl = synth.WORKLOADS[name]
+        x = synth.make_inputs(wl, seed=args.seed, device=dev)
+        p = focus.Params.from_workload(wl)
+        mask, _ = focus.route(p, x["r"], x["C"])
+        o, lse = focus.attn_fwd(p, x["q"], x["k"], x["v"], mask=mask)
+        g = torch.Generator(device="cpu").manual_seed(args.seed + 1)
+        d_o = torch.randn(x["q"].shape, generator=g).to(torch.bfloat16).to(dev)
+        ws = torch.empty(focus.bwd_workspace_size(p), dtype=torch.uint8, device=dev)
+        grads = (torch.empty_like(x["q"]), torch.empty_like(x["k"]), torch.empty_like(x["v"]))
+        run = lambda evs=None: focus.attn_bwd(p, x["q"], x["k"], x["v"], mask, o, lse, d_o, dq=grads[0],
+                                             dk=grads[1], dv=grads[2], ws=ws, stream=stream, stage_events=evs)
+        for _ in range(max(args.warmup, 2)):
+            run()
+        torch.cuda.synchronize()
+        status = focus.get_status(ws)
+        if status != 0:
+            raise RuntimeError(f"device status {status}")
+        steps = 5
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(focus.N_BWD_STAGE_EVENTS)]
+               for _ in range(steps)]
+        for e in evs:
+            run(e)
+        torch.cuda.synchronize()
+        stage = {n: statistics.median(e[i].elapsed_time(e[i + 1]) for e in evs)
+                 for i, n in enumerate(focus.BWD_STAGES)}
+        bwd_ms = statistics.median(e[0].elapsed_time(e[-1]) for e in evs)
+        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        f0.record(stream)
+        for _ in range(steps):
+            focus.attn_fwd(p, x["q"], x["k"], x["v"], mask=mask, out=o, lse=lse, stream=stream)
+        f1.record(stream)
+        torch.cuda.synchronize()
+        fwd_ms = f0.elapsed_time(f1) / steps
+        allowed = int(pairs.allowed_pairs(mask.cpu().numpy().view(np.uint32), wl.w).sum()) * (wl.H // wl.R)
+        window = pairs.window_pairs(wl.N, wl.w) * wl.B * wl.H
+        longr = allowed - window
+        d = wl.d_head
+        tf = lambda flops, ms: flops / (ms / 1e3) / 1e12
+        dkdv = tf(8.0 * d * longr, stage["long_dkdv"])
+        rows.append({
+            "workload": name, "config": config_of(wl), "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
+            "bwd_over_fwd": bwd_ms / fwd_ms, "stages_ms": stage,
+            "fwd_allowed_pair_tflops": tf(4.0 * d * allowed, fwd_ms),
+            "bwd_allowed_pair_tflops": tf(10.0 * d * allowed, bwd_ms),
+            "bwd_executed_tflops": tf(14.0 * d * allowed, bwd_ms),
+            "long_dq_tflops": tf(6.0 * d * longr, stage["long_dq"]),
+            "long_dkdv_tflops": dkdv,
+            "roofline": {"kernel": "bwd_dkdv (long range, tcgen05)", "bound": "tensor",
+                         "achieved": dkdv, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                         "frac": dkdv / peaks["bf16_tflops"], "peak_source": peak_src},
+        })
+        del x, ws, o, lse, d_o, grads
+        torch.cuda.empty_cache()
+    print(json.dumps({"sweep": "backward", "unit": "ms per pass", "dtype": "bf16", "data": "synthetic",
+                      "l2": "inputs larger than L2, no flush", "rows": rows}), flush=True)
+
+
 def main():
     args = parse_args()
+    if args.sweep == "backward":
+        run_backward(args)
+        return
     if args.sweep == "schedule":
         run_schedule(args)
         return

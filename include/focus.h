@@ -278,6 +278,19 @@ int focus_attn_bwd(const focus_params* p, const uint16_t* q, const uint16_t* k, 
                    void* stream);
 
 /*
+ * focus_attn_bwd with stage timing (as focus_attn_fwd_ev): FOCUS_BWD_STAGE_EVENTS
+ * caller-created cudaEvent_t handles (or NULL), recorded on `stream` at [0] start,
+ * [1] after bucketing, plans, permuted copies and D, [2] after the window pass
+ * (dQ and dK/dV kernels), [3] after the long-range dQ kernel, [4] after the
+ * long-range dK/dV kernel.
+ */
+#define FOCUS_BWD_STAGE_EVENTS 5
+int focus_attn_bwd_ev(const focus_params* p, const uint16_t* q, const uint16_t* k,
+                      const uint16_t* v, const uint32_t* mask, const uint16_t* o, const float* lse,
+                      const uint16_t* d_o, uint16_t* dq, uint16_t* dk, uint16_t* dv, void* ws,
+                      size_t ws_bytes, void* stream, void* const* stage_events);
+
+/*
  * Diagnostic of the device-side failure path (no counterpart in the paper): runs
  * the attention kernel on a tiny problem with its TMA producer held back and
  * ~10 ms wait limits, so the tensor-core issuer's first bounded wait runs out. The

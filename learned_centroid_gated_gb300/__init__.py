@@ -120,6 +120,11 @@ _lib.focus_bwd_workspace_size.argtypes = [_PP]
 _lib.focus_bwd_workspace_size.restype = ctypes.c_size_t
 _lib.focus_attn_bwd.argtypes = [_PP, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]
 _lib.focus_attn_bwd.restype = ctypes.c_int
+_lib.focus_attn_bwd_ev.argtypes = [_PP, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P,
+                                   ctypes.POINTER(ctypes.c_void_p)]
+_lib.focus_attn_bwd_ev.restype = ctypes.c_int
+N_BWD_STAGE_EVENTS = 5
+BWD_STAGES = ("prepare", "window", "long_dq", "long_dkdv")
 _lib.focus_decode_workspace_size.argtypes = [_PP]
 _lib.focus_decode_workspace_size.restype = ctypes.c_size_t
 _lib.focus_decode.argtypes = [_PP, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]
@@ -357,10 +362,13 @@ def bwd_workspace_size(p: Params) -> int:
 
 def attn_bwd(p: Params, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, mask: torch.Tensor,
              o: torch.Tensor, lse: torch.Tensor, d_o: torch.Tensor, *, dq=None, dk=None, dv=None,
-             ws=None, stream=None):
+             ws=None, stream=None, stage_events=None):
     """Backward of attn_fwd with the masks held fixed.  q, o, d_o [B, N, H, d] bf16;
     k, v [B, N, H_kv, d] bf16; mask [B, R, N] (the forward's); lse [B, H, N] fp32 (the
-    forward's).  Returns (dq, dk, dv) bf16 in the layouts of q, k, v."""
+    forward's).  Returns (dq, dk, dv) bf16 in the layouts of q, k, v.
+
+    stage_events: optional list of N_BWD_STAGE_EVENTS torch.cuda.Event(enable_timing=True)
+    recorded at the stage boundaries (see focus_attn_bwd_ev)."""
     for t in (q, k, v, o, d_o):
         _bf16_bits(t)
     dq = torch.empty_like(q) if dq is None else dq
@@ -371,9 +379,18 @@ def attn_bwd(p: Params, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, mask:
         raise FocusError(-2, "focus_bwd_workspace_size")
     if ws is None or ws.numel() < need:
         ws = torch.empty(need, dtype=torch.uint8, device=q.device)
-    _check(_lib.focus_attn_bwd(ctypes.byref(p.c()), _ptr(q), _ptr(k), _ptr(v), _ptr(mask.contiguous()),
-                               _ptr(o), _ptr(lse.contiguous()), _ptr(d_o), _ptr(dq), _ptr(dk), _ptr(dv),
-                               _ptr(ws), ws.numel(), _stream(stream)), "focus_attn_bwd")
+    args = (ctypes.byref(p.c()), _ptr(q), _ptr(k), _ptr(v), _ptr(mask.contiguous()), _ptr(o),
+            _ptr(lse.contiguous()), _ptr(d_o), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws), ws.numel(),
+            _stream(stream))
+    if stage_events is None:
+        _check(_lib.focus_attn_bwd(*args), "focus_attn_bwd")
+    else:
+        assert len(stage_events) == N_BWD_STAGE_EVENTS
+        for e in stage_events:
+            if e.cuda_event == 0:  # torch creates the CUDA event on its first record
+                e.record(stream or torch.cuda.current_stream())
+        evs = (ctypes.c_void_p * N_BWD_STAGE_EVENTS)(*[e.cuda_event for e in stage_events])
+        _check(_lib.focus_attn_bwd_ev(*args, evs), "focus_attn_bwd_ev")
     return dq, dk, dv
 
 

@@ -28,9 +28,9 @@
 // The window pass writes fp32 partials; the long-range pass adds them and writes
 // the bf16 gradients (the two key sets are disjoint, so the sums are the totals).
 //
-// Warps: 0-7 elementwise (two warpgroups, each 64 columns of every tile, lane =
-// TMEM row), 8 producer (TMA; in bwd_dkdv the whole warp also stages the tile's
-// per-query LSE, D and position), 9 MMA issuer, 10-11 idle.
+// Warps: 0-15 elementwise (four warpgroups, each 32 columns of every tile, lane =
+// TMEM row), 16 producer (TMA; in bwd_dkdv the whole warp also stages the tile's
+// per-query LSE, D and position), 17 MMA issuer.
 #include <math.h>
 
 #include <mutex>
@@ -43,9 +43,11 @@ namespace {
 
 using namespace ptx;
 
-constexpr int NTHREADS = 384;
-constexpr int PRODUCER_WARP = 8;
-constexpr int MMA_WARP = 9;
+constexpr int EW_WARPS = 16;             // elementwise warps: four warpgroups
+constexpr int EW_THREADS = 32 * EW_WARPS;
+constexpr int NTHREADS = EW_THREADS + 64;
+constexpr int PRODUCER_WARP = EW_WARPS;
+constexpr int MMA_WARP = EW_WARPS + 1;
 constexpr int BM = kBwdBlock;       // rows per item
 constexpr int NK = kBwdKeyTile;     // keys per dQ tile
 constexpr int NQ = kBwdQryTile;     // queries per dK/dV tile
@@ -337,6 +339,31 @@ __device__ __forceinline__ void emit32(const uint32_t (&y)[32], float mul, float
   }
 }
 
+// 16-column form of emit32.
+template <bool LONG>
+__device__ __forceinline__ void emit16(const uint32_t (&y)[16], float mul, float* part, bf16* out) {
+  if constexpr (!LONG) {
+    float4* dst = reinterpret_cast<float4*>(part);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      dst[i] = make_float4(__uint_as_float(y[4 * i]) * mul, __uint_as_float(y[4 * i + 1]) * mul,
+                           __uint_as_float(y[4 * i + 2]) * mul, __uint_as_float(y[4 * i + 3]) * mul);
+  } else {
+    const float4* src = reinterpret_cast<const float4*>(part);
+    uint32_t pk[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float4 w = src[i];
+      pk[2 * i] = pack_bf16(w.x + __uint_as_float(y[4 * i]) * mul, w.y + __uint_as_float(y[4 * i + 1]) * mul);
+      pk[2 * i + 1] =
+          pack_bf16(w.z + __uint_as_float(y[4 * i + 2]) * mul, w.w + __uint_as_float(y[4 * i + 3]) * mul);
+    }
+    uint4* dst = reinterpret_cast<uint4*>(out);
+#pragma unroll
+    for (int i = 0; i < 2; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+  }
+}
+
 // Common prologue: TMEM allocation, barrier initialisation.
 template <int NST>
 __device__ __forceinline__ void init_cta(uint8_t* bar, int warp, uint32_t full_count) {
@@ -352,8 +379,8 @@ __device__ __forceinline__ void init_cta(uint8_t* bar, int warp, uint32_t full_c
       mbar_init(base + BB::EMPTY + 8 * s, 1);
     }
     mbar_init(base + BB::SDP, 1);
-    mbar_init(base + BB::DS, 256);
-    mbar_init(base + BB::A, 256);
+    mbar_init(base + BB::DS, EW_THREADS);
+    mbar_init(base + BB::A, EW_THREADS);
     mbar_init(base + BB::FIN, 1);
     mbar_init(base + BB::DRAIN, 1);
     mbar_init(base + BB::KVF, 1);
@@ -365,13 +392,6 @@ __device__ __forceinline__ void init_cta(uint8_t* bar, int warp, uint32_t full_c
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-}
-
-// Elementwise step on 32 columns of one row: P = 2^(s sl2 - lse2) where allowed,
-// dS = P (dP - D); returns dS (or P) packed as bf16 pairs.
-__device__ __forceinline__ float p_of(float s, float sl2, float lse2, bool allowed) {
-  const float pr = ex2(fmaf(s, sl2, -lse2));
-  return allowed ? pr : 0.0f;
 }
 
 // ================================================================ dQ kernel ==
@@ -472,10 +492,10 @@ bwd_dq(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorM
           if (!(ok = mbar_wait(b_ds, (uint32_t)(gc & 1), abort_flag, status, tlim))) break;
           tc_fence_after();
           const uint32_t ka = kaddr(gc);
-          // dS of keys 64w + 2i, 64w + 2i + 1 sits in column 64w + i of the S region
+          // dS of keys 32w + 2i, 32w + 2i + 1 sits in column 32w + i of the S region
 #pragma unroll
           for (int kk = 0; kk < NK / 16; ++kk)
-            umma_ts(tmem + L::COL_DQ, tmem + L::COL_S + 64 * (kk >> 2) + 8 * (kk & 3),
+            umma_ts(tmem + L::COL_DQ, tmem + L::COL_S + 32 * (kk >> 1) + 8 * (kk & 1),
                     sw128_desc(ka + kk * 2048, BOX, 1024), IDQ, (t > 0 || kk > 0) ? 1u : 0u);
           umma_commit(b_empty + 8 * (gc % NST));
           if (t + 1 < it.n) {
@@ -492,7 +512,7 @@ bwd_dq(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorM
       mbar_drain(b_drain, 0);
     }
     __syncwarp();
-  } else if (warp < 8) {
+  } else if (warp < EW_WARPS) {
     // ---------------------------------------------------------- elementwise --
     const int wg = warp >> 2;
     const int r = (warp & 3) * 32 + lane;
@@ -510,9 +530,11 @@ bwd_dq(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorM
       const int qp = LONG ? __ldg(P + it.row0 + rr) : it.row0 + rr;
       const int64_t grow = ((int64_t)it.b * a.N + qp) * a.H + it.h;  // [B, N, H] row
       if (it.n > 0) {
-        const bf16* src = (wg == 0 ? a.q : a.dout) + grow * D;
-        stage_row<D>(tl + (wg == 0 ? L::COL_Q : L::COL_DO), row_ok ? src : nullptr);
-        tmem_st_wait();
+        if (wg < 2) {  // warpgroup 0 stages the Q rows, 1 the dO rows
+          const bf16* src = (wg == 0 ? a.q : a.dout) + grow * D;
+          stage_row<D>(tl + (wg == 0 ? L::COL_Q : L::COL_DO), row_ok ? src : nullptr);
+          tmem_st_wait();
+        }
         tc_fence_before();
         mbar_arrive(b_a);
         ++ac;
@@ -527,13 +549,18 @@ bwd_dq(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorM
         int start, cnt;
         bool full;
         wk.next(a, it, LONG, t, start, cnt, full);
-        int c_lo = 0, c_hi;
-        if constexpr (LONG) c_hi = full ? cnt : upper_bound_g(P + start, 0, cnt, qp - a.w);
-        else {
+        // every (row, key) pair of the tile allowed?  (uniform over the CTA; rows past
+        // the block are never stored, so they need no mask)
+        bool need_mask;
+        int c_lo = 0, c_hi = cnt;
+        if constexpr (LONG) {
+          need_mask = !(full && cnt == NK);
+          if (need_mask && !full) c_hi = upper_bound_g(P + start, 0, cnt, qp - a.w);
+        } else {
+          need_mask = !(cnt == NK && start + NK - 1 <= it.row0 && it.row0 + BM - 1 - start < a.w);
           c_lo = max(0, qp - a.w + 1 - start);
           c_hi = min(cnt, qp - start + 1);
         }
-        if (!row_ok) c_hi = c_lo;
         const uint32_t width = (uint32_t)max(c_hi - c_lo, 0);
         ok = mbar_wait(b_sdp, (uint32_t)(gc & 1), abort_flag, status, tlim);
         if (!__all_sync(0xffffffffu, ok)) {
@@ -543,21 +570,27 @@ bwd_dq(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorM
         tc_fence_after();
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
-          const int c = 64 * wg + 32 * hh;  // first key column of this half
-          uint32_t s[32], dp[32];
-          tmem_ld32(tl + L::COL_S + c, s);
-          tmem_ld32(tl + L::COL_DP + c, dp);
+          const int c = 32 * wg + 16 * hh;  // first key column of this half
+          uint32_t s[16], dp[16];
+          tmem_ld16(tl + L::COL_S + c, s);
+          tmem_ld16(tl + L::COL_DP + c, dp);
           tmem_ld_wait(s);
-          tie32(dp);
-          uint32_t pk[16];
+          tie16(dp);
+          uint32_t pk[8];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float p0 = p_of(__uint_as_float(s[2 * i]), sl2, lse2, (uint32_t)(c + 2 * i - c_lo) < width);
-            const float p1 =
-                p_of(__uint_as_float(s[2 * i + 1]), sl2, lse2, (uint32_t)(c + 2 * i + 1 - c_lo) < width);
-            pk[i] = pack_bf16(p0 * (__uint_as_float(dp[2 * i]) - Dr), p1 * (__uint_as_float(dp[2 * i + 1]) - Dr));
+          for (int i = 0; i < 8; ++i) {
+            float y0, y1, t0, t1, d0, d1;
+            ffma2(y0, y1, __uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1]), sl2, sl2, -lse2, -lse2);
+            float p0 = ex2(y0), p1 = ex2(y1);
+            if (need_mask) {
+              if ((uint32_t)(c + 2 * i - c_lo) >= width) p0 = 0.0f;
+              if ((uint32_t)(c + 2 * i + 1 - c_lo) >= width) p1 = 0.0f;
+            }
+            fadd2(t0, t1, __uint_as_float(dp[2 * i]), __uint_as_float(dp[2 * i + 1]), -Dr, -Dr);
+            fmul2(d0, d1, p0, p1, t0, t1);
+            pk[i] = pack_bf16(d0, d1);
           }
-          tmem_st16(tl + L::COL_S + 64 * wg + 16 * hh, pk);  // over columns already read
+          tmem_st8(tl + L::COL_S + 32 * wg + 8 * hh, pk);  // over columns already read
         }
         tmem_st_wait();
         tc_fence_before();
@@ -576,16 +609,16 @@ bwd_dq(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorM
       g += it.n;
 #pragma unroll
       for (int c = 0; c < D / 64; ++c) {
-        const int col = wg * (D / 2) + 32 * c;
-        uint32_t y[32];
+        const int col = wg * (D / 4) + 16 * c;
+        uint32_t y[16];
         if (it.n > 0) {
-          tmem_ld32(tl + L::COL_DQ + col, y);
+          tmem_ld16(tl + L::COL_DQ + col, y);
           tmem_ld_wait(y);
         } else {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) y[i] = 0u;
+          for (int i = 0; i < 16; ++i) y[i] = 0u;
         }
-        if (row_ok) emit32<LONG>(y, a.scale, a.dq_w + grow * D + col, a.dq + grow * D + col);
+        if (row_ok) emit16<LONG>(y, a.scale, a.dq_w + grow * D + col, a.dq + grow * D + col);
       }
       tc_fence_before();
     }
@@ -752,11 +785,11 @@ bwd_dkdv(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtenso
           if (!(ok = mbar_wait(b_ds, (uint32_t)(gc & 1), abort_flag, status, tlim))) break;
           tc_fence_after();
           const uint32_t qa = qaddr(gc), da = qa + L::TILE;
-          // P^T (dS^T) of queries 64w + 2i, 64w + 2i + 1 sits in column 64w + i
+          // P^T (dS^T) of queries 32w + 2i, 32w + 2i + 1 sits in column 32w + i
 #pragma unroll
           for (int kk = 0; kk < NQ / 16; ++kk) {
             const uint32_t acc = (t > 0 || kk > 0) ? 1u : 0u;
-            const uint32_t col = 64 * (kk >> 2) + 8 * (kk & 3);
+            const uint32_t col = 32 * (kk >> 1) + 8 * (kk & 1);
             umma_ts(tmem + L::COL_DV, tmem + L::COL_ST + col, sw128_desc(da + kk * 2048, BOX, 1024), IKV,
                     acc);
             umma_ts(tmem + L::COL_DK, tmem + L::COL_DPT + col, sw128_desc(qa + kk * 2048, BOX, 1024), IKV,
@@ -778,7 +811,7 @@ bwd_dkdv(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtenso
       mbar_drain(b_drain, 0);
     }
     __syncwarp();
-  } else if (warp < 8) {
+  } else if (warp < EW_WARPS) {
     // ---------------------------------------------------------- elementwise --
     const int wg = warp >> 2;
     const int r = (warp & 3) * 32 + lane;
@@ -795,6 +828,9 @@ bwd_dkdv(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtenso
       const int rr = min(r, it.rows - 1);
       const int pj = LONG ? __ldg(a.perm + (int64_t)it.br * a.NR + it.row0 + rr) : it.row0 + rr;
       const int64_t grow = ((int64_t)it.b * a.N + pj) * a.H_kv + it.kvh;  // [B, N, H_kv] row
+      // last key position of the block (keys ascend in it)
+      const int p_hi = LONG ? __ldg(a.perm + (int64_t)it.br * a.NR + it.row0 + it.rows - 1)
+                            : it.row0 + it.rows - 1;
       if (it.n > 0) {
         tc_fence_before();
         mbar_arrive(b_a);  // the previous item's dK, dV have been read
@@ -810,44 +846,59 @@ bwd_dkdv(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtenso
         }
         tc_fence_after();
         const float* sc = scal + slot * 3 * NQ;
+        // every (key, query) pair of the tile allowed?  Queries past the tile's count
+        // carry LSE = +inf (P = 0) and keys past the block are never stored, so only
+        // the position rule needs a mask: long range, the first (lowest) query
+        // position against the last key; window, both window edges.
+        const int q_first = reinterpret_cast<const int*>(sc)[2 * NQ];
+        const bool need_mask =
+            LONG ? q_first < p_hi + w : !(q_first >= it.row0 + BM - 1 && q_first + NQ - 1 - it.row0 < w);
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
-          const int c = 64 * wg + 32 * hh;  // first query column of this half
-          uint32_t st[32], dpt[32];
-          tmem_ld32(tl + L::COL_ST + c, st);
-          tmem_ld32(tl + L::COL_DPT + c, dpt);
+          const int c = 32 * wg + 16 * hh;  // first query column of this half
+          uint32_t st[16], dpt[16];
+          tmem_ld16(tl + L::COL_ST + c, st);
+          tmem_ld16(tl + L::COL_DPT + c, dpt);
           tmem_ld_wait(st);
-          tie32(dpt);
-          uint32_t pp[16], pd[16];
+          tie16(dpt);
+          uint32_t pp[8], pd[8];
 #pragma unroll
-          for (int i = 0; i < 32; i += 4) {
+          for (int i = 0; i < 16; i += 4) {
             const float4 l4 = *reinterpret_cast<const float4*>(sc + c + i);
             const float4 d4 = *reinterpret_cast<const float4*>(sc + NQ + c + i);
             const int4 q4 = *reinterpret_cast<const int4*>(reinterpret_cast<const int*>(sc) + 2 * NQ + c + i);
             const float ls[4] = {l4.x, l4.y, l4.z, l4.w}, dd[4] = {d4.x, d4.y, d4.z, d4.w};
             const int pq[4] = {q4.x, q4.y, q4.z, q4.w};
-            float pv[4], dv4[4];
+            float pv[4], dv4[4], y[4], tt[4];
+            ffma2(y[0], y[1], __uint_as_float(st[i]), __uint_as_float(st[i + 1]), sl2, sl2, -ls[0], -ls[1]);
+            ffma2(y[2], y[3], __uint_as_float(st[i + 2]), __uint_as_float(st[i + 3]), sl2, sl2, -ls[2], -ls[3]);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int dpos = pq[e] - pj;
-              const bool allowed = row_ok && (LONG ? dpos >= w : (uint32_t)dpos < (uint32_t)w);
-              pv[e] = p_of(__uint_as_float(st[i + e]), sl2, ls[e], allowed);
-              dv4[e] = pv[e] * (__uint_as_float(dpt[i + e]) - dd[e]);
+            for (int e = 0; e < 4; ++e) pv[e] = ex2(y[e]);
+            if (need_mask) {
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int dpos = pq[e] - pj;
+                if (!(LONG ? dpos >= w : (uint32_t)dpos < (uint32_t)w)) pv[e] = 0.0f;
+              }
             }
+            fadd2(tt[0], tt[1], __uint_as_float(dpt[i]), __uint_as_float(dpt[i + 1]), -dd[0], -dd[1]);
+            fadd2(tt[2], tt[3], __uint_as_float(dpt[i + 2]), __uint_as_float(dpt[i + 3]), -dd[2], -dd[3]);
+            fmul2(dv4[0], dv4[1], pv[0], pv[1], tt[0], tt[1]);
+            fmul2(dv4[2], dv4[3], pv[2], pv[3], tt[2], tt[3]);
             pp[i / 2] = pack_bf16(pv[0], pv[1]);
             pp[i / 2 + 1] = pack_bf16(pv[2], pv[3]);
             pd[i / 2] = pack_bf16(dv4[0], dv4[1]);
             pd[i / 2 + 1] = pack_bf16(dv4[2], dv4[3]);
           }
-          tmem_st16(tl + L::COL_ST + 64 * wg + 16 * hh, pp);   // over columns already read
-          tmem_st16(tl + L::COL_DPT + 64 * wg + 16 * hh, pd);
+          tmem_st8(tl + L::COL_ST + 32 * wg + 8 * hh, pp);   // over columns already read
+          tmem_st8(tl + L::COL_DPT + 32 * wg + 8 * hh, pd);
         }
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(b_ds);
       }
       if (!ok) break;
-      // ---- epilogue: dK = scale * (dS^T Q) (warpgroup 0), dV = P^T dO (warpgroup 1) ----
+      // ---- epilogue: dK = scale * (dS^T Q) (warpgroups 0, 1), dV = P^T dO (2, 3) ----
       if (it.n > 0) {
         ok = mbar_wait(b_fin, (uint32_t)((ac - 1) & 1), abort_flag, status, tlim);
         if (!__all_sync(0xffffffffu, ok)) {
@@ -857,12 +908,14 @@ bwd_dkdv(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtenso
         tc_fence_after();
       }
       g += it.n;
-      const int col_acc = wg == 0 ? L::COL_DK : L::COL_DV;
-      const float mul = wg == 0 ? a.scale : 1.0f;
-      float* part = (wg == 0 ? a.dk_w : a.dv_w) + grow * D;
-      bf16* out = (wg == 0 ? a.dk : a.dv) + grow * D;
+      const bool is_k = wg < 2;
+      const int half = (wg & 1) * (D / 2);  // this warpgroup's half of the columns
+      const int col_acc = (is_k ? L::COL_DK : L::COL_DV) + half;
+      const float mul = is_k ? a.scale : 1.0f;
+      float* part = (is_k ? a.dk_w : a.dv_w) + grow * D + half;
+      bf16* out = (is_k ? a.dk : a.dv) + grow * D + half;
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = 0; c < D / 64; ++c) {
         uint32_t y[32];
         if (it.n > 0) {
           tmem_ld32(tl + col_acc + 32 * c, y);
@@ -998,14 +1051,14 @@ cudaError_t launch_persistent(Kernel kernel, int smem, const BwdArgs& a, int n_i
 template <int D>
 cudaError_t launch_pass(const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mq,
                         const CUtensorMap& mdo, const BwdArgs& a, int nq_items, int nk_items,
-                        bool long_pass, cudaStream_t s) {
-  cudaError_t e;
-  if (long_pass) {
-    if ((e = launch_persistent(bwd_dq<D, true>, DqLayout<D>::SMEM, a, nq_items, s, mk, mv))) return e;
-    return launch_persistent(bwd_dkdv<D, true>, DkvLayout<D>::SMEM, a, nk_items, s, mk, mv, mq, mdo);
-  }
-  if ((e = launch_persistent(bwd_dq<D, false>, DqLayout<D>::SMEM, a, nq_items, s, mk, mv))) return e;
-  return launch_persistent(bwd_dkdv<D, false>, DkvLayout<D>::SMEM, a, nk_items, s, mk, mv, mq, mdo);
+                        bool long_pass, bool dq_kernel, cudaStream_t s) {
+  if (long_pass)
+    return dq_kernel
+               ? launch_persistent(bwd_dq<D, true>, DqLayout<D>::SMEM, a, nq_items, s, mk, mv)
+               : launch_persistent(bwd_dkdv<D, true>, DkvLayout<D>::SMEM, a, nk_items, s, mk, mv, mq, mdo);
+  return dq_kernel
+             ? launch_persistent(bwd_dq<D, false>, DqLayout<D>::SMEM, a, nq_items, s, mk, mv)
+             : launch_persistent(bwd_dkdv<D, false>, DkvLayout<D>::SMEM, a, nk_items, s, mk, mv, mq, mdo);
 }
 
 }  // namespace
@@ -1035,7 +1088,8 @@ cudaError_t launch_permute_rows(const focus_params& p, const WsLayout& L, const 
 
 cudaError_t launch_attn_bwd(const focus_params& p, const BwdPlan& bp, const bf16* q, const bf16* k,
                             const bf16* v, const bf16* d_o, const float* lse, bf16* dq, bf16* dk,
-                            bf16* dv, char* ws, float scale, bool long_pass, cudaStream_t s) {
+                            bf16* dv, char* ws, float scale, bool long_pass, bool dq_kernel,
+                            cudaStream_t s) {
   const WsLayout& L = bp.L;
   BwdArgs a{};
   a.B = p.B;
@@ -1093,8 +1147,8 @@ cudaError_t launch_attn_bwd(const focus_params& p, const BwdPlan& bp, const bf16
     nq_items = L.qtab_cap * (p.H / p.R);
     nk_items = L.qtab_cap * (p.H_kv / p.R);
   }
-  return D == 64 ? launch_pass<64>(mk, mv, mq, mdo, a, nq_items, nk_items, long_pass, s)
-                 : launch_pass<128>(mk, mv, mq, mdo, a, nq_items, nk_items, long_pass, s);
+  return D == 64 ? launch_pass<64>(mk, mv, mq, mdo, a, nq_items, nk_items, long_pass, dq_kernel, s)
+                 : launch_pass<128>(mk, mv, mq, mdo, a, nq_items, nk_items, long_pass, dq_kernel, s);
 }
 
 }  // namespace focus

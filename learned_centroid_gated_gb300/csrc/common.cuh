@@ -106,7 +106,8 @@ cudaError_t launch_permute_rows(const focus_params& p, const WsLayout& L, const 
                                 const char* ws, cudaStream_t s);
 cudaError_t launch_attn_bwd(const focus_params& p, const BwdPlan& bp, const bf16* q, const bf16* k,
                             const bf16* v, const bf16* d_o, const float* lse, bf16* dq, bf16* dk,
-                            bf16* dv, char* ws, float scale, bool long_pass, cudaStream_t s);
+                            bf16* dv, char* ws, float scale, bool long_pass, bool dq_kernel,
+                            cudaStream_t s);
 // decode.cu
 int decode_chunks(int N);
 size_t decode_workspace_bytes(const focus_params& p);

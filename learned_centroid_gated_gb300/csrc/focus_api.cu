@@ -428,10 +428,10 @@ size_t focus_bwd_workspace_size(const focus_params* p) {
   return bwd_layout(*p).L.total;
 }
 
-int focus_attn_bwd(const focus_params* p, const uint16_t* q, const uint16_t* k, const uint16_t* v,
-                   const uint32_t* mask, const uint16_t* o, const float* lse, const uint16_t* d_o,
-                   uint16_t* dq, uint16_t* dk, uint16_t* dv, void* ws, size_t ws_bytes,
-                   void* stream) {
+int focus_attn_bwd_ev(const focus_params* p, const uint16_t* q, const uint16_t* k,
+                      const uint16_t* v, const uint32_t* mask, const uint16_t* o, const float* lse,
+                      const uint16_t* d_o, uint16_t* dq, uint16_t* dk, uint16_t* dv, void* ws,
+                      size_t ws_bytes, void* stream, void* const* stage_events) {
   int rc = check_bwd_params(p);
   if (rc) return rc;
   if (!q || !k || !v || !mask || !o || !lse || !d_o || !dq || !dk || !dv)
@@ -450,6 +450,18 @@ int focus_attn_bwd(const focus_params* p, const uint16_t* q, const uint16_t* k, 
   const bf16* kb = reinterpret_cast<const bf16*>(k);
   const bf16* vb = reinterpret_cast<const bf16*>(v);
   const bf16* gb = reinterpret_cast<const bf16*>(d_o);
+  bf16* dqb = reinterpret_cast<bf16*>(dq);
+  bf16* dkb = reinterpret_cast<bf16*>(dk);
+  bf16* dvb = reinterpret_cast<bf16*>(dv);
+  auto mark = [&](int i) -> int {
+    if (!stage_events) return FOCUS_OK;
+    return cuda_rc(cudaEventRecord((cudaEvent_t)stage_events[i], s));
+  };
+  auto pass = [&](bool long_pass, bool dq_kernel) {
+    return cuda_rc(launch_attn_bwd(*p, bp, qb, kb, vb, gb, lse, dqb, dkb, dvb, w, scale, long_pass,
+                                   dq_kernel, s));
+  };
+  if ((rc = mark(0))) return rc;
   if ((rc = cuda_rc(reset_header(w, s)))) return rc;
   if ((rc = cuda_rc(launch_bucket(*p, L, mask, w, s)))) return rc;
   if ((rc = cuda_rc(launch_qtab(*p, L, w, kBwdBlock, s)))) return rc;
@@ -464,12 +476,20 @@ int focus_attn_bwd(const focus_params* p, const uint16_t* q, const uint16_t* k, 
   if ((rc = cuda_rc(launch_bwd_rowdot(*p, reinterpret_cast<const bf16*>(o), gb,
                                       reinterpret_cast<float*>(w + bp.dvec), s))))
     return rc;
-  bf16* dqb = reinterpret_cast<bf16*>(dq);
-  bf16* dkb = reinterpret_cast<bf16*>(dk);
-  bf16* dvb = reinterpret_cast<bf16*>(dv);
-  if ((rc = cuda_rc(launch_attn_bwd(*p, bp, qb, kb, vb, gb, lse, dqb, dkb, dvb, w, scale, false, s))))
-    return rc;
-  return cuda_rc(launch_attn_bwd(*p, bp, qb, kb, vb, gb, lse, dqb, dkb, dvb, w, scale, true, s));
+  if ((rc = mark(1))) return rc;
+  if ((rc = pass(false, true)) || (rc = pass(false, false))) return rc;
+  if ((rc = mark(2))) return rc;
+  if ((rc = pass(true, true))) return rc;
+  if ((rc = mark(3))) return rc;
+  if ((rc = pass(true, false))) return rc;
+  return mark(4);
+}
+
+int focus_attn_bwd(const focus_params* p, const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                   const uint32_t* mask, const uint16_t* o, const float* lse, const uint16_t* d_o,
+                   uint16_t* dq, uint16_t* dk, uint16_t* dv, void* ws, size_t ws_bytes,
+                   void* stream) {
+  return focus_attn_bwd_ev(p, q, k, v, mask, o, lse, d_o, dq, dk, dv, ws, ws_bytes, stream, nullptr);
 }
 
 size_t focus_decode_workspace_size(const focus_params* p) {
