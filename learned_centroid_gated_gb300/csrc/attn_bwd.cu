@@ -568,14 +568,21 @@ bwd_dq(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorM
           break;
         }
         tc_fence_after();
+        uint32_t sv[2][16], dpv[2][16];  // both halves loaded before one wait
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          tmem_ld16(tl + L::COL_S + 32 * wg + 16 * hh, sv[hh]);
+          tmem_ld16(tl + L::COL_DP + 32 * wg + 16 * hh, dpv[hh]);
+        }
+        tmem_ld_wait(sv[0]);
+        tie16(sv[1]);
+        tie16(dpv[0]);
+        tie16(dpv[1]);
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
           const int c = 32 * wg + 16 * hh;  // first key column of this half
-          uint32_t s[16], dp[16];
-          tmem_ld16(tl + L::COL_S + c, s);
-          tmem_ld16(tl + L::COL_DP + c, dp);
-          tmem_ld_wait(s);
-          tie16(dp);
+          const uint32_t(&s)[16] = sv[hh];
+          const uint32_t(&dp)[16] = dpv[hh];
           uint32_t pk[8];
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
