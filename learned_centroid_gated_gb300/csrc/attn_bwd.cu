@@ -15,16 +15,16 @@
 // atomics, so the result is deterministic.  Every tensor-core product has N = 128
 // (narrower products ran at a fraction of the rate), so each kernel keeps one
 // 128 x 128 tile of S and dP in TMEM at a time:
-//   bwd_dq<D, LONG>    query-major: 128 query rows of one head per item.  Their Q
-//                      and dO rows are staged in TMEM as the A operands; per
-//                      128-key tile: S = Q K^T and dP = dO V^T, dS (bf16) written
-//                      over S by the elementwise warps, dQ += dS K; the tensor
-//                      core runs dQ(t), S(t+1), dP(t+1) back to back.
+//   bwd_dq<D, LONG>    query-major: 128 query rows of one head per item (Q resident
+//                      in shared memory, dO staged in TMEM); per 128-key tile:
+//                      S = Q K^T and dP = dO V^T; the warps read them (and release
+//                      them at once, so the next tile's S and dP are computed
+//                      meanwhile), write dS (bf16) to TMEM, dQ += dS K.
 //   bwd_dkdv<D, LONG>  key-major: 128 key rows of one KV head per item (K and V
 //                      resident in shared memory), every query head of its group;
 //                      per 128-query tile: S^T = K Q^T, dP^T = V dO^T, P^T and dS^T
 //                      (bf16) written over them, dV += P^T dO, dK += dS^T Q.
-// TMEM (512 columns): dQ kernel Q | dO | S | dP | dQ, dK/dV kernel S^T | dP^T | dK | dV.
+// TMEM (512 columns): dQ kernel S | dP | dS | dO | dQ, dK/dV kernel S^T | dP^T | dK | dV.
 // The window pass writes fp32 partials; the long-range pass adds them and writes
 // the bf16 gradients (the two key sets are disjoint, so the sums are the totals).
 //
@@ -55,13 +55,14 @@ constexpr uint32_t TMEM_COLS = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kMinSmem = 116 * 1024;  // > half the SM's shared memory: one CTA per SM
 
-// Barrier block shared by both kernels: full[NST], empty[NST], then sdp, ds, a,
-// fin, drain, kv_full, kv_empty (8 bytes each), the TMEM address word and the
-// abort flag.
+// Barrier block shared by both kernels: full[NST], empty[NST], then sdp, ds, dqc,
+// rd, a, fin, drain, kv_full, kv_empty (8 bytes each), the TMEM address word and
+// the abort flag.  (In bwd_dq kv_full / kv_empty guard the item's Q tile.)
 template <int NST>
 struct Bars {
-  static constexpr int FULL = 0, EMPTY = 8 * NST, SDP = 16 * NST, DS = SDP + 8, A = DS + 8;
-  static constexpr int FIN = A + 8, DRAIN = FIN + 8, KVF = DRAIN + 8, KVE = KVF + 8;
+  static constexpr int FULL = 0, EMPTY = 8 * NST, SDP = 16 * NST, DS = SDP + 8, DQC = DS + 8;
+  static constexpr int RD = DQC + 8, A = RD + 8, FIN = A + 8, DRAIN = FIN + 8, KVF = DRAIN + 8;
+  static constexpr int KVE = KVF + 8;
   static constexpr int TMEM_SLOT = KVE + 8, ABORT = TMEM_SLOT + 4;
   static constexpr int BYTES = 256;
   static_assert(ABORT + 4 <= BYTES, "barrier block overflow");
@@ -72,12 +73,15 @@ constexpr int BOX = 128 * 128;  // one TMA box: 128 rows x 128 bytes (64 bf16)
 template <int D>
 struct DqLayout {
   static constexpr int NST = 3;
-  static constexpr int TILE = (D / 64) * BOX;    // one 128-key tile of K or V
-  static constexpr int RING = 0;                 // [NST][K tile, V tile]
+  static constexpr int TILE = (D / 64) * BOX;    // one 128-row tile of Q, K or V
+  static constexpr int QT = 0;                   // the item's Q tile
+  static constexpr int RING = QT + TILE;         // [NST][K tile, V tile]
   static constexpr int BAR = RING + NST * 2 * TILE;
   static constexpr int SMEM = BAR + Bars<NST>::BYTES + 1024;
   static_assert(SMEM <= 232448, "shared memory budget");
-  static constexpr int COL_Q = 0, COL_DO = D / 2, COL_S = D, COL_DP = D + NK, COL_DQ = D + 2 * NK;
+  // S | dP | dS (bf16 pairs) | dO (bf16 pairs, A operand of dP) | dQ
+  static constexpr int COL_S = 0, COL_DP = NK, COL_DS = 2 * NK, COL_DO = 2 * NK + NK / 2;
+  static constexpr int COL_DQ = COL_DO + D / 2;
   static_assert(COL_DQ + D <= (int)TMEM_COLS, "tensor memory budget");
 };
 
@@ -380,6 +384,8 @@ __device__ __forceinline__ void init_cta(uint8_t* bar, int warp, uint32_t full_c
     }
     mbar_init(base + BB::SDP, 1);
     mbar_init(base + BB::DS, EW_THREADS);
+    mbar_init(base + BB::DQC, 1);
+    mbar_init(base + BB::RD, EW_THREADS);
     mbar_init(base + BB::A, EW_THREADS);
     mbar_init(base + BB::FIN, 1);
     mbar_init(base + BB::DRAIN, 1);
@@ -395,9 +401,14 @@ __device__ __forceinline__ void init_cta(uint8_t* bar, int warp, uint32_t full_c
 }
 
 // ================================================================ dQ kernel ==
+// Per 128-key tile t: the tensor core computes S(t), dP(t); the warps load them
+// (and signal "read" at once, so S(t+1), dP(t+1) can overwrite them), form
+// dS(t) = P (dP - D) and, once dQ(t-1) has consumed the previous one, store it as
+// bf16; then dQ += dS(t) K(t).
 template <int D, bool LONG>
 __global__ void __launch_bounds__(NTHREADS, 1)
 bwd_dq(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv,
+       const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mdo,
        const BwdArgs a, const int n_items) {
   using L = DqLayout<D>;
   using BB = Bars<L::NST>;
@@ -408,7 +419,9 @@ bwd_dq(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorM
   uint8_t* bar = sm + L::BAR;
   const uint32_t bb = smem_u32(bar);
   const uint32_t b_full = bb + BB::FULL, b_empty = bb + BB::EMPTY, b_sdp = bb + BB::SDP;
-  const uint32_t b_ds = bb + BB::DS, b_a = bb + BB::A, b_fin = bb + BB::FIN, b_drain = bb + BB::DRAIN;
+  const uint32_t b_ds = bb + BB::DS, b_rd = bb + BB::RD, b_a = bb + BB::A, b_fin = bb + BB::FIN;
+  const uint32_t b_dqc = bb + BB::DQC;
+  const uint32_t b_drain = bb + BB::DRAIN, b_qf = bb + BB::KVF, b_qe = bb + BB::KVE;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bar + BB::ABORT);
   init_cta<NST>(bar, warp, 1);
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(bar + BB::TMEM_SLOT);
@@ -419,13 +432,26 @@ bwd_dq(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorM
     if (lane == 0) {
       tma_prefetch(&mk);
       tma_prefetch(&mv);
+      tma_prefetch(&mq);
       int last_par[NST];
       for (int s = 0; s < NST; ++s) last_par[s] = -1;
-      int g = 0;
+      int g = 0, qc = 0, q_par = -1;
       bool ok = true;
       for (int x = blockIdx.x; ok && x < n_items; x += gridDim.x) {
         const BItem it = dq_item<LONG>(a, x);
         if (!it.valid || it.n == 0) continue;
+        // the item's Q rows, once the previous item's products are done
+        if (!(ok = mbar_wait(b_qe, (uint32_t)((qc & 1) ^ 1), abort_flag, status, tlim))) break;
+        mbar_expect_tx(b_qf, L::TILE);
+        for (int bx = 0; bx < D / 64; ++bx) {
+          const uint32_t dst = smem_u32(sm + L::QT + bx * BOX);
+          if constexpr (LONG)
+            tma_load_2d(dst, &mq, 64 * bx, (it.b * a.H + it.h) * a.NR + it.row0, b_qf);
+          else
+            tma_load_3d(dst, &mq, 64 * bx, it.h, it.b * a.N + it.row0, b_qf);
+        }
+        q_par = qc & 1;
+        ++qc;
         DqWalk wk;
         wk.init(a, it, LONG);
         for (int t = 0; t < it.n && ok; ++t, ++g) {
@@ -449,15 +475,18 @@ bwd_dq(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorM
           last_par[slot] = (int)par;
         }
       }
-      if (*abort_flag)
+      if (*abort_flag) {
+        if (q_par >= 0) mbar_drain(b_qf, (uint32_t)q_par);
         for (int s = 0; s < NST; ++s)
           if (last_par[s] >= 0) mbar_drain(b_full + 8 * s, (uint32_t)last_par[s]);
+      }
     }
     __syncwarp();
   } else if (warp == MMA_WARP) {
     if (lane == 0) {
       constexpr uint32_t ISD = idesc_bf16(128, NK, 0);  // S = Q K^T, dP = dO V^T
       constexpr uint32_t IDQ = idesc_bf16(128, D, 1);   // dQ += dS K (K MN-major)
+      const uint32_t q_base = smem_u32(sm + L::QT);
       const uint32_t r_base = smem_u32(sm + L::RING);
       auto kaddr = [&](int g) { return r_base + (g % NST) * 2 * L::TILE; };
       auto ring_wait = [&](int g) {
@@ -468,44 +497,51 @@ bwd_dq(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorM
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk / 4) * BOX + (kk % 4) * 32;
-          umma_ts(tmem + L::COL_S, tmem + L::COL_Q + 8 * kk, sw128_desc(ka + off, 16, 1024), ISD, kk > 0);
+          umma_ss(tmem + L::COL_S, sw128_desc(q_base + off, 16, 1024), sw128_desc(ka + off, 16, 1024), ISD,
+                  kk > 0);
         }
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk / 4) * BOX + (kk % 4) * 32;
-          umma_ts(tmem + L::COL_DP, tmem + L::COL_DO + 8 * kk, sw128_desc(va + off, 16, 1024), ISD,
-                  kk > 0);
+          umma_ts(tmem + L::COL_DP, tmem + L::COL_DO + 8 * kk, sw128_desc(va + off, 16, 1024), ISD, kk > 0);
         }
         umma_commit(b_sdp);
       };
-      int g = 0, ac = 0;
+      int g = 0, ac = 0, qc = 0;
       bool ok = true;
       for (int x = blockIdx.x; ok && x < n_items; x += gridDim.x) {
         const BItem it = dq_item<LONG>(a, x);
         if (!it.valid || it.n == 0) continue;
-        if (!(ok = mbar_wait(b_a, (uint32_t)(ac & 1), abort_flag, status, tlim) && ring_wait(g))) break;
+        // Q landed; the warps staged dO (and read the previous item's dQ)
+        if (!(ok = mbar_wait(b_qf, (uint32_t)(qc & 1), abort_flag, status, tlim) &&
+                   mbar_wait(b_a, (uint32_t)(ac & 1), abort_flag, status, tlim) && ring_wait(g)))
+          break;
+        ++qc;
         ++ac;
         tc_fence_after();
         issue_sdp(g);
         for (int t = 0; t < it.n; ++t) {
           const int gc = g + t;
-          if (!(ok = mbar_wait(b_ds, (uint32_t)(gc & 1), abort_flag, status, tlim))) break;
-          tc_fence_after();
-          const uint32_t ka = kaddr(gc);
-          // dS of keys 32w + 2i, 32w + 2i + 1 sits in column 32w + i of the S region
-#pragma unroll
-          for (int kk = 0; kk < NK / 16; ++kk)
-            umma_ts(tmem + L::COL_DQ, tmem + L::COL_S + 32 * (kk >> 1) + 8 * (kk & 1),
-                    sw128_desc(ka + kk * 2048, BOX, 1024), IDQ, (t > 0 || kk > 0) ? 1u : 0u);
-          umma_commit(b_empty + 8 * (gc % NST));
+          // S(gc), dP(gc) are in registers: the next tile's products may overwrite them
+          if (!(ok = mbar_wait(b_rd, (uint32_t)(gc & 1), abort_flag, status, tlim))) break;
           if (t + 1 < it.n) {
             if (!(ok = ring_wait(gc + 1))) break;
             tc_fence_after();
             issue_sdp(gc + 1);
           }
+          if (!(ok = mbar_wait(b_ds, (uint32_t)(gc & 1), abort_flag, status, tlim))) break;
+          tc_fence_after();
+          const uint32_t ka = kaddr(gc);
+#pragma unroll
+          for (int kk = 0; kk < NK / 16; ++kk)
+            umma_ts(tmem + L::COL_DQ, tmem + L::COL_DS + 8 * kk, sw128_desc(ka + kk * 2048, BOX, 1024), IDQ,
+                    (t > 0 || kk > 0) ? 1u : 0u);
+          umma_commit(b_empty + 8 * (gc % NST));
+          umma_commit(b_dqc);
         }
         if (!ok) break;
         umma_commit(b_fin);
+        umma_commit(b_qe);
         g += it.n;
       }
       umma_commit(b_drain);
@@ -530,9 +566,9 @@ bwd_dq(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorM
       const int qp = LONG ? __ldg(P + it.row0 + rr) : it.row0 + rr;
       const int64_t grow = ((int64_t)it.b * a.N + qp) * a.H + it.h;  // [B, N, H] row
       if (it.n > 0) {
-        if (wg < 2) {  // warpgroup 0 stages the Q rows, 1 the dO rows
-          const bf16* src = (wg == 0 ? a.q : a.dout) + grow * D;
-          stage_row<D>(tl + (wg == 0 ? L::COL_Q : L::COL_DO), row_ok ? src : nullptr);
+        // the previous item's dQ has been read and its products are done: stage dO
+        if (wg == 0) {
+          stage_row<D>(tl + L::COL_DO, row_ok ? a.dout + grow * D : nullptr);
           tmem_st_wait();
         }
         tc_fence_before();
@@ -568,7 +604,7 @@ bwd_dq(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorM
           break;
         }
         tc_fence_after();
-        uint32_t sv[2][16], dpv[2][16];  // both halves loaded before one wait
+        uint32_t sv[2][16], dpv[2][16];
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
           tmem_ld16(tl + L::COL_S + 32 * wg + 16 * hh, sv[hh]);
@@ -578,12 +614,17 @@ bwd_dq(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorM
         tie16(sv[1]);
         tie16(dpv[0]);
         tie16(dpv[1]);
+        tc_fence_before();
+        mbar_arrive(b_rd);
+        // dS of keys 2i, 2i + 1 of the tile goes to column i of the dS region
+        const uint32_t dsc = tl + L::COL_DS + 16 * wg;
+        uint32_t pkv[2][8];
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
           const int c = 32 * wg + 16 * hh;  // first key column of this half
           const uint32_t(&s)[16] = sv[hh];
           const uint32_t(&dp)[16] = dpv[hh];
-          uint32_t pk[8];
+          uint32_t(&pk)[8] = pkv[hh];
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             float y0, y1, t0, t1, d0, d1;
@@ -597,8 +638,17 @@ bwd_dq(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorM
             fmul2(d0, d1, p0, p1, t0, t1);
             pk[i] = pack_bf16(d0, d1);
           }
-          tmem_st8(tl + L::COL_S + 32 * wg + 8 * hh, pk);  // over columns already read
         }
+        if (gc > 0) {  // dQ(gc - 1) has read the previous dS
+          ok = mbar_wait(b_dqc, (uint32_t)((gc - 1) & 1), abort_flag, status, tlim);
+          if (!__all_sync(0xffffffffu, ok)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+        }
+        tmem_st8(dsc, pkv[0]);
+        tmem_st8(dsc + 8, pkv[1]);
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(b_ds);
@@ -1061,10 +1111,10 @@ cudaError_t launch_pass(const CUtensorMap& mk, const CUtensorMap& mv, const CUte
                         bool long_pass, bool dq_kernel, cudaStream_t s) {
   if (long_pass)
     return dq_kernel
-               ? launch_persistent(bwd_dq<D, true>, DqLayout<D>::SMEM, a, nq_items, s, mk, mv)
+               ? launch_persistent(bwd_dq<D, true>, DqLayout<D>::SMEM, a, nq_items, s, mk, mv, mq, mdo)
                : launch_persistent(bwd_dkdv<D, true>, DkvLayout<D>::SMEM, a, nk_items, s, mk, mv, mq, mdo);
   return dq_kernel
-             ? launch_persistent(bwd_dq<D, false>, DqLayout<D>::SMEM, a, nq_items, s, mk, mv)
+             ? launch_persistent(bwd_dq<D, false>, DqLayout<D>::SMEM, a, nq_items, s, mk, mv, mq, mdo)
              : launch_persistent(bwd_dkdv<D, false>, DkvLayout<D>::SMEM, a, nk_items, s, mk, mv, mq, mdo);
 }
 
