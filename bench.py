@@ -588,8 +588,9 @@ def run_backward(args):
     stream = torch.cuda.current_stream(dev)
     peaks, peak_src = load_peaks()
     rows = []
-    for name in ("mha7b_32k", "gqa_128k"):
-        wl = synth.WORKLOADS[name]
+    cases = [("mha7b_32k", synth.WORKLOADS["mha7b_32k"]), ("gqa_128k", synth.WORKLOADS["gqa_128k"]),
+             ("mha7b_32k_K32_top4", synth.WORKLOADS["mha7b_32k"].replace(K=32, top_k=4))]
+    for name, wl in cases:
         x = synth.make_inputs(wl, seed=args.seed, device=dev)
         p = focus.Params.from_workload(wl)
         mask, _ = focus.route(p, x["r"], x["C"])
@@ -629,7 +630,9 @@ def run_backward(args):
         tf = lambda flops, ms: flops / (ms / 1e3) / 1e12
         dkdv = tf(8.0 * d * longr, stage["long_dkdv"])
         rows.append({
-            "workload": name, "config": config_of(wl), "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
+            "workload": name, "config": config_of(wl),
+            "schedule": "groups" if p.bucket_shape()[0] == focus.SCHEDULE_GROUPS else "segments",
+            "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
             "bwd_over_fwd": bwd_ms / fwd_ms, "stages_ms": stage,
             "fwd_allowed_pair_tflops": tf(4.0 * d * allowed, fwd_ms),
             "bwd_allowed_pair_tflops": tf(10.0 * d * allowed, bwd_ms),

@@ -265,11 +265,12 @@ int focus_decode(const focus_params* p, const uint16_t* q, const uint16_t* k_cac
  *   lse        [B, H, N] fp32: the forward's LSE
  *   dq         [B, N, H, d_head] bf16 out;  dk, dv [B, N, H_kv, d_head] bf16 out
  *   ws         focus_bwd_workspace_size(p) bytes
- * Runs over exact-set segments whatever p->schedule says (so C(K, top_k) <=
- * FOCUS_MAX_SEGMENTS, else FOCUS_ERR_UNSUPPORTED).  Steps on `stream`: bucket,
- * block schedule and backward plans, permuted copies of Q/K/V/dO, D, then per
- * pass (window, long-range) a query-major dQ kernel and a key-major dK/dV kernel
- * on the tensor cores.  Deterministic: no atomics.
+ * The long-range schedule is chosen as for the forward (focus_bucket_shape).
+ * Steps on `stream`: bucket, block schedule and backward plans, permuted copies
+ * of Q/K/V/dO, D, then per pass (window, long-range) a query-major dQ kernel and
+ * a key-major dK/dV kernel on the tensor cores; with group lists the long-range
+ * pass writes each list's part of a token's gradients to one of top_k slots and a
+ * last kernel sums them with the window part.  Deterministic: no atomics.
  */
 size_t focus_bwd_workspace_size(const focus_params* p);
 int focus_attn_bwd(const focus_params* p, const uint16_t* q, const uint16_t* k, const uint16_t* v,

@@ -55,6 +55,9 @@ constexpr uint32_t TMEM_COLS = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kMinSmem = 116 * 1024;  // > half the SM's shared memory: one CTA per SM
 
+// Kernel modes: window pass, long range over exact-set segments, over group lists.
+enum : int { kWin = 0, kSeg = 1, kGrp = 2 };
+
 // Barrier block shared by both kernels: full[NST], empty[NST], then sdp, ds, dqc,
 // rd, a, fin, drain, kv_full, kv_empty (8 bytes each), the TMEM address word and
 // the abort flag.  (In bwd_dq kv_full / kv_empty guard the item's Q tile.)
@@ -76,7 +79,8 @@ struct DqLayout {
   static constexpr int TILE = (D / 64) * BOX;    // one 128-row tile of Q, K or V
   static constexpr int QT = 0;                   // the item's Q tile
   static constexpr int RING = QT + TILE;         // [NST][K tile, V tile]
-  static constexpr int BAR = RING + NST * 2 * TILE;
+  static constexpr int KM = RING + NST * 2 * TILE;  // group lists: [NST][NK] key masks
+  static constexpr int BAR = KM + NST * NK * 4;
   static constexpr int SMEM = BAR + Bars<NST>::BYTES + 1024;
   static_assert(SMEM <= 232448, "shared memory budget");
   // S | dP | dS (bf16 pairs) | dO (bf16 pairs, A operand of dP) | dQ
@@ -91,8 +95,8 @@ struct DkvLayout {
   static constexpr int TILE = (D / 64) * BOX;    // one 128-row tile of K, V, Q or dO
   static constexpr int KV = 0;                   // K tile, V tile of the item
   static constexpr int RING = KV + 2 * TILE;     // [NST][Q tile, dO tile]
-  static constexpr int SCAL = RING + NST * 2 * TILE;  // [NST][lse2, D, pos][NQ]
-  static constexpr int BAR = SCAL + NST * 3 * NQ * 4;
+  static constexpr int SCAL = RING + NST * 2 * TILE;  // [NST][lse2, D, pos, mask][NQ]
+  static constexpr int BAR = SCAL + NST * 4 * NQ * 4;
   static constexpr int SMEM = BAR + Bars<NST>::BYTES + 1024;
   static_assert(SMEM <= 232448, "shared memory budget");
   static constexpr int COL_ST = 0, COL_DPT = NQ, COL_DK = 2 * NQ, COL_DV = 2 * NQ + D;
@@ -122,13 +126,17 @@ struct BwdArgs {
   bf16* dq;           // gradients, bf16, token order
   bf16* dk;
   bf16* dv;
+  const uint32_t* pmask;  // group lists: mask of each permuted row
+  float* dq_s;            // group lists: [top_k][B, N, H, d] list parts
+  float* dk_s;            // group lists: [top_k][B, N, H_kv, d]
+  float* dv_s;
   int* status;
   long long timeout_cycles;
 };
 
 struct BItem {
   bool valid;
-  int b, h, kvh, br, u, row0, rows;
+  int b, h, kvh, br, u, row0, rows, seg;
   int n;     // tiles
   int nsub;  // dK/dV: tiles per query head
   int lo, hi;
@@ -149,6 +157,7 @@ __device__ __forceinline__ BItem dq_item(const BwdArgs& a, int x) {
     const QBlock e = a.qtab[u];
     it.u = u;
     it.br = e.br;
+    it.seg = e.seg;
     it.b = e.br / a.R;
     it.kvh = (e.br % a.R) * nkv + kvl;
     it.h = it.kvh * gq + jq;
@@ -187,6 +196,7 @@ __device__ __forceinline__ BItem dkv_item(const BwdArgs& a, int x) {
     const QBlock e = a.qtab[u];
     it.u = u;
     it.br = e.br;
+    it.seg = e.seg;
     it.b = e.br / a.R;
     it.kvh = (e.br % a.R) * nkv + kvl;
     it.row0 = e.row0;
@@ -405,11 +415,13 @@ __device__ __forceinline__ void init_cta(uint8_t* bar, int warp, uint32_t full_c
 // (and signal "read" at once, so S(t+1), dP(t+1) can overwrite them), form
 // dS(t) = P (dP - D) and, once dQ(t-1) has consumed the previous one, store it as
 // bf16; then dQ += dS(t) K(t).
-template <int D, bool LONG>
+template <int D, int MODE>
 __global__ void __launch_bounds__(NTHREADS, 1)
 bwd_dq(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv,
        const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mdo,
        const BwdArgs a, const int n_items) {
+  constexpr bool LONG = MODE != kWin;
+  constexpr bool GROUP = MODE == kGrp;
   using L = DqLayout<D>;
   using BB = Bars<L::NST>;
   constexpr int NST = L::NST;
@@ -423,45 +435,58 @@ bwd_dq(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorM
   const uint32_t b_dqc = bb + BB::DQC;
   const uint32_t b_drain = bb + BB::DRAIN, b_qf = bb + BB::KVF, b_qe = bb + BB::KVE;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bar + BB::ABORT);
-  init_cta<NST>(bar, warp, 1);
+  uint32_t* kmask = reinterpret_cast<uint32_t*>(sm + L::KM);  // [NST][NK] (group lists)
+  init_cta<NST>(bar, warp, GROUP ? 2 : 1);
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(bar + BB::TMEM_SLOT);
   int* status = a.status;
   const long long tlim = a.timeout_cycles;
 
   if (warp == PRODUCER_WARP) {
+    // lane 0 waits and issues the copies; with group lists every lane also stages
+    // four keys' masks of the tile
     if (lane == 0) {
       tma_prefetch(&mk);
       tma_prefetch(&mv);
       tma_prefetch(&mq);
-      int last_par[NST];
-      for (int s = 0; s < NST; ++s) last_par[s] = -1;
-      int g = 0, qc = 0, q_par = -1;
-      bool ok = true;
-      for (int x = blockIdx.x; ok && x < n_items; x += gridDim.x) {
-        const BItem it = dq_item<LONG>(a, x);
-        if (!it.valid || it.n == 0) continue;
-        // the item's Q rows, once the previous item's products are done
-        if (!(ok = mbar_wait(b_qe, (uint32_t)((qc & 1) ^ 1), abort_flag, status, tlim))) break;
-        mbar_expect_tx(b_qf, L::TILE);
-        for (int bx = 0; bx < D / 64; ++bx) {
-          const uint32_t dst = smem_u32(sm + L::QT + bx * BOX);
-          if constexpr (LONG)
-            tma_load_2d(dst, &mq, 64 * bx, (it.b * a.H + it.h) * a.NR + it.row0, b_qf);
-          else
-            tma_load_3d(dst, &mq, 64 * bx, it.h, it.b * a.N + it.row0, b_qf);
+    }
+    int last_par[NST];
+    for (int s = 0; s < NST; ++s) last_par[s] = -1;
+    int g = 0, qc = 0, q_par = -1;
+    bool ok = true;
+    for (int x = blockIdx.x; ok && x < n_items; x += gridDim.x) {
+      const BItem it = dq_item<LONG>(a, x);
+      if (!it.valid || it.n == 0) continue;
+      // the item's Q rows, once the previous item's products are done
+      if (lane == 0) {
+        ok = mbar_wait(b_qe, (uint32_t)((qc & 1) ^ 1), abort_flag, status, tlim);
+        if (ok) {
+          mbar_expect_tx(b_qf, L::TILE);
+          for (int bx = 0; bx < D / 64; ++bx) {
+            const uint32_t dst = smem_u32(sm + L::QT + bx * BOX);
+            if constexpr (LONG)
+              tma_load_2d(dst, &mq, 64 * bx, (it.b * a.H + it.h) * a.NR + it.row0, b_qf);
+            else
+              tma_load_3d(dst, &mq, 64 * bx, it.h, it.b * a.N + it.row0, b_qf);
+          }
+          q_par = qc & 1;
         }
-        q_par = qc & 1;
-        ++qc;
-        DqWalk wk;
-        wk.init(a, it, LONG);
-        for (int t = 0; t < it.n && ok; ++t, ++g) {
-          int start, cnt;
-          bool full;
-          wk.next(a, it, LONG, t, start, cnt, full);
-          const int slot = g % NST;
-          const uint32_t par = (uint32_t)((g / NST) & 1);
-          if (!(ok = mbar_wait(b_empty + 8 * slot, par ^ 1, abort_flag, status, tlim))) break;
-          const uint32_t fb = b_full + 8 * slot;
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      ++qc;
+      DqWalk wk;
+      wk.init(a, it, LONG);
+      for (int t = 0; t < it.n; ++t, ++g) {
+        int start, cnt;
+        bool full;
+        wk.next(a, it, LONG, t, start, cnt, full);
+        const int slot = g % NST;
+        const uint32_t par = (uint32_t)((g / NST) & 1);
+        if (lane == 0) ok = mbar_wait(b_empty + 8 * slot, par ^ 1, abort_flag, status, tlim);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        const uint32_t fb = b_full + 8 * slot;
+        if (lane == 0) {
           mbar_expect_tx(fb, 2 * L::TILE);
           for (int kv = 0; kv < 2; ++kv)
             for (int bx = 0; bx < D / 64; ++bx) {
@@ -472,14 +497,24 @@ bwd_dq(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorM
               else
                 tma_load_3d(dst, m, 64 * bx, it.kvh, it.b * a.N + start, fb);
             }
-          last_par[slot] = (int)par;
         }
+        if constexpr (GROUP) {  // masks of the tile's keys (0 past its count)
+          const uint32_t* PM = a.pmask + (int64_t)it.br * a.NR;
+#pragma unroll
+          for (int i = 0; i < NK / 32; ++i) {
+            const int kc = 32 * i + lane;
+            kmask[slot * NK + kc] = kc < cnt ? __ldg(PM + start + kc) : 0u;
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(fb);
+        }
+        last_par[slot] = (int)par;
       }
-      if (*abort_flag) {
-        if (q_par >= 0) mbar_drain(b_qf, (uint32_t)q_par);
-        for (int s = 0; s < NST; ++s)
-          if (last_par[s] >= 0) mbar_drain(b_full + 8 * s, (uint32_t)last_par[s]);
-      }
+    }
+    if (lane == 0 && *abort_flag) {
+      if (q_par >= 0) mbar_drain(b_qf, (uint32_t)q_par);
+      for (int s = 0; s < NST; ++s)
+        if (last_par[s] >= 0) mbar_drain(b_full + 8 * s, (uint32_t)last_par[s]);
     }
     __syncwarp();
   } else if (warp == MMA_WARP) {
@@ -578,6 +613,12 @@ bwd_dq(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorM
       const int64_t li = ((int64_t)it.b * a.H + it.h) * a.N + qp;
       const float lse2 = __ldg(a.lse + li) * kLog2e;
       const float Dr = __ldg(a.dvec + li);
+      // group lists: the row's groups below list g (keys sharing one of them are
+      // counted in a lower list) and its slot
+      uint32_t m_low = 0u;
+      if constexpr (GROUP)
+        m_low = __ldg(a.pmask + (int64_t)it.br * a.NR + it.row0 + rr) & ((1u << it.seg) - 1u);
+      const bool dedup = GROUP && __any_sync(0xffffffffu, m_low != 0u);
       DqWalk wk;
       wk.init(a, it, LONG);
       for (int t = 0; t < it.n; ++t) {
@@ -618,6 +659,14 @@ bwd_dq(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorM
         mbar_arrive(b_rd);
         // dS of keys 2i, 2i + 1 of the tile goes to column i of the dS region
         const uint32_t dsc = tl + L::COL_DS + 16 * wg;
+        const uint32_t* km = kmask + (gc % NST) * NK;
+        if (GROUP && dedup) {  // the tile's key masks (staged with its K and V)
+          ok = mbar_wait(b_full + 8 * (gc % NST), (uint32_t)((gc / NST) & 1), abort_flag, status, tlim);
+          if (!__all_sync(0xffffffffu, ok)) {
+            ok = false;
+            break;
+          }
+        }
         uint32_t pkv[2][8];
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
@@ -633,6 +682,10 @@ bwd_dq(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorM
             if (need_mask) {
               if ((uint32_t)(c + 2 * i - c_lo) >= width) p0 = 0.0f;
               if ((uint32_t)(c + 2 * i + 1 - c_lo) >= width) p1 = 0.0f;
+            }
+            if (GROUP && dedup) {
+              if (m_low & km[c + 2 * i]) p0 = 0.0f;
+              if (m_low & km[c + 2 * i + 1]) p1 = 0.0f;
             }
             fadd2(t0, t1, __uint_as_float(dp[2 * i]), __uint_as_float(dp[2 * i + 1]), -Dr, -Dr);
             fmul2(d0, d1, p0, p1, t0, t1);
@@ -675,7 +728,13 @@ bwd_dq(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorM
 #pragma unroll
           for (int i = 0; i < 16; ++i) y[i] = 0u;
         }
-        if (row_ok) emit16<LONG>(y, a.scale, a.dq_w + grow * D + col, a.dq + grow * D + col);
+        if constexpr (GROUP) {  // list part into the row's slot
+          if (row_ok)
+            emit16<false>(y, a.scale, a.dq_s + (int64_t)__popc(m_low) * a.B * a.N * a.H * D + grow * D + col,
+                          nullptr);
+        } else if (row_ok) {
+          emit16<LONG>(y, a.scale, a.dq_w + grow * D + col, a.dq + grow * D + col);
+        }
       }
       tc_fence_before();
     }
@@ -689,11 +748,13 @@ bwd_dq(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorM
 }
 
 // ============================================================= dK/dV kernel ==
-template <int D, bool LONG>
+template <int D, int MODE>
 __global__ void __launch_bounds__(NTHREADS, 1)
 bwd_dkdv(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv,
          const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mdo,
          const BwdArgs a, const int n_items) {
+  constexpr bool LONG = MODE != kWin;
+  constexpr bool GROUP = MODE == kGrp;
   using L = DkvLayout<D>;
   using BB = Bars<L::NST>;
   constexpr int NST = L::NST;
@@ -706,7 +767,7 @@ bwd_dkdv(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtenso
   const uint32_t b_ds = bb + BB::DS, b_a = bb + BB::A, b_fin = bb + BB::FIN, b_drain = bb + BB::DRAIN;
   const uint32_t b_kvf = bb + BB::KVF, b_kve = bb + BB::KVE;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bar + BB::ABORT);
-  float* scal = reinterpret_cast<float*>(sm + L::SCAL);  // [NST][3][NQ]
+  float* scal = reinterpret_cast<float*>(sm + L::SCAL);  // [NST][4][NQ]
   init_cta<NST>(bar, warp, 2);
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(bar + BB::TMEM_SLOT);
   int* status = a.status;
@@ -771,22 +832,26 @@ bwd_dkdv(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtenso
                 tma_load_3d(dst, m, 64 * bx, h, it.b * a.N + start, fb);
             }
         }
-        // query scalars: LSE * log2(e) (+inf marks "no query"), D, position
-        float* sc = scal + slot * 3 * NQ;
+        // query scalars: LSE * log2(e) (+inf marks "no query"), D, position and,
+        // with group lists, the query's mask
+        float* sc = scal + slot * 4 * NQ;
 #pragma unroll
         for (int i = 0; i < NQ / 32; ++i) {
           const int qc = 32 * i + lane;
           float lse2 = INFINITY, dd = 0.0f;
           int pos = 0;
+          uint32_t qm = 0u;
           if (qc < cnt) {
             pos = LONG ? __ldg(P + start + qc) : start + qc;
             const int64_t li = ((int64_t)it.b * a.H + h) * a.N + pos;
             lse2 = __ldg(a.lse + li) * kLog2e;
             dd = __ldg(a.dvec + li);
+            if constexpr (GROUP) qm = __ldg(a.pmask + (int64_t)it.br * a.NR + start + qc);
           }
           sc[qc] = lse2;
           sc[NQ + qc] = dd;
           reinterpret_cast<int*>(sc)[2 * NQ + qc] = pos;
+          reinterpret_cast<uint32_t*>(sc)[3 * NQ + qc] = qm;
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(fb);
@@ -888,6 +953,12 @@ bwd_dkdv(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtenso
       // last key position of the block (keys ascend in it)
       const int p_hi = LONG ? __ldg(a.perm + (int64_t)it.br * a.NR + it.row0 + it.rows - 1)
                             : it.row0 + it.rows - 1;
+      // group lists: the key's groups below list g (queries sharing one of them count
+      // it in a lower list) and its slot
+      uint32_t m_low = 0u;
+      if constexpr (GROUP)
+        m_low = __ldg(a.pmask + (int64_t)it.br * a.NR + it.row0 + rr) & ((1u << it.seg) - 1u);
+      const bool dedup = GROUP && __any_sync(0xffffffffu, m_low != 0u);
       if (it.n > 0) {
         tc_fence_before();
         mbar_arrive(b_a);  // the previous item's dK, dV have been read
@@ -902,7 +973,7 @@ bwd_dkdv(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtenso
           break;
         }
         tc_fence_after();
-        const float* sc = scal + slot * 3 * NQ;
+        const float* sc = scal + slot * 4 * NQ;
         // every (key, query) pair of the tile allowed?  Queries past the tile's count
         // carry LSE = +inf (P = 0) and keys past the block are never stored, so only
         // the position rule needs a mask: long range, the first (lowest) query
@@ -937,6 +1008,13 @@ bwd_dkdv(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtenso
                 const int dpos = pq[e] - pj;
                 if (!(LONG ? dpos >= w : (uint32_t)dpos < (uint32_t)w)) pv[e] = 0.0f;
               }
+            }
+            if (GROUP && dedup) {
+              const uint4 m4 = *reinterpret_cast<const uint4*>(reinterpret_cast<const uint32_t*>(sc) + 3 * NQ + c + i);
+              if (m_low & m4.x) pv[0] = 0.0f;
+              if (m_low & m4.y) pv[1] = 0.0f;
+              if (m_low & m4.z) pv[2] = 0.0f;
+              if (m_low & m4.w) pv[3] = 0.0f;
             }
             fadd2(tt[0], tt[1], __uint_as_float(dpt[i]), __uint_as_float(dpt[i + 1]), -dd[0], -dd[1]);
             fadd2(tt[2], tt[3], __uint_as_float(dpt[i + 2]), __uint_as_float(dpt[i + 3]), -dd[2], -dd[3]);
@@ -981,7 +1059,15 @@ bwd_dkdv(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtenso
 #pragma unroll
           for (int i = 0; i < 32; ++i) y[i] = 0u;
         }
-        if (row_ok) emit32<LONG>(y, mul, part + 32 * c, out + 32 * c);
+        if constexpr (GROUP) {  // list part into the key's slot
+          if (row_ok) {
+            float* sl = (is_k ? a.dk_s : a.dv_s) + (int64_t)__popc(m_low) * a.B * a.N * a.H_kv * D +
+                        grow * D + half;
+            emit32<false>(y, mul, sl + 32 * c, nullptr);
+          }
+        } else if (row_ok) {
+          emit32<LONG>(y, mul, part + 32 * c, out + 32 * c);
+        }
       }
       tc_fence_before();
     }
@@ -1037,6 +1123,27 @@ permute_rows(int N, int NR, int H, int R, int d, const int* __restrict__ perm,
     const int hh = rho * hq + i / vec, c = i % vec;
     dst[(((int64_t)b * H + hh) * NR + np) * vec + c] = src[(((int64_t)b * N + n) * H + hh) * vec + c];
   }
+}
+
+// Group lists, last step: gradient = window part + the top_k list parts, in bf16.
+// One thread per four values of a row.
+__global__ void __launch_bounds__(256)
+bwd_sum_slots(int64_t n4, int top_k, const float4* __restrict__ win, const float4* __restrict__ slots,
+              uint2* __restrict__ out) {
+  const int64_t x = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (x >= n4) return;
+  float4 acc = __ldg(win + x);
+  for (int s = 0; s < top_k; ++s) {
+    const float4 v = __ldg(slots + s * n4 + x);
+    acc.x += v.x;
+    acc.y += v.y;
+    acc.z += v.z;
+    acc.w += v.w;
+  }
+  uint2 o;
+  o.x = pack_bf16(acc.x, acc.y);
+  o.y = pack_bf16(acc.z, acc.w);
+  out[x] = o;
 }
 
 // ------------------------------------------------------------- host side --
@@ -1105,17 +1212,22 @@ cudaError_t launch_persistent(Kernel kernel, int smem, const BwdArgs& a, int n_i
   return cudaGetLastError();
 }
 
+template <int D, int MODE>
+cudaError_t launch_mode(const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mq,
+                        const CUtensorMap& mdo, const BwdArgs& a, int nq_items, int nk_items,
+                        bool dq_kernel, cudaStream_t s) {
+  return dq_kernel
+             ? launch_persistent(bwd_dq<D, MODE>, DqLayout<D>::SMEM, a, nq_items, s, mk, mv, mq, mdo)
+             : launch_persistent(bwd_dkdv<D, MODE>, DkvLayout<D>::SMEM, a, nk_items, s, mk, mv, mq, mdo);
+}
+
 template <int D>
 cudaError_t launch_pass(const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mq,
                         const CUtensorMap& mdo, const BwdArgs& a, int nq_items, int nk_items,
-                        bool long_pass, bool dq_kernel, cudaStream_t s) {
-  if (long_pass)
-    return dq_kernel
-               ? launch_persistent(bwd_dq<D, true>, DqLayout<D>::SMEM, a, nq_items, s, mk, mv, mq, mdo)
-               : launch_persistent(bwd_dkdv<D, true>, DkvLayout<D>::SMEM, a, nk_items, s, mk, mv, mq, mdo);
-  return dq_kernel
-             ? launch_persistent(bwd_dq<D, false>, DqLayout<D>::SMEM, a, nq_items, s, mk, mv, mq, mdo)
-             : launch_persistent(bwd_dkdv<D, false>, DkvLayout<D>::SMEM, a, nk_items, s, mk, mv, mq, mdo);
+                        bool long_pass, bool group, bool dq_kernel, cudaStream_t s) {
+  if (!long_pass) return launch_mode<D, kWin>(mk, mv, mq, mdo, a, nq_items, nk_items, dq_kernel, s);
+  if (group) return launch_mode<D, kGrp>(mk, mv, mq, mdo, a, nq_items, nk_items, dq_kernel, s);
+  return launch_mode<D, kSeg>(mk, mv, mq, mdo, a, nq_items, nk_items, dq_kernel, s);
 }
 
 }  // namespace
@@ -1179,6 +1291,10 @@ cudaError_t launch_attn_bwd(const focus_params& p, const BwdPlan& bp, const bf16
   a.dq = dq;
   a.dk = dk;
   a.dv = dv;
+  a.pmask = reinterpret_cast<const uint32_t*>(ws + L.pmask);
+  a.dq_s = reinterpret_cast<float*>(ws + bp.dqs);
+  a.dk_s = reinterpret_cast<float*>(ws + bp.dks);
+  a.dv_s = reinterpret_cast<float*>(ws + bp.dvs);
   a.status = &reinterpret_cast<WsHeader*>(ws)->status;
   a.timeout_cycles = kTimeoutCycles;
   const int D = p.d_head;
@@ -1204,8 +1320,25 @@ cudaError_t launch_attn_bwd(const focus_params& p, const BwdPlan& bp, const bf16
     nq_items = L.qtab_cap * (p.H / p.R);
     nk_items = L.qtab_cap * (p.H_kv / p.R);
   }
-  return D == 64 ? launch_pass<64>(mk, mv, mq, mdo, a, nq_items, nk_items, long_pass, dq_kernel, s)
-                 : launch_pass<128>(mk, mv, mq, mdo, a, nq_items, nk_items, long_pass, dq_kernel, s);
+  const bool group = L.group != 0;
+  return D == 64 ? launch_pass<64>(mk, mv, mq, mdo, a, nq_items, nk_items, long_pass, group, dq_kernel, s)
+                 : launch_pass<128>(mk, mv, mq, mdo, a, nq_items, nk_items, long_pass, group, dq_kernel, s);
+}
+
+cudaError_t launch_bwd_merge_slots(const focus_params& p, const BwdPlan& bp, const char* ws, bf16* dq,
+                                   bf16* dk, bf16* dv, cudaStream_t s) {
+  const int64_t nq4 = (int64_t)p.B * p.N * p.H * p.d_head / 4;
+  const int64_t nk4 = (int64_t)p.B * p.N * p.H_kv * p.d_head / 4;
+  auto run = [&](int64_t n4, size_t win, size_t slots, bf16* out) {
+    bwd_sum_slots<<<(unsigned)((n4 + 255) / 256), 256, 0, s>>>(
+        n4, p.top_k, reinterpret_cast<const float4*>(ws + win), reinterpret_cast<const float4*>(ws + slots),
+        reinterpret_cast<uint2*>(out));
+    return cudaGetLastError();
+  };
+  cudaError_t e;
+  if ((e = run(nq4, bp.dqw, bp.dqs, dq))) return e;
+  if ((e = run(nk4, bp.dkw, bp.dks, dk))) return e;
+  return run(nk4, bp.dvw, bp.dvs, dv);
 }
 
 }  // namespace focus

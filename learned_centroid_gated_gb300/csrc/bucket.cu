@@ -371,25 +371,26 @@ build_plan(int N, int NR, int w, int nseg, int group, const int* __restrict__ se
 }
 
 // Backward plans of 128-row block u (segment S, positions p_lo..p_hi), over the
-// compatible segments T in segment order (exact-set schedule):
+// compatible segments T in segment order (exact-set schedule; with group lists the
+// block's own list only):
 //   query-major (dQ):  keys of T with pos <= p_hi - w, in tiles of kBwdKeyTile;
 //                      PlanEnt.nfull = keys with pos <= p_lo - w (need no mask);
 //   key-major (dK, dV): queries of T with pos >= p_lo + w, in tiles of kBwdQryTile.
 // One warp per block; lanes take segments in parallel.
 __global__ void __launch_bounds__(32)
-build_plan_bwd(int N, int w, int nseg, const int* __restrict__ seg_off, const int* __restrict__ perm,
-               const uint32_t* __restrict__ mask, const QBlock* __restrict__ qtab,
-               const int* __restrict__ qtab_count, PlanHead* __restrict__ qheads,
-               PlanEnt* __restrict__ qents, PlanHead* __restrict__ rheads,
-               PlanEnt* __restrict__ rents) {
+build_plan_bwd(int N, int NR, int w, int nseg, int group, const int* __restrict__ seg_off,
+               const int* __restrict__ perm, const uint32_t* __restrict__ mask,
+               const QBlock* __restrict__ qtab, const int* __restrict__ qtab_count,
+               PlanHead* __restrict__ qheads, PlanEnt* __restrict__ qents,
+               PlanHead* __restrict__ rheads, PlanEnt* __restrict__ rents) {
   const int u = blockIdx.x, lane = threadIdx.x;
   if (u >= *qtab_count) return;
   const QBlock e = qtab[u];
-  const int* P = perm + (int64_t)e.br * N;
+  const int* P = perm + (int64_t)e.br * NR;
   const int* SO = seg_off + (int64_t)e.br * (nseg + 1);
   const uint32_t* M = mask + (int64_t)e.br * N;
   const int p_lo = __ldg(P + e.row0), p_hi = __ldg(P + e.row0 + e.rows - 1);
-  const uint32_t mS = __ldg(M + p_lo);
+  const uint32_t mS = group ? 0u : __ldg(M + p_lo);
   PlanEnt* qo = qents + (int64_t)u * nseg;
   PlanEnt* ro = rents + (int64_t)u * nseg;
   int nq = 0, nr = 0, tq = 0, tr = 0;
@@ -399,7 +400,8 @@ build_plan_bwd(int N, int w, int nseg, const int* __restrict__ seg_off, const in
     bool qok = false, rok = false;
     if (T < nseg) {
       const int s0 = __ldg(SO + T), s1 = __ldg(SO + T + 1);
-      if (s1 > s0 && (__ldg(M + __ldg(P + s0)) & mS)) {
+      const bool compatible = group ? T == e.seg : (s1 > s0 && (__ldg(M + __ldg(P + s0)) & mS));
+      if (s1 > s0 && compatible) {
         const int hi = upper_bound_pos(P, s0, s1, p_hi - w) - s0;
         if (hi > 0) {
           qok = true;
@@ -527,7 +529,8 @@ cudaError_t launch_permute(const focus_params& p, const WsLayout& L, const bf16*
 cudaError_t launch_plan_bwd(const focus_params& p, const WsLayout& L, const uint32_t* mask, char* ws,
                             PlanHead* qheads, PlanEnt* qents, PlanHead* rheads, PlanEnt* rents,
                             cudaStream_t s) {
-  build_plan_bwd<<<L.qtab_cap, 32, 0, s>>>(p.N, p.w, L.nseg, reinterpret_cast<const int*>(ws + L.segoff),
+  build_plan_bwd<<<L.qtab_cap, 32, 0, s>>>(p.N, L.NR, p.w, L.nseg, L.group,
+                                           reinterpret_cast<const int*>(ws + L.segoff),
                                            reinterpret_cast<const int*>(ws + L.perm), mask,
                                            reinterpret_cast<const QBlock*>(ws + L.qtab),
                                            &reinterpret_cast<const WsHeader*>(ws)->qtab_count,

@@ -64,6 +64,7 @@ struct WsLayout {
 struct BwdPlan {
   WsLayout L;
   size_t qhead, qent, rhead, rent, dop, dvec, dqw, dkw, dvw;
+  size_t dqs, dks, dvs;  // group lists: [top_k][...] fp32 list parts of dq, dk, dv
 };
 
 // Binomial coefficient C(n, r) for n <= 32 (fits uint32 for all r).
@@ -108,6 +109,8 @@ cudaError_t launch_attn_bwd(const focus_params& p, const BwdPlan& bp, const bf16
                             const bf16* v, const bf16* d_o, const float* lse, bf16* dq, bf16* dk,
                             bf16* dv, char* ws, float scale, bool long_pass, bool dq_kernel,
                             cudaStream_t s);
+cudaError_t launch_bwd_merge_slots(const focus_params& p, const BwdPlan& bp, const char* ws, bf16* dq,
+                                   bf16* dk, bf16* dv, cudaStream_t s);
 // decode.cu
 int decode_chunks(int N);
 size_t decode_workspace_bytes(const focus_params& p);

@@ -91,27 +91,20 @@ WsLayout layout(const focus_params& p) {
   return L;
 }
 
-// Backward: exact-set segments over 128-row blocks (the gradients do not depend on
-// the schedule; the group-list form is not built for the backward).
-int check_bwd_params(const focus_params* p) {
-  const int rc = check_params(p);
-  if (rc) return rc;
-  if (binom(p->K, p->top_k) > (uint32_t)FOCUS_MAX_SEGMENTS) return FOCUS_ERR_UNSUPPORTED;
-  const int64_t rows = (int64_t)p->B * (p->H > p->R ? p->H : p->R) * p->N;
-  if (rows >= (int64_t)INT32_MAX) return FOCUS_ERR_UNSUPPORTED;
-  return FOCUS_OK;
-}
+// Backward: the same schedule choice as the forward (exact-set segments or group
+// lists) over 128-row blocks.
+int check_bwd_params(const focus_params* p) { return check_params(p); }
 
 BwdPlan bwd_layout(const focus_params& p) {
   BwdPlan bp{};
   WsLayout& L = bp.L;
   const int BR = p.B * p.R;
-  L.group = 0;
-  L.nseg = (int)binom(p.K, p.top_k);
-  L.NR = p.N;
+  L.group = use_groups(p) ? 1 : 0;
+  L.nseg = L.group ? p.K : (int)binom(p.K, p.top_k);
+  L.NR = L.group ? p.N * p.top_k : p.N;
   L.nchunk = (p.N + kChunk - 1) / kChunk;
   L.nblk_sk = (p.N + 255) / 256;
-  L.qtab_cap = BR * ((p.N + kBwdBlock - 1) / kBwdBlock + L.nseg);
+  L.qtab_cap = BR * ((L.NR + kBwdBlock - 1) / kBwdBlock + L.nseg);
   const size_t A = 256;
   size_t off = 0;
   auto take = [&](size_t bytes) {
@@ -120,25 +113,31 @@ BwdPlan bwd_layout(const focus_params& p) {
     return at;
   };
   const size_t BHN = (size_t)p.B * p.H * p.N, BKN = (size_t)p.B * p.H_kv * p.N;
+  const size_t rep = L.group ? (size_t)p.top_k : 1;  // permuted rows per token
   L.hdr = take(sizeof(WsHeader));
   L.hist = take(sizeof(int) * (size_t)BR * L.nchunk * L.nseg);
   L.segoff = take(sizeof(int) * (size_t)BR * (L.nseg + 1));
   L.cbase = take(sizeof(int) * (size_t)BR * L.nchunk * L.nseg);
   L.perm = take(sizeof(int) * (size_t)BR * L.NR);
+  L.pmask = take(L.group ? sizeof(uint32_t) * (size_t)BR * L.NR : 0);
   L.entoff = take(sizeof(int) * ((size_t)BR * L.nseg + 1));
   L.qtab = take(sizeof(QBlock) * (size_t)L.qtab_cap);
-  L.qp = take(sizeof(uint16_t) * BHN * p.d_head);
-  L.kp = take(sizeof(uint16_t) * BKN * p.d_head);
-  L.vp = take(sizeof(uint16_t) * BKN * p.d_head);
+  L.qp = take(sizeof(uint16_t) * BHN * rep * p.d_head);
+  L.kp = take(sizeof(uint16_t) * BKN * rep * p.d_head);
+  L.vp = take(sizeof(uint16_t) * BKN * rep * p.d_head);
   bp.qhead = take(sizeof(PlanHead) * (size_t)L.qtab_cap);
   bp.qent = take(sizeof(PlanEnt) * (size_t)L.qtab_cap * L.nseg);
   bp.rhead = take(sizeof(PlanHead) * (size_t)L.qtab_cap);
   bp.rent = take(sizeof(PlanEnt) * (size_t)L.qtab_cap * L.nseg);
-  bp.dop = take(sizeof(uint16_t) * BHN * p.d_head);
+  bp.dop = take(sizeof(uint16_t) * BHN * rep * p.d_head);
   bp.dvec = take(sizeof(float) * BHN);
   bp.dqw = take(sizeof(float) * BHN * p.d_head);
   bp.dkw = take(sizeof(float) * BKN * p.d_head);
   bp.dvw = take(sizeof(float) * BKN * p.d_head);
+  const size_t slots = L.group ? (size_t)p.top_k : 0;
+  bp.dqs = take(sizeof(float) * slots * BHN * p.d_head);
+  bp.dks = take(sizeof(float) * slots * BKN * p.d_head);
+  bp.dvs = take(sizeof(float) * slots * BKN * p.d_head);
   L.total = off;
   return bp;
 }
@@ -482,6 +481,7 @@ int focus_attn_bwd_ev(const focus_params* p, const uint16_t* q, const uint16_t* 
   if ((rc = pass(true, true))) return rc;
   if ((rc = mark(3))) return rc;
   if ((rc = pass(true, false))) return rc;
+  if (L.group && (rc = cuda_rc(launch_bwd_merge_slots(*p, bp, w, dqb, dkb, dvb, s)))) return rc;
   return mark(4);
 }
 

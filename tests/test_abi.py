@@ -140,7 +140,8 @@ def test_backward_sizes_and_argument_errors():
     n = focus.bwd_workspace_size(p)
     # permuted Q, K, V, dO (bf16) + fp32 window partials of dq, dk, dv + D
     assert n >= (4 * 2 + 3 * 4) * p.N * p.H * p.d_head + 4 * p.N * p.H
-    assert focus.bwd_workspace_size(_params(K=32, top_k=4)) == 0      # 35960 sets: no segments
+    assert focus.bwd_workspace_size(_params(K=32, top_k=4)) > n       # group lists: top_k-fold rows
+    assert focus.bwd_workspace_size(_params(K=32, top_k=4, schedule=focus.SCHEDULE_SEGMENTS)) == 0
     assert focus.bwd_workspace_size(_params(d_head=96)) == 0
     E = {v: k for k, v in focus.ERRORS.items()}
     P = ctypes.c_void_p

@@ -51,18 +51,18 @@ def _check(name, g, ref, mag):
     return worst
 
 
-def _inputs(wl, seed):
+def _inputs(wl, seed, schedule=0):
     x = synth.make_inputs(wl, seed=seed, device="cuda")
-    p = focus.Params.from_workload(wl)
+    p = focus.Params.from_workload(wl, schedule=schedule)
     mask, _ = focus.route(p, x["r"], x["C"])
     g = torch.Generator(device="cpu").manual_seed(seed + 100)
     d_o = torch.randn(x["q"].shape, generator=g).to(torch.bfloat16).cuda()
     return x, p, mask, d_o
 
 
-def _run(wl, seed=0):
+def _run(wl, seed=0, schedule=0):
     """GPU forward, then GPU backward."""
-    x, p, mask, d_o = _inputs(wl, seed)
+    x, p, mask, d_o = _inputs(wl, seed, schedule)
     o, lse = focus.attn_fwd(p, x["q"], x["k"], x["v"], mask=mask)
     dq, dk, dv = focus.attn_bwd(p, x["q"], x["k"], x["v"], mask, o, lse, d_o)
     torch.cuda.synchronize()
@@ -82,13 +82,19 @@ SMALL = {
     "many_segments_K32": synth.WORKLOADS["tiny"].replace(N=3000, K=32, top_k=2, w=50),
     "gqa4_R8_small": synth.WORKLOADS["gqa_128k"].replace(N=2048, w=128),
     "gpt2_layer": synth.WORKLOADS["gpt2_layer"],
+    "K16_top3_gqa": synth.WORKLOADS["tiny"].replace(N=1500, H=8, H_kv=2, R=2, d_head=128, K=16,
+                                                    top_k=3, w=100),
 }
 
 
+SCHEDULES = {"segments": focus.SCHEDULE_SEGMENTS, "groups": focus.SCHEDULE_GROUPS}
+
+
+@pytest.mark.parametrize("schedule", list(SCHEDULES))
 @pytest.mark.parametrize("name", list(SMALL))
-def test_backward_kernel_parity_all_rows(name):
+def test_backward_kernel_parity_all_rows(name, schedule):
     wl = SMALL[name]
-    x, p, mask, d_o = _inputs(wl, seed=7)
+    x, p, mask, d_o = _inputs(wl, seed=7, schedule=SCHEDULES[schedule])
     m = mask_np(mask)
     B, N, H, d = x["q"].shape
     o_ref, lse_ref = oracle.attn(x["q"], x["k"], x["v"], m, w=wl.w, scale=p.scale)
@@ -100,7 +106,7 @@ def test_backward_kernel_parity_all_rows(name):
     wq = _check("dq", dq.reshape(B * N, H, d), rq, mq)
     wk = _check("dk", dk.reshape(B * N, wl.H_kv, d), rk, mk)
     wv = _check("dv", dv.reshape(B * N, wl.H_kv, d), rv, mv)
-    print(f"{name}: err/bound dq {wq:.2f} dk {wk:.2f} dv {wv:.2f}")
+    print(f"{name} ({schedule}): err/bound dq {wq:.2f} dk {wk:.2f} dv {wv:.2f}")
 
 
 @pytest.mark.parametrize("name", ["tiny", "routing_per_kv_group_d128_b2", "many_segments_K32",
@@ -149,3 +155,18 @@ def test_backward_full_size_sampled_rows_and_sum_rules():
     adk = dk.double().abs().sum(dim=1)
     assert (sdk.abs() <= 1e-2 * adk + 1e-3).all()
     assert ((sdv - sdo).abs() <= 2e-2 * sdo.abs() + 2.0).all()
+
+
+def test_backward_group_lists_35960_sets_end_to_end():
+    """K = 32, top_k = 4 (35960 exact sets: group lists only), 8K tokens, GQA 8/2,
+    d = 128: GPU forward then GPU backward, every row."""
+    wl = synth.WORKLOADS["tiny"].replace(N=8192, H=8, H_kv=2, R=1, d_head=128, K=32, top_k=4, w=256)
+    x, p, mask, o, lse, d_o, (dq, dk, dv) = _run(wl, seed=9)
+    assert p.bucket_shape()[0] == focus.SCHEDULE_GROUPS
+    rq, rk, rv, mq, mk, mv = oracle.attn_bwd(x["q"], x["k"], x["v"], mask_np(mask), d_o, w=wl.w,
+                                             scale=p.scale, magnitudes=True, d_rel=O_REL_UNITS)
+    B, N, H, d = x["q"].shape
+    wq = _check("dq", dq.reshape(B * N, H, d), rq, mq)
+    wk = _check("dk", dk.reshape(B * N, wl.H_kv, d), rk, mk)
+    wv = _check("dv", dv.reshape(B * N, wl.H_kv, d), rv, mv)
+    print(f"K32 top4 8K end to end: err/bound dq {wq:.2f} dk {wk:.2f} dv {wv:.2f}")
