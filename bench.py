@@ -206,16 +206,16 @@ def config_of(wl):
             "sinkhorn_iters": wl.sinkhorn_iters, "softmax_scale": 1.0 / math.sqrt(wl.d_head)}
 
 
-def traffic_of(kernel_src: str):
+def traffic_of(kernel_src: str, workload: str):
     """Per-launch DRAM bytes of the dominant kernel from a committed ncu summary, if it
-    was taken on the current kernel source (else None)."""
+    was taken on the current kernel source and this workload (else None)."""
     path = os.path.join(ROOT, "profiles", "attn_long_traffic.json")
     if not os.path.exists(path):
         return None
     try:
         d = json.load(open(path))
         h = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()
-        if d.get("source_sha256") == h and d.get("workload") == DEFAULT_WORKLOAD:
+        if d.get("source_sha256") == h and d.get("workload") == workload:
             return d.get("traffic_bytes_per_launch")
     except Exception:
         pass
@@ -293,7 +293,8 @@ def run_focus(args):
     flops = 4.0 * wl.d_head * allowed
     flops_long = 4.0 * wl.d_head * longrange
     # executed tensor-core work (whole 256 x 128 tiles, masked elements included)
-    lt, wt = pairs.executed_tiles(mask_np, wl.w)
+    group_lists = p.bucket_shape()[0] == focus.SCHEDULE_GROUPS
+    lt, wt = pairs.executed_tiles(mask_np, wl.w, group_lists=group_lists)
     tile_flops = 4.0 * wl.d_head * 256 * 128
     exec_long = tile_flops * int(lt.sum()) * heads_per_rho
     exec_win = tile_flops * wt * wl.B * wl.H
@@ -343,14 +344,16 @@ def run_focus(args):
     peaks, peak_src = load_peaks()
     t_long = stage_ms["attn_long"] / 1e3
     achieved = flops_long / t_long / 1e12
+    sched = "kGrp" if group_lists else "kSeg"
     roofline = {
-        "kernel": "attn_tc<128, long> (long-range block-sparse attention, tcgen05)",
+        "kernel": f"attn_tc<{wl.d_head}, {sched}> (long-range block-sparse attention, tcgen05)",
         "bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
         "frac": achieved / peaks["bf16_tflops"],
         "peak_source": f"{peak_src} bf16 dense burst",
         "peak_sustained": peaks["bf16_tflops_sustained"],
         "frac_sustained": achieved / peaks["bf16_tflops_sustained"],
-        "traffic": traffic_of(os.path.join(ROOT, "learned_centroid_gated_gb300", "csrc", "attn_tc.cu")),
+        "traffic": None if group_lists else traffic_of(
+            os.path.join(ROOT, "learned_centroid_gated_gb300", "csrc", "attn_tc.cu"), wl.name),
         "algorithmic_flops_per_launch": flops_long,
         "executed_flops_per_launch": exec_long,
         "tile_efficiency": flops_long / exec_long,

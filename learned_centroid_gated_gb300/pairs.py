@@ -48,19 +48,31 @@ def allowed_flops(mask, w: int, H: int, H_kv: int, d_head: int) -> int:
     return int(4 * d_head * heads_per_rho * cnt.sum())
 
 
-def executed_tiles(mask, w: int, block_rows: int = 256, key_tile: int = 128):
+def executed_tiles(mask, w: int, block_rows: int = 256, key_tile: int = 128,
+                   group_lists: bool = False):
     """Key tiles the tensor-core kernels run, per (b, routing head), for FLOP
     accounting of executed (not just allowed) work: long-range = for every block of
     `block_rows` consecutive rows of one mask value, ceil(keys / key_tile) over each
-    compatible mask value's keys with pos <= (last row's pos) - w; window = for every
-    block of `block_rows` consecutive tokens, ceil(span / key_tile) with span the
-    keys (first row - w, last row].  Returns (long_tiles [B, R], window_tiles)."""
+    compatible mask value's keys with pos <= (last row's pos) - w (with group_lists:
+    blocks of each group's list against that list's keys); window = for every block
+    of `block_rows` consecutive tokens, ceil(span / key_tile) with span the keys
+    (first row - w, last row].  Returns (long_tiles [B, R], window_tiles)."""
     m = np.asarray(mask).astype(np.int64) & 0xFFFFFFFF
     B, R, N = m.shape
     long_t = np.zeros((B, R), np.int64)
     for b in range(B):
         for rho in range(R):
             row = m[b, rho]
+            if group_lists:
+                for g in range(32):
+                    pos = np.nonzero((row >> g) & 1)[0]
+                    if len(pos) == 0:
+                        continue
+                    last = pos[np.minimum(np.arange(block_rows - 1, len(pos) + block_rows - 1,
+                                                    block_rows), len(pos) - 1)]
+                    cnt = np.searchsorted(pos, last - w, side="right")
+                    long_t[b, rho] += int(((cnt + key_tile - 1) // key_tile).sum())
+                continue
             vals, inv = np.unique(row, return_inverse=True)
             pos = [np.nonzero(inv == a)[0] for a in range(len(vals))]
             for a, va in enumerate(vals):
