@@ -1,4 +1,6 @@
-"""Focus centroid-gated sparse attention, forward pass, for GB300 (sm_103a).
+"""Focus centroid-gated sparse attention for GB300 (sm_103a): routing, the forward
+pass (exact-set segments or group lists), decode, and the backward pass with the
+group masks held fixed.
 
 Thin ctypes binding over the C ABI in ``include/focus.h`` (``libfocus.so``, built
 in-tree by ``learned_centroid_gated_gb300.build``). This module only marshals

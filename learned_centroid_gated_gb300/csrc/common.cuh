@@ -40,7 +40,6 @@ constexpr int kKeyTile = 128;     // keys per attention key tile
 constexpr int kChunk = 1024;      // tokens per bucketing chunk (one warp)
 constexpr int kSinkBlock = 256;   // tokens per Sinkhorn partial-reduction block
 constexpr int kAttnBM = 256;      // query rows per long-range work item
-constexpr int kKeySentinel = 0x7fffffff;
 constexpr int kBwdBlock = 128;    // backward: query rows (dQ) or key rows (dK, dV) per item
 constexpr int kBwdKeyTile = 128;  // backward dQ: keys per tile
 constexpr int kBwdQryTile = 128;  // backward dK, dV: queries per tile

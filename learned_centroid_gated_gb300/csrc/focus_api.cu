@@ -57,7 +57,7 @@ WsLayout layout(const focus_params& p) {
   L.nseg = L.group ? p.K : (int)binom(p.K, p.top_k);
   L.NR = L.group ? p.N * p.top_k : p.N;
   L.nchunk = (p.N + kChunk - 1) / kChunk;
-  L.nblk_sk = (p.N + 255) / 256;
+  L.nblk_sk = (p.N + kSinkBlock - 1) / kSinkBlock;
   L.qtab_cap = BR * ((L.NR + kAttnBM - 1) / kAttnBM + L.nseg);
   const size_t A = 256;
   size_t off = 0;
@@ -103,7 +103,7 @@ BwdPlan bwd_layout(const focus_params& p) {
   L.nseg = L.group ? p.K : (int)binom(p.K, p.top_k);
   L.NR = L.group ? p.N * p.top_k : p.N;
   L.nchunk = (p.N + kChunk - 1) / kChunk;
-  L.nblk_sk = (p.N + 255) / 256;
+  L.nblk_sk = (p.N + kSinkBlock - 1) / kSinkBlock;
   L.qtab_cap = BR * ((L.NR + kBwdBlock - 1) / kBwdBlock + L.nseg);
   const size_t A = 256;
   size_t off = 0;
