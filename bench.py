@@ -53,12 +53,13 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target CPU time of the oracle sample")
-    ap.add_argument("--sweep", choices=["table6", "decode", "schedule", "backward"], default=None,
+    ap.add_argument("--sweep", choices=["table6", "decode", "schedule", "backward", "graph"], default=None,
                     help="table6: speedup of Focus over this build's own dense causal mode "
                          "(K=1) across context lengths, K=4 and K=8; decode: one decode step "
                          "per workload; schedule: exact-set segments vs group lists over "
                          "(K, top_k) at 32K tokens; backward: dq, dk, dv with the masks held "
-                         "fixed, per kernel (one JSON line each)")
+                         "fixed, per kernel; graph: eager calls vs one captured CUDA graph "
+                         "on the launch-bound small layers (one JSON line each)")
     return ap.parse_args()
 
 
@@ -652,8 +653,64 @@ def run_backward(args):
                       "l2": "inputs larger than L2, no flush", "rows": rows}), flush=True)
 
 
+# ---------------------------------------------------------------- graph --
+def run_graph(args):
+    """Forward pass on the small layers (launch-bound: nine launches per call), eager
+    against the replay of one captured CUDA graph, same buffers, CUDA events."""
+    import learned_centroid_gated_gb300 as focus
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    rows = []
+    for name in ("tiny", "gpt2_layer"):
+        wl = synth.WORKLOADS[name]
+        p = focus.Params.from_workload(wl)
+        x = synth.make_inputs(wl, seed=args.seed, device=dev)
+        ws = focus.Workspace(dev).get(p)
+        o = torch.empty_like(x["q"])
+        lse = torch.empty(p.B, p.H, p.N, dtype=torch.float32, device=dev)
+        side = torch.cuda.Stream(dev)
+        call = lambda st: focus.attn_fwd(p, x["q"], x["k"], x["v"], x["r"], x["C"], out=o, lse=lse,
+                                         ws=ws, stream=st)
+        side.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(side):
+            for _ in range(3):
+                call(side)
+        torch.cuda.current_stream(dev).wait_stream(side)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            call(torch.cuda.current_stream(dev))
+        stream = torch.cuda.current_stream(dev)
+        steps = 200
+
+        def timed(fn):
+            for _ in range(10):
+                fn()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(steps):
+                fn()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            return e0.elapsed_time(e1) / steps
+
+        eager = timed(lambda: call(stream))
+        replay = timed(graph.replay)
+        rows.append({"workload": name, "config": config_of(wl),
+                     "schedule": "groups" if p.bucket_shape()[0] == focus.SCHEDULE_GROUPS else "segments",
+                     "eager_ms": eager, "graph_ms": replay,
+                     "eager_tokens_per_s": wl.B * wl.N / (eager / 1e3),
+                     "graph_tokens_per_s": wl.B * wl.N / (replay / 1e3)})
+    print(json.dumps({"sweep": "graph", "unit": "ms per forward", "dtype": "bf16", "data": "synthetic",
+                      "rows": rows}), flush=True)
+
+
 def main():
     args = parse_args()
+    if args.sweep == "graph":
+        run_graph(args)
+        return
     if args.sweep == "backward":
         run_backward(args)
         return
