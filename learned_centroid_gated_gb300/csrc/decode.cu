@@ -7,10 +7,12 @@
 // One query row per head is memory-bound work (each allowed key's K and V rows are
 // read once per KV head), so this runs on the CUDA cores, split over the keys:
 //   decode_chunk    one CTA per (chunk of kDecChunk keys, KV head, batch row) and up
-//                   to kDecHeads query heads of that KV head: compacts the allowed keys
-//                   of the chunk (window, or mask overlap), scores them (one thread per
-//                   key, its K row as independent 16-byte loads), and accumulates P V
-//                   (16-byte V loads, several keys in flight); writes (max, sum, acc).
+//                   to NH query heads of that KV head (NH, a template parameter, is the
+//                   GQA ratio rounded down to 1, 2, 4 or 8, so the per-thread arrays fit
+//                   the heads there are): compacts the allowed keys of the chunk
+//                   (window, or mask overlap), scores them (one thread per key, its K
+//                   row as independent 16-byte loads), and accumulates P V (16-byte V
+//                   loads, kDecUnroll batches of keys in flight); writes (max, sum, acc).
 //   decode_combine  merges the chunks of one (batch, head) by their maxima: O, LSE.
 #include <math.h>
 
@@ -21,7 +23,8 @@ namespace {
 
 constexpr int kDecChunk = 256;   // keys per CTA
 constexpr int kDecThreads = 128;
-constexpr int kDecHeads = 8;     // query heads per CTA (of one KV head)
+constexpr int kDecHeads = 8;     // most query heads per CTA (of one KV head)
+constexpr int kDecUnroll = 8;    // P V: batches of keys whose V loads are in flight together
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -31,26 +34,26 @@ __device__ __forceinline__ unsigned lanemask_lt_dec() {
   return r;
 }
 
-template <int D>
+template <int D, int NH>
 __global__ void __launch_bounds__(kDecThreads)
 decode_chunk(int N, int H, int H_kv, int R, int w, float sl2, const bf16* __restrict__ q,
              const bf16* __restrict__ k, const bf16* __restrict__ v,
              const uint32_t* __restrict__ mask, float2* __restrict__ part_ml,
              float* __restrict__ part_acc, int nch) {
-  __shared__ float qs[kDecHeads][D];
+  __shared__ float qs[NH][D];
   __shared__ int idx[kDecChunk];
-  __shared__ float sc[kDecHeads][kDecChunk];
+  __shared__ float sc[NH][kDecChunk];
   __shared__ int wsum[kDecThreads / 32];
-  __shared__ float red[kDecHeads][kDecThreads / 32];
-  __shared__ float stat[kDecHeads];
+  __shared__ float red[NH][kDecThreads / 32];
+  __shared__ float stat[NH];
   __shared__ float accx[kDecThreads / (D / 8)][D];
 
   const int c = blockIdx.x, b = blockIdx.z;
   const int gq = H / H_kv;
-  const int nhg = (gq + kDecHeads - 1) / kDecHeads;
+  const int nhg = (gq + NH - 1) / NH;
   const int kvh = blockIdx.y / nhg, hg = blockIdx.y % nhg;
-  const int h0 = kvh * gq + hg * kDecHeads;
-  const int nh = min(kDecHeads, gq - hg * kDecHeads);
+  const int h0 = kvh * gq + hg * NH;
+  const int nh = min(NH, gq - hg * NH);
   const int rho = kvh / (H_kv / R);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int i = N - 1;
@@ -86,9 +89,9 @@ decode_chunk(int N, int H, int H_kv, int R, int w, float sl2, const bf16* __rest
     uint4 raw[D / 8];
 #pragma unroll
     for (int c8 = 0; c8 < D / 8; ++c8) raw[c8] = __ldg(kr + c8);
-    float s[kDecHeads];
+    float s[NH];
 #pragma unroll
-    for (int hh = 0; hh < kDecHeads; ++hh) s[hh] = 0.0f;
+    for (int hh = 0; hh < NH; ++hh) s[hh] = 0.0f;
 #pragma unroll
     for (int c8 = 0; c8 < D / 8; ++c8) {
       const __nv_bfloat162* p2 = reinterpret_cast<const __nv_bfloat162*>(&raw[c8]);
@@ -96,7 +99,7 @@ decode_chunk(int N, int H, int H_kv, int R, int w, float sl2, const bf16* __rest
       for (int e2 = 0; e2 < 4; ++e2) {
         const float2 f = __bfloat1622float2(p2[e2]);
 #pragma unroll
-        for (int hh = 0; hh < kDecHeads; ++hh) {
+        for (int hh = 0; hh < NH; ++hh) {
           if (hh < nh) {
             s[hh] = fmaf(f.x, qs[hh][c8 * 8 + 2 * e2], s[hh]);
             s[hh] = fmaf(f.y, qs[hh][c8 * 8 + 2 * e2 + 1], s[hh]);
@@ -105,7 +108,7 @@ decode_chunk(int N, int H, int H_kv, int R, int w, float sl2, const bf16* __rest
       }
     }
 #pragma unroll
-    for (int hh = 0; hh < kDecHeads; ++hh)
+    for (int hh = 0; hh < NH; ++hh)
       if (hh < nh) sc[hh][a] = s[hh] * sl2;
   }
   __syncthreads();
@@ -139,29 +142,39 @@ decode_chunk(int N, int H, int H_kv, int R, int w, float sl2, const bf16* __rest
   constexpr int TPR = D / 8;                // threads per row
   constexpr int KPAR = kDecThreads / TPR;   // keys in flight per iteration
   const int seg = tid % TPR, kg = tid / TPR;
-  float acc[kDecHeads][8];
+  float acc[NH][8];
 #pragma unroll
-  for (int hh = 0; hh < kDecHeads; ++hh)
+  for (int hh = 0; hh < NH; ++hh)
 #pragma unroll
     for (int u = 0; u < 8; ++u) acc[hh][u] = 0.0f;
-#pragma unroll 2
-  for (int a = kg; a < na; a += KPAR) {
-    const uint4 raw = __ldg(reinterpret_cast<const uint4*>(
-                                v + (((int64_t)b * N + idx[a]) * H_kv + kvh) * D) + seg);
-    const __nv_bfloat162* p2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
-    float vv[8];
+  const uint4* vbase = reinterpret_cast<const uint4*>(v + ((int64_t)b * N * H_kv + kvh) * D) + seg;
+  const int64_t vstride = (int64_t)H_kv * D / 8;  // uint4 per token
+  for (int a0 = kg; a0 < na; a0 += KPAR * kDecUnroll) {
+    uint4 raw[kDecUnroll];  // the batch's V loads are issued before any is used
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const float2 f = __bfloat1622float2(p2[u]);
-      vv[2 * u] = f.x;
-      vv[2 * u + 1] = f.y;
+    for (int u = 0; u < kDecUnroll; ++u) {
+      const int a = a0 + u * KPAR;
+      raw[u] = a < na ? __ldg(vbase + idx[a] * vstride) : make_uint4(0u, 0u, 0u, 0u);
     }
 #pragma unroll
-    for (int hh = 0; hh < kDecHeads; ++hh) {
-      if (hh < nh) {
-        const float pa = sc[hh][a];
+    for (int u = 0; u < kDecUnroll; ++u) {
+      const int a = a0 + u * KPAR;
+      if (a >= na) break;
+      const __nv_bfloat162* p2 = reinterpret_cast<const __nv_bfloat162*>(&raw[u]);
+      float vv[8];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) acc[hh][u] = fmaf(pa, vv[u], acc[hh][u]);
+      for (int e = 0; e < 4; ++e) {
+        const float2 f = __bfloat1622float2(p2[e]);
+        vv[2 * e] = f.x;
+        vv[2 * e + 1] = f.y;
+      }
+#pragma unroll
+      for (int hh = 0; hh < NH; ++hh) {
+        if (hh < nh) {
+          const float pa = sc[hh][a];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) acc[hh][e] = fmaf(pa, vv[e], acc[hh][e]);
+        }
       }
     }
   }
@@ -242,18 +255,27 @@ cudaError_t launch_decode(const focus_params& p, const bf16* q, const bf16* k, c
                           cudaStream_t s) {
   const int nch = decode_chunks(p.N);
   const int gq = p.H / p.H_kv;
-  const int nhg = (gq + kDecHeads - 1) / kDecHeads;
+  const int nh = gq >= 8 ? 8 : gq >= 4 ? 4 : gq >= 2 ? 2 : 1;  // query heads per CTA
+  const int nhg = (gq + nh - 1) / nh;
   float2* part_ml = reinterpret_cast<float2*>(ws);
   float* part_acc = reinterpret_cast<float*>(ws + align_up(sizeof(float2) * (size_t)p.B * p.H * nch, 256));
   dim3 grid(nch, p.H_kv * nhg, p.B);
   const float sl2 = scale * kLog2e;
+  auto chunk = [&](auto kernel) {
+    kernel<<<grid, kDecThreads, 0, s>>>(p.N, p.H, p.H_kv, p.R, p.w, sl2, q, k, v, mask, part_ml,
+                                        part_acc, nch);
+  };
   if (p.d_head == 64) {
-    decode_chunk<64><<<grid, kDecThreads, 0, s>>>(p.N, p.H, p.H_kv, p.R, p.w, sl2, q, k, v, mask,
-                                                  part_ml, part_acc, nch);
+    if (nh == 8) chunk(decode_chunk<64, 8>);
+    else if (nh == 4) chunk(decode_chunk<64, 4>);
+    else if (nh == 2) chunk(decode_chunk<64, 2>);
+    else chunk(decode_chunk<64, 1>);
     decode_combine<64><<<p.B * p.H, kCombThreads, 0, s>>>(p.H, nch, part_ml, part_acc, o, lse);
   } else {
-    decode_chunk<128><<<grid, kDecThreads, 0, s>>>(p.N, p.H, p.H_kv, p.R, p.w, sl2, q, k, v, mask,
-                                                   part_ml, part_acc, nch);
+    if (nh == 8) chunk(decode_chunk<128, 8>);
+    else if (nh == 4) chunk(decode_chunk<128, 4>);
+    else if (nh == 2) chunk(decode_chunk<128, 2>);
+    else chunk(decode_chunk<128, 1>);
     decode_combine<128><<<p.B * p.H, kCombThreads, 0, s>>>(p.H, nch, part_ml, part_acc, o, lse);
   }
   return cudaGetLastError();
