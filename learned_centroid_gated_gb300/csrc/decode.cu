@@ -6,7 +6,7 @@
 //
 // One query row per head is memory-bound work (each allowed key's K and V rows are
 // read once per KV head), so this runs on the CUDA cores, split over the keys:
-//   decode_chunk    one CTA per (chunk of kDecChunk keys, KV head, batch row) and up
+//   decode_chunk    one CTA per (chunk of CHUNK keys, KV head, batch row) and up
 //                   to NH query heads of that KV head (NH, a template parameter, is the
 //                   GQA ratio rounded down to 1, 2, 4 or 8, so the per-thread arrays fit
 //                   the heads there are): compacts the allowed keys of the chunk
@@ -14,6 +14,8 @@
 //                   row as independent 16-byte loads), and accumulates P V (16-byte V
 //                   loads, kDecUnroll batches of keys in flight); writes (max, sum, acc).
 //   decode_combine  merges the chunks of one (batch, head) by their maxima: O, LSE.
+// CHUNK is 1024 keys, or 2048 when that still leaves at least 2048 CTAs (long
+// caches: fewer, longer CTAs amortise the chunk's dependent memory round trips).
 #include <math.h>
 
 #include "common.cuh"
@@ -21,7 +23,6 @@
 namespace focus {
 namespace {
 
-constexpr int kDecChunk = 256;   // keys per CTA
 constexpr int kDecThreads = 128;
 constexpr int kDecHeads = 8;     // most query heads per CTA (of one KV head)
 constexpr int kDecUnroll = 8;    // P V: batches of keys whose V loads are in flight together
@@ -34,15 +35,15 @@ __device__ __forceinline__ unsigned lanemask_lt_dec() {
   return r;
 }
 
-template <int D, int NH>
+template <int D, int NH, int CHUNK>
 __global__ void __launch_bounds__(kDecThreads)
 decode_chunk(int N, int H, int H_kv, int R, int w, float sl2, const bf16* __restrict__ q,
              const bf16* __restrict__ k, const bf16* __restrict__ v,
              const uint32_t* __restrict__ mask, float2* __restrict__ part_ml,
              float* __restrict__ part_acc, int nch) {
   __shared__ float qs[NH][D];
-  __shared__ int idx[kDecChunk];
-  __shared__ float sc[NH][kDecChunk];
+  __shared__ int idx[CHUNK];
+  __shared__ float sc[NH][CHUNK];
   __shared__ int wsum[kDecThreads / 32];
   __shared__ float red[NH][kDecThreads / 32];
   __shared__ float stat[NH];
@@ -65,7 +66,7 @@ decode_chunk(int N, int H, int H_kv, int R, int w, float sl2, const bf16* __rest
     qs[hh][e] = __bfloat162float(q[((int64_t)b * H + h0 + hh) * D + e]);
   }
   // compaction of the chunk's allowed keys (every key of the cache is j <= i)
-  const int j0 = c * kDecChunk, j1 = min(N, j0 + kDecChunk);
+  const int j0 = c * CHUNK, j1 = min(N, j0 + CHUNK);
   int na = 0;
   for (int jb = j0; jb < j1; jb += kDecThreads) {
     const int j = jb + tid;
@@ -248,15 +249,27 @@ decode_combine(int H, int nch, const float2* __restrict__ part_ml, const float* 
 
 }  // namespace
 
-int decode_chunks(int N) { return (N + kDecChunk - 1) / kDecChunk; }
+int heads_per_cta(const focus_params& p) {
+  const int gq = p.H / p.H_kv;
+  return gq >= 8 ? 8 : gq >= 4 ? 4 : gq >= 2 ? 2 : 1;
+}
+
+int chunk_keys(const focus_params& p) {
+  const int gq = p.H / p.H_kv, nh = heads_per_cta(p);
+  const int64_t ctas = (int64_t)((p.N + 1023) / 1024) * p.H_kv * ((gq + nh - 1) / nh) * p.B;
+  return (nh <= 4 && ctas >= 2048) ? 2048 : 1024;
+}
+
+int decode_chunks(const focus_params& p) { return (p.N + chunk_keys(p) - 1) / chunk_keys(p); }
 
 cudaError_t launch_decode(const focus_params& p, const bf16* q, const bf16* k, const bf16* v,
                           const uint32_t* mask, bf16* o, float* lse, char* ws, float scale,
                           cudaStream_t s) {
-  const int nch = decode_chunks(p.N);
+  const int nch = decode_chunks(p);
   const int gq = p.H / p.H_kv;
-  const int nh = gq >= 8 ? 8 : gq >= 4 ? 4 : gq >= 2 ? 2 : 1;  // query heads per CTA
+  const int nh = heads_per_cta(p);  // query heads per CTA
   const int nhg = (gq + nh - 1) / nh;
+  const bool wide = chunk_keys(p) == 2048;
   float2* part_ml = reinterpret_cast<float2*>(ws);
   float* part_acc = reinterpret_cast<float*>(ws + align_up(sizeof(float2) * (size_t)p.B * p.H * nch, 256));
   dim3 grid(nch, p.H_kv * nhg, p.B);
@@ -266,23 +279,23 @@ cudaError_t launch_decode(const focus_params& p, const bf16* q, const bf16* k, c
                                         part_acc, nch);
   };
   if (p.d_head == 64) {
-    if (nh == 8) chunk(decode_chunk<64, 8>);
-    else if (nh == 4) chunk(decode_chunk<64, 4>);
-    else if (nh == 2) chunk(decode_chunk<64, 2>);
-    else chunk(decode_chunk<64, 1>);
+    if (nh == 8) chunk(decode_chunk<64, 8, 1024>);
+    else if (nh == 4) wide ? chunk(decode_chunk<64, 4, 2048>) : chunk(decode_chunk<64, 4, 1024>);
+    else if (nh == 2) wide ? chunk(decode_chunk<64, 2, 2048>) : chunk(decode_chunk<64, 2, 1024>);
+    else wide ? chunk(decode_chunk<64, 1, 2048>) : chunk(decode_chunk<64, 1, 1024>);
     decode_combine<64><<<p.B * p.H, kCombThreads, 0, s>>>(p.H, nch, part_ml, part_acc, o, lse);
   } else {
-    if (nh == 8) chunk(decode_chunk<128, 8>);
-    else if (nh == 4) chunk(decode_chunk<128, 4>);
-    else if (nh == 2) chunk(decode_chunk<128, 2>);
-    else chunk(decode_chunk<128, 1>);
+    if (nh == 8) chunk(decode_chunk<128, 8, 1024>);
+    else if (nh == 4) wide ? chunk(decode_chunk<128, 4, 2048>) : chunk(decode_chunk<128, 4, 1024>);
+    else if (nh == 2) wide ? chunk(decode_chunk<128, 2, 2048>) : chunk(decode_chunk<128, 2, 1024>);
+    else wide ? chunk(decode_chunk<128, 1, 2048>) : chunk(decode_chunk<128, 1, 1024>);
     decode_combine<128><<<p.B * p.H, kCombThreads, 0, s>>>(p.H, nch, part_ml, part_acc, o, lse);
   }
   return cudaGetLastError();
 }
 
 size_t decode_workspace_bytes(const focus_params& p) {
-  const size_t nch = (size_t)decode_chunks(p.N);
+  const size_t nch = (size_t)decode_chunks(p);
   return align_up(sizeof(float2) * (size_t)p.B * p.H * nch, 256) +
          align_up(sizeof(float) * (size_t)p.B * p.H * nch * p.d_head, 256);
 }

@@ -19,6 +19,7 @@ CASES = {
     "gqa_128k": synth.WORKLOADS["gqa_128k"],
     "extreme_1m": synth.WORKLOADS["extreme_1m"],
     "mqa16_b2": synth.WORKLOADS["tiny"].replace(B=2, N=3000, H=16, H_kv=1, d_head=128, K=6, top_k=2, w=100),
+    "gqa3_ragged_heads": synth.WORKLOADS["tiny"].replace(N=5000, H=6, H_kv=2, R=2, d_head=64, K=5, top_k=2, w=77),
     "single_token": synth.WORKLOADS["tiny"].replace(N=1),
     "window_covers_all": synth.WORKLOADS["tiny"].replace(N=700, w=4096),
     "one_group": synth.WORKLOADS["tiny"].replace(N=1025, K=1, top_k=1, w=16),
