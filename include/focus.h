@@ -243,8 +243,9 @@ int focus_get_status(const void* ws, void* stream);
  *   o        [B, H, d_head] bf16 out;  lse [B, H] fp32 out or NULL
  *   ws       focus_decode_workspace_size(p) bytes
  * p->N is the cache length including the newest token. Split over the keys in
- * chunks of 1024 or 2048 (one CTA per chunk, KV head and up to 8 of its query
- * heads), then an LSE merge of the chunks.
+ * slices (one warp per slice, KV head and up to 8 of its query heads, streaming the
+ * slice's allowed K and V rows through shared memory), then an LSE merge of the
+ * slices. The workspace holds the slices' partial results only.
  */
 size_t focus_decode_workspace_size(const focus_params* p);
 int focus_decode(const focus_params* p, const uint16_t* q, const uint16_t* k_cache,

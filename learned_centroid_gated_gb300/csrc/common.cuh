@@ -111,7 +111,6 @@ cudaError_t launch_attn_bwd(const focus_params& p, const BwdPlan& bp, const bf16
 cudaError_t launch_bwd_merge_slots(const focus_params& p, const BwdPlan& bp, const char* ws, bf16* dq,
                                    bf16* dk, bf16* dv, cudaStream_t s);
 // decode.cu
-int decode_chunks(const focus_params& p);
 size_t decode_workspace_bytes(const focus_params& p);
 cudaError_t launch_decode(const focus_params& p, const bf16* q, const bf16* k, const bf16* v,
                           const uint32_t* mask, bf16* o, float* lse, char* ws, float scale,
