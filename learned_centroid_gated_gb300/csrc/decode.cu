@@ -111,7 +111,8 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 // columns = heads, reduction over the keys), so P never leaves the registers.
 template <int D>
 __global__ void __launch_bounds__(32)
-decode_split(int N, int H, int H_kv, int R, int w, int B, int nsl, int slice, float sl2,
+decode_split(int N, int H, int H_kv, int R, int w, int B, int nsl, int nsl1, int s1, int s2,
+             float sl2,
              const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16* __restrict__ v,
              const uint32_t* __restrict__ mask, float2* __restrict__ part_ml,
              float* __restrict__ part_acc) {
@@ -151,9 +152,15 @@ decode_split(int N, int H, int H_kv, int R, int w, int B, int nsl, int slice, fl
     }
   }
 
+  // PDL: the combine kernel may be scheduled now; it waits for this grid's results.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // ---- compaction of the allowed keys of keys [js, je), one block of kDecBlock raw
-  // keys at a time; tiles of kDecTile keys are issued from a block's list
-  const int js = sl * slice, je = min(N, js + slice);
+  // keys at a time; tiles of kDecTile keys are issued from a block's list.  Slices
+  // 0 .. nsl1-1 cover the keys before the window (s1 keys each), the rest cover the
+  // window (s2 keys each, all of them allowed).
+  const int nw = max(0, N - w);
+  const int js = sl < nsl1 ? sl * s1 : nw + (sl - nsl1) * s2;
+  const int je = sl < nsl1 ? min(nw, js + s1) : min(N, js + s2);
   int jb = js, ncomp = 0, pos = 0;  // next block; keys in the list; keys issued
   constexpr int MW = kDecBlock / 32;
   uint32_t mw[MW];  // mask words of block jb, loaded one block ahead
@@ -287,58 +294,78 @@ decode_split(int N, int H, int H_kv, int R, int w, int B, int nsl, int slice, fl
   }
 }
 
-// Merge the slices of one (batch, head): grid = B * H, kCombThreads threads: thread
-// (g, e) sums element e over the slices c = g (mod kCombThreads / D).
-constexpr int kCombThreads = 1024;
+// Merge the slices of one (batch, head): grid = B * H, 32 warps; warp g folds the
+// slices c = g (mod 32) into a running (max, sum, acc) (lane: D / 32 columns), then
+// warp 0 folds the 32 warps' results in order.  Launched as a programmatic dependent
+// of decode_split: it waits for that grid's results before reading them.
+constexpr int kCombWarps = 32;
 template <int D>
-__global__ void __launch_bounds__(kCombThreads)
-decode_combine(int H, int nch, const float2* __restrict__ part_ml, const float* __restrict__ part_acc,
+__global__ void __launch_bounds__(32 * kCombWarps)
+decode_combine(int nch, const float2* __restrict__ part_ml, const float* __restrict__ part_acc,
                bf16* __restrict__ o, float* __restrict__ lse) {
-  constexpr int G = kCombThreads / D;
-  __shared__ float red[kCombThreads / 32];
-  __shared__ float partial[G][D];
-  __shared__ float lpart[G];
-  __shared__ float Ms;
-  const int bh = blockIdx.x, tid = threadIdx.x, e = tid % D, g = tid / D;
-  const float2* ml = part_ml + (int64_t)bh * nch;
-  float M = -INFINITY;
-  for (int c = tid; c < nch; c += kCombThreads) M = fmaxf(M, ml[c].x);
-  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-  if ((tid & 31) == 0) red[tid >> 5] = M;
-  __syncthreads();
-  if (tid == 0) {
-    float m = -INFINITY;
-    for (int w2 = 0; w2 < kCombThreads / 32; ++w2) m = fmaxf(m, red[w2]);
-    Ms = m;
-  }
-  __syncthreads();
-  M = Ms;
-  float L = 0.0f, acc = 0.0f;
+  constexpr int CPL = D / 32;
+  __shared__ float wm[kCombWarps], wl[kCombWarps];
+  __shared__ __align__(16) float wacc[kCombWarps][D];
+  const int bh = blockIdx.x, g = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  float m = -INFINITY, l = 0.0f, a[CPL];
+#pragma unroll
+  for (int e = 0; e < CPL; ++e) a[e] = 0.0f;
 #pragma unroll 4
-  for (int c = g; c < nch; c += G) {
-    const float2 x = ml[c];
-    const float f = x.y > 0.0f ? exp2f(x.x - M) : 0.0f;
-    L += x.y * f;
-    acc += part_acc[((int64_t)bh * nch + c) * D + e] * f;
+  for (int c = g; c < nch; c += kCombWarps) {
+    const int64_t slot = (int64_t)bh * nch + c;
+    const float2 x = part_ml[slot];
+    float v[CPL];
+    if constexpr (CPL == 4) {
+      const float4 t = *reinterpret_cast<const float4*>(part_acc + slot * D + 4 * lane);
+      v[0] = t.x, v[1] = t.y, v[2] = t.z, v[3] = t.w;
+    } else {
+      const float2 t = *reinterpret_cast<const float2*>(part_acc + slot * D + 2 * lane);
+      v[0] = t.x, v[1] = t.y;
+    }
+    if (x.y > 0.0f) {  // a slice without allowed keys holds (-inf, 0)
+      const float mn = fmaxf(m, x.x), f0 = ex2(m - mn), f1 = ex2(x.x - mn);
+      l = l * f0 + x.y * f1;
+#pragma unroll
+      for (int e = 0; e < CPL; ++e) a[e] = a[e] * f0 + v[e] * f1;
+      m = mn;
+    }
   }
-  partial[g][e] = acc;
-  if (e == 0) lpart[g] = L;
+#pragma unroll
+  for (int e = 0; e < CPL; ++e) wacc[g][CPL * lane + e] = a[e];
+  if (lane == 0) {
+    wm[g] = m;
+    wl[g] = l;
+  }
   __syncthreads();
   if (g == 0) {
-    float tot = 0.0f, Lt = 0.0f;
-    for (int gg = 0; gg < G; ++gg) {
-      tot += partial[gg][e];
-      Lt += lpart[gg];
+    float M = -INFINITY;
+    for (int gg = 0; gg < kCombWarps; ++gg) M = fmaxf(M, wm[gg]);
+    float L = 0.0f, A[CPL];
+#pragma unroll
+    for (int e = 0; e < CPL; ++e) A[e] = 0.0f;
+    for (int gg = 0; gg < kCombWarps; ++gg) {
+      if (wl[gg] > 0.0f) {
+        const float f = ex2(wm[gg] - M);
+        L += wl[gg] * f;
+#pragma unroll
+        for (int e = 0; e < CPL; ++e) A[e] += wacc[gg][CPL * lane + e] * f;
+      }
     }
-    o[(int64_t)bh * D + e] = __float2bfloat16_rn(tot / Lt);
-    if (e == 0 && lse) lse[bh] = (M + log2f(Lt)) * kLn2;
+#pragma unroll
+    for (int e = 0; e < CPL; ++e) o[(int64_t)bh * D + CPL * lane + e] = __float2bfloat16_rn(A[e] / L);
+    if (lane == 0 && lse) lse[bh] = (M + log2f(L)) * kLn2;
   }
 }
 
-// Work split: head groups per KV head (nhg), number of slices of the cache (nsl)
-// and raw keys per slice.
+// Work split: head groups per KV head (nhg) and slices of the cache per (batch, KV
+// head, head group): nsl1 slices of s1 keys before the window, nsl - nsl1 slices of
+// s2 keys over it.  The window is fully allowed, the rest only where the masks meet,
+// so the slices are sized for equal expected work: the density outside the window is
+// estimated as the chance that two uniformly drawn top_k-sets of the K groups share
+// one, 1 - C(K - k, k) / C(K, k) (load balance only; every key is still visited).
 struct DecPlan {
-  int nhg, nsl, slice;
+  int nhg, nsl, nsl1, s1, s2;
 };
 
 DecPlan dec_plan(const focus_params& p) {
@@ -348,8 +375,17 @@ DecPlan dec_plan(const focus_params& p) {
   const int64_t base = (int64_t)p.B * p.H_kv * d.nhg;
   int64_t nsl = std::max<int64_t>(1, (kDecTargetWarps + base - 1) / base);
   nsl = std::min<int64_t>(nsl, (p.N + kDecMinSlice - 1) / kDecMinSlice);
-  d.slice = (int)((p.N + nsl - 1) / nsl + 31) / 32 * 32;
-  d.nsl = (p.N + d.slice - 1) / d.slice;
+  const int64_t nwin = std::min<int64_t>(p.w, p.N), nrest = p.N - nwin;
+  double miss = 1.0;  // C(K - k, k) / C(K, k)
+  for (int t = 0; t < p.top_k; ++t) miss *= std::max(0.0, (double)(p.K - p.top_k - t)) / (p.K - t);
+  const double work = (1.0 - miss) * nrest + nwin;
+  int64_t n2 = nrest == 0 ? nsl : std::llround(nwin * nsl / std::max(work, 1.0));
+  n2 = std::min<int64_t>(std::max<int64_t>(n2, 1), nrest == 0 ? nsl : std::max<int64_t>(nsl - 1, 1));
+  const int64_t n1 = nrest == 0 ? 0 : std::max<int64_t>(nsl - n2, 1);
+  d.s1 = n1 ? (int)(((nrest + n1 - 1) / n1 + 31) / 32 * 32) : 32;
+  d.s2 = (int)(((nwin + n2 - 1) / n2 + 31) / 32 * 32);
+  d.nsl1 = n1 ? (int)((nrest + d.s1 - 1) / d.s1) : 0;
+  d.nsl = d.nsl1 + (int)((nwin + d.s2 - 1) / d.s2);
   return d;
 }
 
@@ -371,8 +407,8 @@ cudaError_t launch_split(const focus_params& p, const DecPlan& d, float sl2, con
   }
   const int64_t items = (int64_t)p.B * p.H_kv * d.nhg * d.nsl;
   decode_split<D><<<(unsigned)items, 32, L::BYTES, s>>>(p.N, p.H, p.H_kv, p.R, p.w, p.B, d.nsl,
-                                                        d.slice, sl2, q, k, v, mask, part_ml,
-                                                        part_acc);
+                                                        d.nsl1, d.s1, d.s2, sl2, q, k, v, mask,
+                                                        part_ml, part_acc);
   return cudaGetLastError();
 }
 
@@ -389,10 +425,20 @@ cudaError_t launch_decode(const focus_params& p, const bf16* q, const bf16* k, c
                       ? launch_split<64>(p, d, sl2, q, k, v, mask, part_ml, part_acc, s)
                       : launch_split<128>(p, d, sl2, q, k, v, mask, part_ml, part_acc, s);
   if (e != cudaSuccess) return e;
-  if (p.d_head == 64)
-    decode_combine<64><<<p.B * p.H, kCombThreads, 0, s>>>(p.H, d.nsl, part_ml, part_acc, o, lse);
-  else
-    decode_combine<128><<<p.B * p.H, kCombThreads, 0, s>>>(p.H, d.nsl, part_ml, part_acc, o, lse);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(p.B * p.H));
+  cfg.blockDim = dim3(32 * kCombWarps);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const float2* ml = part_ml;
+  const float* pa = part_acc;
+  e = p.d_head == 64 ? cudaLaunchKernelEx(&cfg, decode_combine<64>, d.nsl, ml, pa, o, lse)
+                     : cudaLaunchKernelEx(&cfg, decode_combine<128>, d.nsl, ml, pa, o, lse);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
