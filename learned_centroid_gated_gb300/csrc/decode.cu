@@ -295,8 +295,9 @@ decode_split(int N, int H, int H_kv, int R, int w, int B, int nsl, int nsl1, int
 }
 
 // Merge the slices of one (batch, head): grid = B * H, 32 warps; warp g folds the
-// slices c = g (mod 32) into a running (max, sum, acc) (lane: D / 32 columns), then
-// warp 0 folds the 32 warps' results in order.  Launched as a programmatic dependent
+// slices c = g (mod 32) into a running (max, sum, acc) (lane: D / 32 columns; the
+// loads of 8 slices in flight together), then warp 0 folds the 32 warps' results in
+// order.  Launched as a programmatic dependent
 // of decode_split: it waits for that grid's results before reading them.
 constexpr int kCombWarps = 32;
 template <int D>
@@ -311,24 +312,32 @@ decode_combine(int nch, const float2* __restrict__ part_ml, const float* __restr
   float m = -INFINITY, l = 0.0f, a[CPL];
 #pragma unroll
   for (int e = 0; e < CPL; ++e) a[e] = 0.0f;
-#pragma unroll 4
-  for (int c = g; c < nch; c += kCombWarps) {
-    const int64_t slot = (int64_t)bh * nch + c;
-    const float2 x = part_ml[slot];
-    float v[CPL];
-    if constexpr (CPL == 4) {
-      const float4 t = *reinterpret_cast<const float4*>(part_acc + slot * D + 4 * lane);
-      v[0] = t.x, v[1] = t.y, v[2] = t.z, v[3] = t.w;
-    } else {
-      const float2 t = *reinterpret_cast<const float2*>(part_acc + slot * D + 2 * lane);
-      v[0] = t.x, v[1] = t.y;
-    }
-    if (x.y > 0.0f) {  // a slice without allowed keys holds (-inf, 0)
-      const float mn = fmaxf(m, x.x), f0 = ex2(m - mn), f1 = ex2(x.x - mn);
-      l = l * f0 + x.y * f1;
+  constexpr int U = 8;  // slices whose loads are issued together
+  for (int c0 = g; c0 < nch; c0 += U * kCombWarps) {
+    float2 x[U];
+    float v[U][CPL];
 #pragma unroll
-      for (int e = 0; e < CPL; ++e) a[e] = a[e] * f0 + v[e] * f1;
-      m = mn;
+    for (int u = 0; u < U; ++u) {
+      const int c = c0 + u * kCombWarps;
+      const int64_t slot = (int64_t)bh * nch + min(c, nch - 1);
+      x[u] = c < nch ? part_ml[slot] : make_float2(-INFINITY, 0.0f);
+      if constexpr (CPL == 4) {
+        const float4 t = *reinterpret_cast<const float4*>(part_acc + slot * D + 4 * lane);
+        v[u][0] = t.x, v[u][1] = t.y, v[u][2] = t.z, v[u][3] = t.w;
+      } else {
+        const float2 t = *reinterpret_cast<const float2*>(part_acc + slot * D + 2 * lane);
+        v[u][0] = t.x, v[u][1] = t.y;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      if (x[u].y > 0.0f) {  // a slice without allowed keys holds (-inf, 0)
+        const float mn = fmaxf(m, x[u].x), f0 = ex2(m - mn), f1 = ex2(x[u].x - mn);
+        l = l * f0 + x[u].y * f1;
+#pragma unroll
+        for (int e = 0; e < CPL; ++e) a[e] = a[e] * f0 + v[u][e] * f1;
+        m = mn;
+      }
     }
   }
 #pragma unroll
