@@ -766,6 +766,7 @@ bwd_dkdv(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtenso
   const uint32_t b_full = bb + BB::FULL, b_empty = bb + BB::EMPTY, b_sdp = bb + BB::SDP;
   const uint32_t b_ds = bb + BB::DS, b_a = bb + BB::A, b_fin = bb + BB::FIN, b_drain = bb + BB::DRAIN;
   const uint32_t b_kvf = bb + BB::KVF, b_kve = bb + BB::KVE;
+  const uint32_t b_ds0 = bb + BB::RD;  // first half of dS^T / P^T written (RD is the dQ kernel's)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bar + BB::ABORT);
   float* scal = reinterpret_cast<float*>(sm + L::SCAL);  // [NST][4][NQ]
   init_cta<NST>(bar, warp, 2);
@@ -904,19 +905,27 @@ bwd_dkdv(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtenso
         ++ac;
         for (int t = 0; t < it.n; ++t) {
           const int gc = g + t;
-          if (!(ok = mbar_wait(b_ds, (uint32_t)(gc & 1), abort_flag, status, tlim))) break;
-          tc_fence_after();
           const uint32_t qa = qaddr(gc), da = qa + L::TILE;
-          // P^T (dS^T) of queries 32w + 2i, 32w + 2i + 1 sits in column 32w + i
+          // P^T (dS^T) of queries 32w + 16h + 2i, +1 sits in column 32w + 8h + i.  The
+          // elementwise warps hand over the first 16 queries of each warpgroup (h = 0,
+          // barrier DS0) before the second (h = 1, barrier DS), so the products of the
+          // first half run while the second half is computed.
 #pragma unroll
-          for (int kk = 0; kk < NQ / 16; ++kk) {
-            const uint32_t acc = (t > 0 || kk > 0) ? 1u : 0u;
-            const uint32_t col = 32 * (kk >> 1) + 8 * (kk & 1);
-            umma_ts(tmem + L::COL_DV, tmem + L::COL_ST + col, sw128_desc(da + kk * 2048, BOX, 1024), IKV,
-                    acc);
-            umma_ts(tmem + L::COL_DK, tmem + L::COL_DPT + col, sw128_desc(qa + kk * 2048, BOX, 1024), IKV,
-                    acc);
+          for (int hh = 0; hh < 2; ++hh) {
+            if (!(ok = mbar_wait(hh ? b_ds : b_ds0, (uint32_t)(gc & 1), abort_flag, status, tlim))) break;
+            tc_fence_after();
+#pragma unroll
+            for (int w4 = 0; w4 < NQ / 32; ++w4) {
+              const int kk = 2 * w4 + hh;
+              const uint32_t acc = (t > 0 || kk > 0) ? 1u : 0u;
+              const uint32_t col = 32 * w4 + 8 * hh;
+              umma_ts(tmem + L::COL_DV, tmem + L::COL_ST + col, sw128_desc(da + kk * 2048, BOX, 1024), IKV,
+                      acc);
+              umma_ts(tmem + L::COL_DK, tmem + L::COL_DPT + col, sw128_desc(qa + kk * 2048, BOX, 1024), IKV,
+                      acc);
+            }
           }
+          if (!ok) break;
           umma_commit(b_empty + 8 * (gc % NST));
           if (t + 1 < it.n) {
             if (!(ok = ring_wait(gc + 1))) break;
@@ -994,15 +1003,15 @@ bwd_dkdv(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtenso
           for (int i = 0; i < 16; i += 4) {
             const float4 l4 = *reinterpret_cast<const float4*>(sc + c + i);
             const float4 d4 = *reinterpret_cast<const float4*>(sc + NQ + c + i);
-            const int4 q4 = *reinterpret_cast<const int4*>(reinterpret_cast<const int*>(sc) + 2 * NQ + c + i);
             const float ls[4] = {l4.x, l4.y, l4.z, l4.w}, dd[4] = {d4.x, d4.y, d4.z, d4.w};
-            const int pq[4] = {q4.x, q4.y, q4.z, q4.w};
             float pv[4], dv4[4], y[4], tt[4];
             ffma2(y[0], y[1], __uint_as_float(st[i]), __uint_as_float(st[i + 1]), sl2, sl2, -ls[0], -ls[1]);
             ffma2(y[2], y[3], __uint_as_float(st[i + 2]), __uint_as_float(st[i + 3]), sl2, sl2, -ls[2], -ls[3]);
 #pragma unroll
             for (int e = 0; e < 4; ++e) pv[e] = ex2(y[e]);
             if (need_mask) {
+              const int4 q4 = *reinterpret_cast<const int4*>(reinterpret_cast<const int*>(sc) + 2 * NQ + c + i);
+              const int pq[4] = {q4.x, q4.y, q4.z, q4.w};
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
                 const int dpos = pq[e] - pj;
@@ -1027,10 +1036,10 @@ bwd_dkdv(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtenso
           }
           tmem_st8(tl + L::COL_ST + 32 * wg + 8 * hh, pp);   // over columns already read
           tmem_st8(tl + L::COL_DPT + 32 * wg + 8 * hh, pd);
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(hh ? b_ds : b_ds0);
         }
-        tmem_st_wait();
-        tc_fence_before();
-        mbar_arrive(b_ds);
       }
       if (!ok) break;
       // ---- epilogue: dK = scale * (dS^T Q) (warpgroups 0, 1), dV = P^T dO (2, 3) ----
