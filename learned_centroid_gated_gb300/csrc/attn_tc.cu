@@ -9,9 +9,13 @@
 // softmax is the log-sum-exp merge of two partial softmaxes; every key is
 // visited once because tokens are bucketed by their exact group set.
 //
-// Persistent kernel: one CTA per SM walks a static round-robin share of the work
-// items (query blocks of 256 rows of one head).  Each item is two 128-row query
-// tiles A and B that ping-pong on the tensor core:
+// Persistent kernel: one CTA per SM; the producer warp takes the next work item
+// (query block of 256 rows of one head) from a global counter and hands it to the
+// MMA issuer and the softmax warps through a small shared-memory ring, so the CTAs
+// share the items dynamically in the schedule's order (heaviest first within a head):
+// a static round-robin share left the average SM idle ~10% of the launch while the
+// most loaded one finished.  Each item is two 128-row query tiles A and B that
+// ping-pong on the tensor core:
 //   warp 8      TMA producer: Q tiles of each item, then K and V tiles through a
 //               3-slot ring; runs ahead across item boundaries
 //   warp 9      MMA issuer (one thread): S = Q K^T into TMEM, O += P V into TMEM
@@ -60,6 +64,8 @@ constexpr int QT = 128;        // rows per query tile (MMA M)
 constexpr int BMQ = 2 * QT;    // query rows per work item
 constexpr int BNK = kKeyTile;  // keys per tile (MMA N of S, K of P V)
 constexpr int NSTAGE = 3;      // K/V ring slots
+constexpr int NRING = 4;       // work items handed from the producer to the other roles
+constexpr int RING_CONSUMERS = 9;  // MMA issuer + the 8 softmax warps
 constexpr int NTHREADS = 384;
 constexpr int PRODUCER_WARP = 8;
 constexpr int MMA_WARP = 9;
@@ -85,13 +91,15 @@ struct Layout {
   static constexpr int RING = Q + 2 * TILE;
   static constexpr int BAR = RING + NSTAGE * TILE;
   // barrier block: q, q_empty, full[NSTAGE], empty[NSTAGE], s[2], p[2], o[2], drain,
-  // key-set[2] (8 bytes each), then the TMEM address word and the abort flag
+  // key-set[2], item ring full[NRING] / empty[NRING] (8 bytes each), then the TMEM
+  // address word, the abort flag and the ring's item indices
   static constexpr int BAR_Q = 0, BAR_QE = 8, BAR_FULL = 16, BAR_EMPTY = BAR_FULL + 8 * NSTAGE;
   static constexpr int BAR_S = BAR_EMPTY + 8 * NSTAGE, BAR_P = BAR_S + 16, BAR_O = BAR_P + 16;
   static constexpr int BAR_DRAIN = BAR_O + 16, BAR_KS = BAR_DRAIN + 8;
-  static constexpr int TMEM_SLOT = BAR_KS + 16, ABORT = TMEM_SLOT + 4;
+  static constexpr int BAR_RF = BAR_KS + 16, BAR_RE = BAR_RF + 8 * NRING;  // item ring full / empty
+  static constexpr int TMEM_SLOT = BAR_RE + 8 * NRING, ABORT = TMEM_SLOT + 4, RING_X = ABORT + 4;
   static constexpr int BAR_BYTES = 256;
-  static_assert(ABORT + 4 <= BAR_BYTES, "barrier block overflow");
+  static_assert(RING_X + 4 * NRING <= BAR_BYTES, "barrier block overflow");
   // group lists: per query tile, two buffers of [32 group bits][4 words] key sets
   static constexpr int KSET = BAR + BAR_BYTES;
   static constexpr int KSET_BYTES = 2 * 2 * 32 * 4 * 4;
@@ -116,6 +124,7 @@ struct TcArgs {
   bf16* o;
   float* lse;
   int* status;
+  int* item_counter;         // next work item (zero before the launch)
   long long timeout_cycles;  // limit of every bounded wait
   int stall_producer;        // diagnostic: the producer issues nothing (waits run out)
 };
@@ -211,8 +220,10 @@ attn_tc(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensor
   const uint32_t b_o = smem_u32(bar) + L::BAR_O;
   const uint32_t b_drain = smem_u32(bar) + L::BAR_DRAIN;
   const uint32_t b_ks = smem_u32(bar) + L::BAR_KS;  // + 8 * query tile
+  const uint32_t b_rf = smem_u32(bar) + L::BAR_RF, b_re = smem_u32(bar) + L::BAR_RE;  // + 8 * slot
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(bar + L::TMEM_SLOT);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bar + L::ABORT);
+  volatile int* ring_x = reinterpret_cast<volatile int*>(bar + L::RING_X);
 
   if (warp == MMA_WARP) {
     tmem_alloc(smem_u32(bar + L::TMEM_SLOT), TMEM_COLS);
@@ -232,6 +243,10 @@ attn_tc(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensor
     }
     mbar_init(b_drain, 1);
     for (int t = 0; t < 2; ++t) mbar_init(b_ks + 8 * t, 4);
+    for (int r = 0; r < NRING; ++r) {
+      mbar_init(b_rf + 8 * r, 1);
+      mbar_init(b_re + 8 * r, RING_CONSUMERS);
+    }
     *abort_flag = 0;
     fence_barrier_init();
     fence_proxy_async_smem();
@@ -255,7 +270,13 @@ attn_tc(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensor
       int stage = 0, qcnt = 0, q_par = -1;
       uint32_t phase = 0;
       bool ok = true;
-      for (int x = a.stall_producer ? n_items : blockIdx.x; ok && x < n_items; x += gridDim.x) {
+      for (int kr = 0; !a.stall_producer; ++kr) {  // diagnostic: a stalled producer hands out nothing
+        const int rs = kr % NRING;
+        if (!(ok = mbar_wait(b_re + 8 * rs, ((kr / NRING) & 1) ^ 1, abort_flag, status, tlim))) break;
+        const int x = atomicAdd(a.item_counter, 1);
+        ring_x[rs] = x;
+        mbar_arrive(b_rf + 8 * rs);
+        if (x >= n_items) break;
         const Item it = decode<LONG>(a, x);
         if (!it.valid || it.n == 0) continue;
         if (!(ok = mbar_wait(b_qe, (qcnt & 1) ^ 1, abort_flag, status, tlim))) break;
@@ -302,6 +323,7 @@ attn_tc(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensor
             }
           }
         }
+        if (!ok) break;
       }
       if (*abort_flag) {  // let every copy in flight land before the CTA exits
         if (q_par >= 0) mbar_drain(b_q, (uint32_t)q_par);
@@ -335,7 +357,12 @@ attn_tc(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensor
       };
       int ri = 0, gt = 0, qcnt = 0;
       bool ok = true;
-      for (int x = blockIdx.x; ok && x < n_items; x += gridDim.x) {
+      for (int kr = 0;; ++kr) {
+        const int rs = kr % NRING;
+        if (!(ok = mbar_wait(b_rf + 8 * rs, (kr / NRING) & 1, abort_flag, status, tlim))) break;
+        const int x = ring_x[rs];
+        mbar_arrive(b_re + 8 * rs);
+        if (x >= n_items) break;
         const Item it = decode<LONG>(a, x);
         if (!it.valid || it.n == 0) continue;
         const int n = it.n;
@@ -375,6 +402,7 @@ attn_tc(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensor
         }
         ri += 2 * n;
         gt += n;
+        if (!ok) break;
       }
       umma_commit(b_drain);  // every MMA issued above completes before TMEM is released
       mbar_drain(b_drain, 0);
@@ -392,7 +420,17 @@ attn_tc(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensor
     int gt = 0;
     int ks_cnt = 0;  // key-set barrier uses (group lists)
     bool ok = true;
-    for (int x = blockIdx.x; ok && x < n_items; x += gridDim.x) {
+    for (int kr = 0;; ++kr) {
+      const int rs = kr % NRING;
+      ok = mbar_wait(b_rf + 8 * rs, (kr / NRING) & 1, abort_flag, status, tlim);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
+      const int x = ring_x[rs];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(b_re + 8 * rs);
+      if (x >= n_items) break;
       const Item it = decode<LONG>(a, x);
       if (!it.valid) continue;
       const int n = it.n;
@@ -763,6 +801,7 @@ TcArgs make_args(const focus_params& p, const WsLayout& L, char* ws, float scale
   a.o_part = reinterpret_cast<float*>(ws + L.olr);
   a.lse_part = reinterpret_cast<float*>(ws + L.lselr);
   a.status = &reinterpret_cast<WsHeader*>(ws)->status;
+  a.item_counter = &reinterpret_cast<WsHeader*>(ws)->item_counter[0];
   a.timeout_cycles = kTimeoutCycles;
   a.stall_producer = 0;
   return a;
@@ -818,6 +857,7 @@ cudaError_t launch_attn_long_tc(const focus_params& p, const WsLayout& L, char* 
   TcArgs a = make_args(p, L, ws, scale);
   a.o = o;
   a.lse = lse;
+  a.item_counter = &reinterpret_cast<WsHeader*>(ws)->item_counter[1];
   CUtensorMap mq, mk, mv;
   if (!make_map(&mq, ws + L.qp, p.d_head, (int64_t)p.B * p.H * L.NR, 0) ||
       !make_map(&mk, ws + L.kp, p.d_head, (int64_t)p.B * p.H_kv * L.NR, 0) ||

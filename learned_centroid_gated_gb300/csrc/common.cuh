@@ -16,7 +16,8 @@ using bf16 = __nv_bfloat16;
 struct WsHeader {
   int status;       // first error code raised by a kernel, 0 if none
   int qtab_count;   // number of query blocks in the long-range schedule
-  int pad[62];
+  int item_counter[2];  // next work item of the window / long-range attention kernel
+  int pad[60];
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 
