@@ -61,15 +61,53 @@ enum : int { kWin = 0, kSeg = 1, kGrp = 2 };
 // Barrier block shared by both kernels: full[NST], empty[NST], then sdp, ds, dqc,
 // rd, a, fin, drain, kv_full, kv_empty (8 bytes each), the TMEM address word and
 // the abort flag.  (In bwd_dq kv_full / kv_empty guard the item's Q tile.)
+constexpr int NRING = 4;            // work-item ring entries
+constexpr int RING_CONSUMERS = 1 + EW_WARPS;  // MMA issuer + one lane per elementwise warp
 template <int NST>
 struct Bars {
   static constexpr int FULL = 0, EMPTY = 8 * NST, SDP = 16 * NST, DS = SDP + 8, DQC = DS + 8;
   static constexpr int RD = DQC + 8, A = RD + 8, FIN = A + 8, DRAIN = FIN + 8, KVF = DRAIN + 8;
   static constexpr int KVE = KVF + 8;
   static constexpr int TMEM_SLOT = KVE + 8, ABORT = TMEM_SLOT + 4;
+  // work-item ring: full[NRING], empty[NRING] barriers and the item indices
+  static constexpr int RF = (ABORT + 4 + 7) / 8 * 8, RE = RF + 8 * NRING, RING_X = RE + 8 * NRING;
   static constexpr int BYTES = 256;
-  static_assert(ABORT + 4 <= BYTES, "barrier block overflow");
+  static_assert(RING_X + 4 * NRING <= BYTES, "barrier block overflow");
 };
+
+// Work items reach the MMA issuer and the elementwise warps through a small ring
+// filled by the producer warp from a global counter, so the CTAs share the items
+// dynamically in order (a static round-robin share left the average SM idle ~3.5% of
+// a long-range launch while the most loaded one finished).  Each item writes only
+// its own rows, so the result does not depend on which CTA takes it.
+__device__ __forceinline__ bool ring_put(uint32_t rf, uint32_t re, volatile int* rx, int kr, int* counter,
+                                         int& x, volatile int* abort_flag, int* status, long long tlim) {
+  const int rs = kr % NRING;
+  if (!mbar_wait(re + 8 * rs, (uint32_t)(((kr / NRING) & 1) ^ 1), abort_flag, status, tlim)) return false;
+  x = atomicAdd(counter, 1);
+  rx[rs] = x;
+  mbar_arrive(rf + 8 * rs);
+  return true;
+}
+__device__ __forceinline__ bool ring_get(uint32_t rf, uint32_t re, volatile int* rx, int kr, int& x,
+                                         volatile int* abort_flag, int* status, long long tlim) {
+  const int rs = kr % NRING;
+  if (!mbar_wait(rf + 8 * rs, (uint32_t)((kr / NRING) & 1), abort_flag, status, tlim)) return false;
+  x = rx[rs];
+  mbar_arrive(re + 8 * rs);
+  return true;
+}
+// Whole-warp consumer: every lane waits, lane 0 releases the slot.
+__device__ __forceinline__ bool ring_get_warp(uint32_t rf, uint32_t re, volatile int* rx, int kr, int& x,
+                                              volatile int* abort_flag, int* status, long long tlim) {
+  const int rs = kr % NRING;
+  const bool ok = mbar_wait(rf + 8 * rs, (uint32_t)((kr / NRING) & 1), abort_flag, status, tlim);
+  if (!__all_sync(0xffffffffu, ok)) return false;
+  x = rx[rs];
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(re + 8 * rs);
+  return true;
+}
 
 constexpr int BOX = 128 * 128;  // one TMA box: 128 rows x 128 bytes (64 bf16)
 
@@ -131,6 +169,7 @@ struct BwdArgs {
   float* dk_s;            // group lists: [top_k][B, N, H_kv, d]
   float* dv_s;
   int* status;
+  int* item_counter;  // next work item of this launch (zero before it)
   long long timeout_cycles;
 };
 
@@ -401,6 +440,10 @@ __device__ __forceinline__ void init_cta(uint8_t* bar, int warp, uint32_t full_c
     mbar_init(base + BB::DRAIN, 1);
     mbar_init(base + BB::KVF, 1);
     mbar_init(base + BB::KVE, 1);
+    for (int r = 0; r < NRING; ++r) {
+      mbar_init(base + BB::RF + 8 * r, 1);
+      mbar_init(base + BB::RE + 8 * r, RING_CONSUMERS);
+    }
     *reinterpret_cast<volatile int*>(bar + BB::ABORT) = 0;
     fence_barrier_init();
     fence_proxy_async_smem();
@@ -440,6 +483,8 @@ bwd_dq(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorM
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(bar + BB::TMEM_SLOT);
   int* status = a.status;
   const long long tlim = a.timeout_cycles;
+  const uint32_t b_rf = bb + BB::RF, b_re = bb + BB::RE;
+  volatile int* ring_x = reinterpret_cast<volatile int*>(bar + BB::RING_X);
 
   if (warp == PRODUCER_WARP) {
     // lane 0 waits and issues the copies; with group lists every lane also stages
@@ -453,7 +498,12 @@ bwd_dq(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorM
     for (int s = 0; s < NST; ++s) last_par[s] = -1;
     int g = 0, qc = 0, q_par = -1;
     bool ok = true;
-    for (int x = blockIdx.x; ok && x < n_items; x += gridDim.x) {
+    for (int kr = 0;; ++kr) {
+      int x = 0;
+      if (lane == 0) ok = ring_put(b_rf, b_re, ring_x, kr, a.item_counter, x, abort_flag, status, tlim);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      x = __shfl_sync(0xffffffffu, x, 0);
+      if (!ok || x >= n_items) break;
       const BItem it = dq_item<LONG>(a, x);
       if (!it.valid || it.n == 0) continue;
       // the item's Q rows, once the previous item's products are done
@@ -510,6 +560,7 @@ bwd_dq(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorM
         }
         last_par[slot] = (int)par;
       }
+      if (!ok) break;
     }
     if (lane == 0 && *abort_flag) {
       if (q_par >= 0) mbar_drain(b_qf, (uint32_t)q_par);
@@ -544,7 +595,9 @@ bwd_dq(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorM
       };
       int g = 0, ac = 0, qc = 0;
       bool ok = true;
-      for (int x = blockIdx.x; ok && x < n_items; x += gridDim.x) {
+      for (int kr = 0;; ++kr) {
+        int x = 0;
+        if (!(ok = ring_get(b_rf, b_re, ring_x, kr, x, abort_flag, status, tlim)) || x >= n_items) break;
         const BItem it = dq_item<LONG>(a, x);
         if (!it.valid || it.n == 0) continue;
         // Q landed; the warps staged dO (and read the previous item's dQ)
@@ -592,7 +645,9 @@ bwd_dq(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorM
     const float sl2 = a.sl2;
     int g = 0, ac = 0;
     bool ok = true;
-    for (int x = blockIdx.x; ok && x < n_items; x += gridDim.x) {
+    for (int kr = 0;; ++kr) {
+      int x = 0;
+      if (!(ok = ring_get_warp(b_rf, b_re, ring_x, kr, x, abort_flag, status, tlim)) || x >= n_items) break;
       const BItem it = dq_item<LONG>(a, x);
       if (!it.valid) continue;
       const bool row_ok = r < it.rows;
@@ -767,6 +822,8 @@ bwd_dkdv(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtenso
   const uint32_t b_ds = bb + BB::DS, b_a = bb + BB::A, b_fin = bb + BB::FIN, b_drain = bb + BB::DRAIN;
   const uint32_t b_kvf = bb + BB::KVF, b_kve = bb + BB::KVE;
   const uint32_t b_ds0 = bb + BB::RD;  // first half of dS^T / P^T written (RD is the dQ kernel's)
+  const uint32_t b_rf = bb + BB::RF, b_re = bb + BB::RE;
+  volatile int* ring_x = reinterpret_cast<volatile int*>(bar + BB::RING_X);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bar + BB::ABORT);
   float* scal = reinterpret_cast<float*>(sm + L::SCAL);  // [NST][4][NQ]
   init_cta<NST>(bar, warp, 2);
@@ -786,7 +843,12 @@ bwd_dkdv(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtenso
     for (int s = 0; s < NST; ++s) last_par[s] = -1;
     int g = 0, kc = 0, kv_par = -1;
     bool ok = true;
-    for (int x = blockIdx.x; ok && x < n_items; x += gridDim.x) {
+    for (int kr = 0;; ++kr) {
+      int x = 0;
+      if (lane == 0) ok = ring_put(b_rf, b_re, ring_x, kr, a.item_counter, x, abort_flag, status, tlim);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      x = __shfl_sync(0xffffffffu, x, 0);
+      if (!ok || x >= n_items) break;
       const BItem it = dkv_item<LONG>(a, x);
       if (!it.valid || it.n == 0) continue;
       // the item's K and V rows, once the previous item's products are done
@@ -858,6 +920,7 @@ bwd_dkdv(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtenso
         if (lane == 0) mbar_arrive(fb);
         last_par[slot] = (int)par;
       }
+      if (!ok) break;
     }
     if (lane == 0 && *abort_flag) {
       if (kv_par >= 0) mbar_drain(b_kvf, (uint32_t)kv_par);
@@ -893,7 +956,9 @@ bwd_dkdv(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtenso
       };
       int g = 0, ac = 0, kc = 0;
       bool ok = true;
-      for (int x = blockIdx.x; ok && x < n_items; x += gridDim.x) {
+      for (int kr = 0;; ++kr) {
+        int x = 0;
+        if (!(ok = ring_get(b_rf, b_re, ring_x, kr, x, abort_flag, status, tlim)) || x >= n_items) break;
         const BItem it = dkv_item<LONG>(a, x);
         if (!it.valid || it.n == 0) continue;
         if (!(ok = mbar_wait(b_kvf, (uint32_t)(kc & 1), abort_flag, status, tlim) && ring_wait(g))) break;
@@ -952,7 +1017,9 @@ bwd_dkdv(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtenso
     const int w = a.w;
     int g = 0, ac = 0;
     bool ok = true;
-    for (int x = blockIdx.x; ok && x < n_items; x += gridDim.x) {
+    for (int kr = 0;; ++kr) {
+      int x = 0;
+      if (!(ok = ring_get_warp(b_rf, b_re, ring_x, kr, x, abort_flag, status, tlim)) || x >= n_items) break;
       const BItem it = dkv_item<LONG>(a, x);
       if (!it.valid) continue;
       const bool row_ok = r < it.rows;
@@ -1305,6 +1372,8 @@ cudaError_t launch_attn_bwd(const focus_params& p, const BwdPlan& bp, const bf16
   a.dk_s = reinterpret_cast<float*>(ws + bp.dks);
   a.dv_s = reinterpret_cast<float*>(ws + bp.dvs);
   a.status = &reinterpret_cast<WsHeader*>(ws)->status;
+  // one counter per launch of the call: window dQ, window dK/dV, long dQ, long dK/dV
+  a.item_counter = &reinterpret_cast<WsHeader*>(ws)->item_counter[(long_pass ? 2 : 0) + (dq_kernel ? 0 : 1)];
   a.timeout_cycles = kTimeoutCycles;
   const int D = p.d_head;
   CUtensorMap mk, mv, mq, mdo;

@@ -16,8 +16,8 @@ using bf16 = __nv_bfloat16;
 struct WsHeader {
   int status;       // first error code raised by a kernel, 0 if none
   int qtab_count;   // number of query blocks in the long-range schedule
-  int item_counter[2];  // next work item of the window / long-range attention kernel
-  int pad[60];
+  int item_counter[4];  // next work item of each persistent attention kernel of a call
+  int pad[58];
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 
