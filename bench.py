@@ -171,6 +171,19 @@ def oracle_time_tokens(wl, inputs_cpu, target_s: float, seed: int = 11):
     return 1.0 / sec_per_token, cores, desc, t_route + t_attn
 
 
+def oracle_single_core_tiny():
+    """The oracle on one host core over the whole tiny workload (N = 512, 2 heads):
+    routing of every token and attention of every row.  Returns tokens/s."""
+    import oracle
+    wl = synth.WORKLOADS["tiny"]
+    x = synth.make_inputs(wl, seed=0, device="cpu")
+    t0 = time.perf_counter()
+    mask, _, _, _ = oracle.route(x["r"], x["C"], K=wl.K, top_k=wl.top_k,
+                                 sinkhorn_iters=wl.sinkhorn_iters, sinkhorn_eps=wl.sinkhorn_eps)
+    oracle.attn(x["q"], x["k"], x["v"], mask, w=wl.w, n_threads=1)
+    return wl.B * wl.N / (time.perf_counter() - t0)
+
+
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -392,7 +405,10 @@ def run_focus(args):
         xc = {n: t.cpu() for n, t in x.items()}
         v, cores, desc, secs = oracle_time_tokens(wl, xc, args.cpu_seconds)
         line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
-                                "sample": desc, "seconds": secs}
+                                "sample": desc, "seconds": secs,
+                                "single_core_tiny": {"value": oracle_single_core_tiny(), "unit": UNIT,
+                                                     "cores": 1, "sample": "whole tiny workload "
+                                                     "(N=512, 2 heads, d=64): routing + every row"}}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist is not None:
