@@ -23,14 +23,17 @@
 //   bwd_dkdv<D, LONG>  key-major: 128 key rows of one KV head per item (K and V
 //                      resident in shared memory), every query head of its group;
 //                      per 128-query tile: S^T = K Q^T, dP^T = V dO^T, P^T and dS^T
-//                      (bf16) written over them, dV += P^T dO, dK += dS^T Q.
+//                      (bf16) written over them, dV += P^T dO, dK += dS^T Q (each
+//                      warpgroup hands over its first 16 query columns before the
+//                      other 16, so half of the dV, dK products overlap the rest).
 // TMEM (512 columns): dQ kernel S | dP | dS | dO | dQ, dK/dV kernel S^T | dP^T | dK | dV.
 // The window pass writes fp32 partials; the long-range pass adds them and writes
 // the bf16 gradients (the two key sets are disjoint, so the sums are the totals).
 //
 // Warps: 0-15 elementwise (four warpgroups, each 32 columns of every tile, lane =
 // TMEM row), 16 producer (TMA; in bwd_dkdv the whole warp also stages the tile's
-// per-query LSE, D and position), 17 MMA issuer.
+// per-query LSE, D and position; it also draws the work items from a global counter
+// and passes them to the other warps through a shared-memory ring), 17 MMA issuer.
 #include <math.h>
 
 #include <mutex>
