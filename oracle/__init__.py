@@ -44,25 +44,59 @@ def build(force: bool = False) -> str:
     return _LIB_PATH
 
 
+def _open(path: str):
+    """The oracle library at `path` with its entry points' signatures."""
+    lib = ctypes.CDLL(path)
+    P = ctypes.c_void_p
+    i32, f64, i64 = ctypes.c_int, ctypes.c_double, ctypes.c_int64
+    lib.oracle_route.argtypes = [i32, i32, i32, i32, i32, i32, f64, i32, P, P, P, P, P, P]
+    lib.oracle_route.restype = i32
+    lib.oracle_allowed_pairs.argtypes = [i32, i32, i32, i32, P, P]
+    lib.oracle_allowed_pairs.restype = i32
+    lib.oracle_attn.argtypes = [i32, i32, i32, i32, i32, i32, i32, f64, P, P, P, P, P, i64, P, i32,
+                                P, P, i32]
+    lib.oracle_attn.restype = i32
+    lib.oracle_attn_bwd.argtypes = [i32, i32, i32, i32, i32, i32, i32, f64, P, P, P, P, P, P, P,
+                                    i64, P, i64, P, i32, P, P, P, P, P, P, f64, i32]
+    lib.oracle_attn_bwd.restype = i32
+    return lib
+
+
 def _load():
     global _lib
     if _lib is None:
         build()
-        lib = ctypes.CDLL(_LIB_PATH)
-        P = ctypes.c_void_p
-        i32, f64, i64 = ctypes.c_int, ctypes.c_double, ctypes.c_int64
-        lib.oracle_route.argtypes = [i32, i32, i32, i32, i32, i32, f64, i32, P, P, P, P, P, P]
-        lib.oracle_route.restype = i32
-        lib.oracle_allowed_pairs.argtypes = [i32, i32, i32, i32, P, P]
-        lib.oracle_allowed_pairs.restype = i32
-        lib.oracle_attn.argtypes = [i32, i32, i32, i32, i32, i32, i32, f64, P, P, P, P, P, i64, P, i32,
-                                    P, P, i32]
-        lib.oracle_attn.restype = i32
-        lib.oracle_attn_bwd.argtypes = [i32, i32, i32, i32, i32, i32, i32, f64, P, P, P, P, P, P, P,
-                                        i64, P, i64, P, i32, P, P, P, P, P, P, f64, i32]
-        lib.oracle_attn_bwd.restype = i32
-        _lib = lib
+        _lib = _open(_LIB_PATH)
     return _lib
+
+
+def compile_variant(source: str, out_path: str) -> str:
+    """Compile a variant of the oracle's C source with the same flags (tests plant
+    mistakes in copies of the source to check that the pins reject them)."""
+    src_path = out_path[:-3] + ".c" if out_path.endswith(".so") else out_path + ".c"
+    with open(src_path, "w") as f:
+        f.write(source)
+    subprocess.check_call(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared",
+                           "-pthread", src_path, "-o", out_path, "-lm"])
+    return out_path
+
+
+class use_library:
+    """Context manager: the module's functions call the library at `path` inside it."""
+
+    def __init__(self, path: str):
+        self.path = path
+
+    def __enter__(self):
+        global _lib
+        self.saved = _load()
+        _lib = _open(self.path)
+        return self
+
+    def __exit__(self, *exc):
+        global _lib
+        _lib = self.saved
+        return False
 
 
 def _ptr(a: np.ndarray | None):

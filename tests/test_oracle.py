@@ -140,6 +140,20 @@ def test_sinkhorn_matches_probability_domain_matrix_scaling():
     np.testing.assert_array_equal(mask[0, 0], want)
 
 
+def test_sinkhorn_first_column_potentials_closed_form():
+    """One iteration: the row potentials are still zero at the column step, so
+    beta_g = log(N / K) - log sum_i exp(s_ig / eps) exactly (target mass N / K per
+    group; a constant shift of every beta_g would leave the masks unchanged, so only
+    this pins the level)."""
+    N, K, eps = 300, 5, 0.8
+    r, C = _routing(2, N, 1, K, seed=29)
+    _, _, _, beta = oracle.route(r, C, K=K, top_k=2, sinkhorn_iters=1, sinkhorn_eps=eps)
+    s = np.einsum("bnt,gt->bng", r[:, :, 0].astype(np.float64), C.astype(np.float64)) / eps
+    m = s.max(axis=1, keepdims=True)
+    lse = (m + np.log(np.exp(s - m).sum(axis=1, keepdims=True)))[:, 0]
+    np.testing.assert_allclose(beta[:, 0], math.log(N / K) - lse, atol=1e-12, rtol=0)
+
+
 def test_sinkhorn_eps_is_a_score_scale():
     r, C = _routing(1, 300, 1, 4, seed=19)
     a, _, ka, _ = oracle.route(r, C, K=4, top_k=2, sinkhorn_iters=3, sinkhorn_eps=1.0)
@@ -222,6 +236,7 @@ def _dense_reference(q, k, v, mask, w, scale):
     (2, 97, 4, 2, 2, 8, 5, 1, 9),
     (1, 64, 4, 1, 1, 32, 3, 1, 1),
     (1, 50, 2, 2, 2, 8, 8, 3, 64),
+    (1, 60, 8, 4, 2, 8, 4, 2, 5),  # two KV heads per routing head: the routing-head map shows
 ])
 def test_attention_matches_dense_masked_softmax(B, N, H, H_kv, R, d, K, top_k, w):
     q, k, v = _bf16((B, N, H, d), 1), _bf16((B, N, H_kv, d), 2), _bf16((B, N, H_kv, d), 3)
@@ -412,6 +427,43 @@ def test_unit_window_top1_gradients_are_per_group_causal_autograd():
         np.testing.assert_allclose(dq[idx], gq[0], atol=1e-11, rtol=0)
         np.testing.assert_allclose(dk[idx], gk[0], atol=1e-11, rtol=0)
         np.testing.assert_allclose(dv[idx], gv[0], atol=1e-11, rtol=0)
+
+
+def _dense_masked_grads(q, k, v, mask, dout, w, scale):
+    """torch autograd (fp64) through an explicit masked softmax, one (b, h) at a time,
+    with the attended set built from the definition for h's routing head."""
+    B, N, H, d = q.shape
+    H_kv, R = k.shape[2], mask.shape[1]
+    qt = q.to(torch.float64).requires_grad_()
+    kt = k.to(torch.float64).requires_grad_()
+    vt = v.to(torch.float64).requires_grad_()
+    g = dout.to(torch.float64)
+    loss = torch.zeros((), dtype=torch.float64)
+    for b in range(B):
+        for h in range(H):
+            kvh = h // (H // H_kv)
+            rho = kvh // (H_kv // R)
+            A = torch.from_numpy(_dense_allowed(mask[b, rho], w))
+            S = (scale * qt[b, :, h] @ kt[b, :, kvh].T).masked_fill(~A, float("-inf"))
+            loss = loss + ((torch.softmax(S, dim=1) @ vt[b, :, kvh]) * g[b, :, h]).sum()
+    loss.backward()
+    return qt.grad.numpy(), kt.grad.numpy(), vt.grad.numpy()
+
+
+@pytest.mark.parametrize("B,N,H,H_kv,R,d,K,top_k,w", [
+    (1, 60, 8, 4, 2, 8, 4, 2, 5), (2, 45, 4, 2, 1, 16, 5, 2, 3)])
+def test_gradients_match_dense_masked_softmax_autograd(B, N, H, H_kv, R, d, K, top_k, w):
+    """General masks, GQA and several routing heads: the oracle's gradients against
+    torch autograd through the dense masked softmax."""
+    q, k, v = _bf16((B, N, H, d), 91), _bf16((B, N, H_kv, d), 92), _bf16((B, N, H_kv, d), 93)
+    dout = _bf16((B, N, H, d), 94)
+    r, C = _routing(B, N, R, K, seed=95)
+    mask, _, _, _ = oracle.route(r, C, K=K, top_k=top_k)
+    dq, dk, dv = oracle.attn_bwd(q, k, v, mask, dout, w=w)
+    gq, gk, gv = _dense_masked_grads(q, k, v, mask, dout, w, 1.0 / math.sqrt(d))
+    np.testing.assert_allclose(dq, gq.reshape(B * N, H, d), atol=1e-11, rtol=0)
+    np.testing.assert_allclose(dk, gk.reshape(B * N, H_kv, d), atol=1e-11, rtol=0)
+    np.testing.assert_allclose(dv, gv.reshape(B * N, H_kv, d), atol=1e-11, rtol=0)
 
 
 @pytest.mark.parametrize("B,N,H,H_kv,R,d,K,top_k,w", [
