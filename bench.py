@@ -5,14 +5,17 @@
 
 A step is one full forward pass (routing, bucketing, permuted copies, long-range
 and window attention with the union merge) over one synthetic batch whose inputs
-are already resident in HBM.  Timing: W untimed warm-up steps, then K steps
-between CUDA events on the launching stream, bracketed by barrier + synchronize,
-max over ranks.  Each rank processes its own independent problem (weak scaling,
-no collective on the data path).  The inputs (Q/K/V) are larger than L2, so no
-flush is needed between steps.
+are already resident in HBM.  The default workload is the largest one that fits
+one GPU: the 1M-token GQA layer (32 query / 8 KV heads, d = 128, K = 4, top_k = 1,
+w = 1024).  Timing: W untimed warm-up steps, then K steps between CUDA events on
+the launching stream, bracketed by barrier + synchronize, max over ranks; the
+median of the per-step durations is reported beside the mean.  Each rank
+processes its own independent problem (weak scaling, no collective on the data
+path).  The inputs (Q/K/V) are larger than L2, so no flush is needed between
+steps.  --tokens N runs the same workload family at N tokens (for profiling).
 
 --impl reference times the CPU oracle (the only comparison implementation: the
-pages ship no code) on the host cores, on a bounded sample of query rows.
+pages ship no code) on the host cores, each step a bounded sample of query rows.
 """
 from __future__ import annotations
 
@@ -37,7 +40,7 @@ import synth  # noqa: E402
 
 METRIC = "Focus attn fwd tokens/s and allowed-pair TFLOP/s vs GB300 BF16 peak"
 UNIT = "tokens/s"
-DEFAULT_WORKLOAD = "mha7b_32k"
+DEFAULT_WORKLOAD = "extreme_1m"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_BYTES = 129 * 2**20
 
@@ -50,6 +53,8 @@ def parse_args():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(synth.WORKLOADS))
     ap.add_argument("--impl", default="focus", choices=["focus", "reference"])
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="run the workload family at this many tokens instead (profiling)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target CPU time of the oracle sample")
@@ -184,26 +189,45 @@ def oracle_single_core_tiny():
     return wl.B * wl.N / (time.perf_counter() - t0)
 
 
+def workload_of(args):
+    """The bench workload; with --tokens, the same family at that many tokens."""
+    wl = synth.WORKLOADS[args.workload]
+    if getattr(args, "tokens", 0):
+        wl = wl.replace(name=f"{wl.name}_n{args.tokens}", N=args.tokens)
+    return wl
+
+
 def run_reference(args):
+    """The oracle on the host cores, on the same workload, metric and config as the
+    GPU arm.  Each step is a bounded sample of the workload (routing of every token +
+    attention of a uniform sample of query rows, all heads), timed on the host wall
+    clock; `value` is the sampled rate in tokens/s and `ms_per_step` the measured
+    seconds of one sampled step (not of a whole-workload pass, which is reported,
+    extrapolated from the rate, under its own key)."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    wl = synth.WORKLOADS[args.workload]
+    wl = workload_of(args)
     x = synth.make_inputs(wl, seed=args.seed, device="cpu")
-    import oracle
     total = max(1, args.steps + args.warmup)
     per_step = max(2.0, min(10.0, 150.0 / total))
-    vals = []
+    vals, step_s = [], []
     desc = cores = None
     for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
         v, cores, desc, _ = oracle_time_tokens(wl, x, per_step, seed=100 + i)
+        dt = time.perf_counter() - t0
         if i >= args.warmup:
             vals.append(v)
+            step_s.append(dt)
     value = statistics.mean(vals)
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": 1000.0 * wl.B * wl.N / value, "higher_is_better": True, "scaling": "weak",
+        "ms_per_step": 1000.0 * statistics.mean(step_s),
+        "ms_per_step_median": 1000.0 * statistics.median(step_s),
+        "full_workload_ms_extrapolated": 1000.0 * wl.B * wl.N / value,
+        "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": config_of(wl),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
@@ -215,25 +239,63 @@ def run_reference(args):
 
 
 def config_of(wl):
+    """The workload description; identical in both arms of the benchmark."""
     return {"workload": wl.name, "B": wl.B, "N": wl.N, "H": wl.H, "H_kv": wl.H_kv,
             "d_head": wl.d_head, "R": wl.R, "K": wl.K, "top_k": wl.top_k, "w": wl.w,
             "sinkhorn_iters": wl.sinkhorn_iters, "softmax_scale": 1.0 / math.sqrt(wl.d_head)}
 
 
+def group_diagnostics(mask_np: np.ndarray, K: int, top_k: int, margin_np: np.ndarray | None):
+    """Group sizes and dominance per (b, routing head), from the masks the kernels
+    used, and the near-tie count of the top-k decisions.  Dominance = the largest
+    share of tokens that are members of one group (balanced: top_k / K); the pages
+    track it as the collapse signal of the grouping (thelatestinai.com list view,
+    Table 9; gist.science "Key Technical Innovation: Sinkhorn Normalization")."""
+    m = mask_np.astype(np.uint32)
+    N = m.shape[-1]
+    sizes = np.stack([((m >> g) & 1).sum(axis=-1) for g in range(K)], axis=-1)  # [B, R, K]
+    share = sizes / float(N)
+    out = {"group_sizes": sizes.tolist(), "dominance": share.max(axis=-1).tolist(),
+           "dominance_max": float(share.max()), "balanced_share": top_k / K,
+           "smallest_group_share": float(share.min())}
+    if margin_np is not None:
+        out["near_ties"] = int((margin_np < 1e-5).sum())
+        out["near_tie_threshold"] = 1e-5
+    return out
+
+
 def traffic_of(kernel_src: str, workload: str):
-    """Per-launch DRAM bytes of the dominant kernel from a committed ncu summary, if it
-    was taken on the current kernel source and this workload (else None)."""
+    """Per-launch DRAM bytes of the dominant kernel from the committed ncu summary,
+    if it was taken on the current kernel source and covers this workload (else
+    None).  The file holds one entry per workload; an entry for a workload too large
+    to capture under ncu is scaled from captures of the same family at fewer tokens
+    (the entry states how)."""
     path = os.path.join(ROOT, "profiles", "attn_long_traffic.json")
     if not os.path.exists(path):
         return None
     try:
         d = json.load(open(path))
         h = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()
-        if d.get("source_sha256") == h and d.get("workload") == workload:
-            return d.get("traffic_bytes_per_launch")
+        if d.get("source_sha256") != h:
+            return None
+        e = d.get("entries", {}).get(workload)
+        return None if e is None else e.get("traffic_bytes_per_launch")
     except Exception:
         pass
     return None
+
+
+def long_range_bytes(wl, group_lists: bool) -> float:
+    """Algorithmic DRAM bytes of one long-range launch: the permuted Q', K', V' read
+    once (bf16), the window part O_w (fp32) and LSE_w read, O (bf16) and LSE
+    written; with group lists the rows are top_k-fold and the list parts (fp32) are
+    written instead of O."""
+    rep = wl.top_k if group_lists else 1
+    qkv = 2.0 * wl.B * wl.N * rep * (wl.H + 2 * wl.H_kv) * wl.d_head
+    rows = wl.B * wl.N * wl.H
+    if group_lists:
+        return qkv + rows * rep * (4.0 * wl.d_head + 4.0)
+    return qkv + rows * (4.0 * wl.d_head + 4.0) + rows * (2.0 * wl.d_head + 4.0)
 
 
 # ------------------------------------------------------------ multi-rank --
@@ -276,7 +338,7 @@ def run_focus(args):
             dist.barrier()
         torch.cuda.synchronize()
 
-    wl = synth.WORKLOADS[args.workload]
+    wl = workload_of(args)
     p = focus.Params.from_workload(wl)
     x = synth.make_inputs(wl, seed=rank_seed(args.seed, rank), device=dev)
     ws = focus.Workspace(dev).get(p)
@@ -296,32 +358,13 @@ def run_focus(args):
     if status != 0:
         raise RuntimeError(f"device status {status}: {focus.strerror(status)}")
 
-    # exact allowed-pair accounting from the membership the kernels used
-    mask, _ = focus.route(p, x["r"], x["C"])
-    mask_np = mask.cpu().numpy().view(np.uint32)
-    cnt = pairs.allowed_pairs(mask_np, wl.w)  # [B, R]
-    heads_per_rho = wl.H // wl.R
-    allowed = int(cnt.sum()) * heads_per_rho
-    window = pairs.window_pairs(wl.N, wl.w) * wl.B * wl.H
-    longrange = allowed - window
-    flops = 4.0 * wl.d_head * allowed
-    flops_long = 4.0 * wl.d_head * longrange
-    # executed tensor-core work (whole 256 x 128 tiles, masked elements included)
-    group_lists = p.bucket_shape()[0] == focus.SCHEDULE_GROUPS
-    lt, wt = pairs.executed_tiles(mask_np, wl.w, group_lists=group_lists)
-    tile_flops = 4.0 * wl.d_head * 256 * 128
-    exec_long = tile_flops * int(lt.sum()) * heads_per_rho
-    exec_win = tile_flops * wt * wl.B * wl.H
-    causal = wl.B * wl.H * wl.N * (wl.N + 1) // 2
-
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(focus.N_STAGE_EVENTS)]
            for _ in range(K)]
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
         time.sleep(0.3)
-        for _ in range(W):
-            step()
+        step()  # the clocks ramp under load before the timed region
         barrier()
         t_start.record(stream)
         for i in range(K):
@@ -332,12 +375,33 @@ def run_focus(args):
     clocks = clk.summary()
     ms = reduce_max(t_start.elapsed_time(t_end), dist, dev)
     ms_step = ms / K
+    step_ms = [e[0].elapsed_time(e[-1]) for e in evs]
+    ms_median = reduce_max(statistics.median(step_ms), dist, dev)
     stage_ms = {}
     for si, name in enumerate(focus.STAGES):
         stage_ms[name] = statistics.mean(e[si].elapsed_time(e[si + 1]) for e in evs)
 
     value = job_throughput(world, wl.B * wl.N, ms_step / 1e3)
+
+    # exact allowed-pair accounting from the membership the kernels used
+    mask, margin = focus.route(p, x["r"], x["C"], margin=True)
+    mask_np = mask.cpu().numpy().view(np.uint32)
+    margin_np = margin.cpu().numpy()
+    cnt = pairs.allowed_pairs(mask_np, wl.w)  # [B, R]
+    heads_per_rho = wl.H // wl.R
+    allowed = int(cnt.sum()) * heads_per_rho
+    window = pairs.window_pairs(wl.N, wl.w) * wl.B * wl.H
+    longrange = allowed - window
+    flops = 4.0 * wl.d_head * allowed
+    flops_long = 4.0 * wl.d_head * longrange
     tflops = flops / (ms_step / 1e3) / 1e12
+    # executed tensor-core work (whole 256 x 128 tiles, masked elements included)
+    group_lists = p.bucket_shape()[0] == focus.SCHEDULE_GROUPS
+    lt, wt = pairs.executed_tiles(mask_np, wl.w, group_lists=group_lists)
+    tile_flops = 4.0 * wl.d_head * 256 * 128
+    exec_long = tile_flops * int(lt.sum()) * heads_per_rho
+    exec_win = tile_flops * wt * wl.B * wl.H
+    causal = wl.B * wl.H * wl.N * (wl.N + 1) // 2
 
     # end-to-end through the public host-buffer API (pinned host inputs)
     host = {n: t.cpu().pin_memory() for n, t in x.items()}
@@ -353,12 +417,15 @@ def run_focus(args):
         e_times.append(time.perf_counter() - e0)
     barrier()
     # median of the calls' wall times (a single slow call of the host process would
-    # otherwise dominate a mean of ten ~10 ms calls); the mean is reported beside it
+    # otherwise dominate a mean of a few calls); the mean is reported beside it
     e_s = reduce_max(statistics.median(e_times), dist, dev)
     e2e = {"value": job_throughput(world, wl.B * wl.N, e_s), "unit": UNIT,
            "h2d_bytes_per_step": sess.h2d_bytes(*host.values()),
            "d2h_bytes_per_step": sess.d2h_bytes(), "ms_per_step": 1e3 * e_s,
-           "ms_per_step_mean": 1e3 * statistics.mean(e_times), "calls": ke}
+           "ms_per_step_mean": 1e3 * statistics.mean(e_times), "calls": ke,
+           "over_device_ms": e_s * 1e3 / ms_step,
+           "head_groups": sess.group_sizes()}
+    del host, sess
 
     peaks, peak_src = load_peaks()
     t_long = stage_ms["attn_long"] / 1e3
@@ -371,8 +438,9 @@ def run_focus(args):
         "peak_source": f"{peak_src} bf16 dense burst",
         "peak_sustained": peaks["bf16_tflops_sustained"],
         "frac_sustained": achieved / peaks["bf16_tflops_sustained"],
-        "traffic": None if group_lists else traffic_of(
+        "traffic": traffic_of(
             os.path.join(ROOT, "learned_centroid_gated_gb300", "csrc", "attn_tc.cu"), wl.name),
+        "algorithmic_bytes_per_launch": long_range_bytes(wl, group_lists),
         "algorithmic_flops_per_launch": flops_long,
         "executed_flops_per_launch": exec_long,
         "tile_efficiency": flops_long / exec_long,
@@ -382,18 +450,19 @@ def run_focus(args):
     # route (+ 2 per Sinkhorn iteration), 3 bucketing, schedule, plan, permute,
     # window, long-range (+ the slot merge under group lists)
     launches_per_step = (1 + 2 * wl.sinkhorn_iters) + 3 + 1 + 1 + 1 + 1 + 1 \
-        + (1 if p.bucket_shape()[0] == focus.SCHEDULE_GROUPS else 0)
+        + (1 if group_lists else 0)
     qkv_bytes = sum(x[n].numel() * x[n].element_size() for n in ("q", "k", "v"))
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
-        "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "ms_per_step": ms_step, "ms_per_step_median": ms_median,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic",
-        "config": dict(config_of(wl), l2=f"inputs larger than L2 (Q/K/V {qkv_bytes / 2**20:.0f} MiB "
-                                          f"> {L2_BYTES / 2**20:.0f} MiB), no flush",
-                       parallelism=f"independent problem per GPU x{world}",
-                       schedule="groups" if p.bucket_shape()[0] == focus.SCHEDULE_GROUPS
-                       else "segments"),
+        "config": config_of(wl),
+        "l2": f"inputs larger than L2 (Q/K/V {qkv_bytes / 2**20:.0f} MiB > {L2_BYTES / 2**20:.0f} MiB), "
+              "no flush",
+        "parallelism": f"independent problem per GPU x{world}",
+        "schedule": "groups" if group_lists else "segments",
         "allowed_pair_tflops": tflops,
         "allowed_pair_frac_of_peak": tflops / peaks["bf16_tflops"],
         "allowed_pairs": allowed, "allowed_fraction_of_causal": allowed / causal,
@@ -401,6 +470,7 @@ def run_focus(args):
         "window": {"algorithmic_tflops": 4.0 * wl.d_head * window / (stage_ms["attn_window"] / 1e3) / 1e12,
                    "executed_tflops": exec_win / (stage_ms["attn_window"] / 1e3) / 1e12,
                    "tile_efficiency": 4.0 * wl.d_head * window / exec_win},
+        "groups": group_diagnostics(mask_np, wl.K, wl.top_k, margin_np),
         "roofline": roofline,
         "e2e": e2e,
         "gpu_launches": launches_per_step * K,

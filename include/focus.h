@@ -84,7 +84,8 @@ enum focus_status {
   FOCUS_ERR_CUDA = -4,        /* a CUDA runtime call or launch failed */
   FOCUS_ERR_TIMEOUT = -5,     /* a bounded device-side wait ran out */
   FOCUS_ERR_BOUNDS = -6,      /* device-side index check failed (bad mask_in) */
-  FOCUS_ERR_ALIGNMENT = -7    /* a pointer is not suitably aligned */
+  FOCUS_ERR_ALIGNMENT = -7,   /* a pointer is not suitably aligned */
+  FOCUS_ERR_NONFINITE = -8    /* a routing score was NaN or infinite (non-finite r or C) */
 };
 
 typedef struct focus_params {
@@ -115,6 +116,11 @@ size_t focus_workspace_size(const focus_params* p);
  * tokens of each (b, routing head): column step beta_g = log(N/K) -
  * LSE_i(s_ig/eps + alpha_i), then row step alpha_i = -LSE_g(s_ig/eps + beta_g);
  * the ranking key is kappa_ig = s_ig/eps + beta_g. With T = 0, kappa = s.
+ * A ranking key that is not finite (NaN or +-inf, e.g. from NaN in r or C) sets
+ * FOCUS_ERR_NONFINITE in the workspace's status word (read it with
+ * focus_get_status); a NaN key ranks below every number, so such a token still
+ * gets exactly top_k groups (the lowest-indexed ones when all its keys are NaN)
+ * and nothing reads out of bounds. Its margin is then unspecified.
  */
 int focus_route(const focus_params* p, const float* r, const float* C, uint32_t* mask_out,
                 float* margin_out, void* ws, size_t ws_bytes, void* stream);
@@ -187,33 +193,47 @@ int focus_attn_fwd_ev(const focus_params* p, const uint16_t* q, const uint16_t* 
  * which such hosts must not do mid-stream). The paper has no counterpart; this is
  * a deployment variant of focus_route with identical results.
  *   Arguments and outputs as in focus_route (r, C, mask_out, optional margin_out,
- *   stream); the caller still owns every input and output buffer.
- *   Scratch: a file-scope device array of 4 MiB inside the library, held by
- *   every GPU that loads the library until the process exits. Problems needing
- *   more (256 * ceil(B*R*K*4 / 256) + B*R*ceil(N/256)*K*8 bytes) return
- *   FOCUS_ERR_WORKSPACE before anything is launched.
- *   The first call on each device looks up the array's device address (once,
- *   with that device current); make that first call before any stream capture.
+ *   stream); the caller still owns every input and output buffer. Parameter
+ *   errors give the same codes as focus_route.
+ *   Scratch: only the Sinkhorn step needs any. It lives in a file-scope device
+ *   array of focus_route_static_limit() bytes (4 MiB) inside the library, held by
+ *   every GPU that loads the library until the process exits. A Sinkhorn problem
+ *   needing more (256 * ceil(B*R*K*4 / 256) + B*R*ceil(N/256)*K*8 bytes) returns
+ *   FOCUS_ERR_WORKSPACE before anything else is checked or launched; without
+ *   Sinkhorn (sinkhorn_iters = 0) there is no size limit and the array is unused.
+ *   The array's device address is looked up (cudaGetSymbolAddress) by the first
+ *   Sinkhorn call on each device, and again by the first call under a new CUDA
+ *   context of that device (e.g. after cudaDeviceReset); make that first call
+ *   before any stream capture.
  *   All calls share the one array and nothing in it needs clearing between calls
- *   (every value is written before it is read), but calls that overlap on the GPU
- *   (concurrent streams, several host threads) race on it: serialise them.
+ *   (every value is written before it is read), but Sinkhorn calls that overlap on
+ *   the GPU (concurrent streams, several host threads) race on it: serialise them.
+ *   Non-finite routing scores are handled as in focus_route, but there is no
+ *   status word to report them.
  *   No device memory is allocated or freed by this call.
  */
 int focus_route_static(const focus_params* p, const float* r, const float* C,
                        uint32_t* mask_out, float* margin_out, void* stream);
 
+/* Size in bytes of focus_route_static's device scratch array (host only). */
+size_t focus_route_static_limit(void);
+
 /*
  * Forward pass on HOST buffers, with host-device copies overlapped with compute.
- * The heads are split into n_groups groups of consecutive KV heads (with their
- * query heads and, when R > 1, their routing heads); group g+1's inputs are copied
- * in while group g computes, and group g's outputs are copied out meanwhile.
+ * The heads are split into groups of consecutive KV heads (with their query heads
+ * and, when R > 1, their routing heads: a group holds whole routing heads); group
+ * g+1's inputs are copied in while group g computes, and group g's outputs are
+ * copied out meanwhile.
  * Each group is an independent problem (attention never mixes heads), so the
  * result equals focus_attn_fwd on the whole problem.
  *   q_h, k_h, v_h, r_h, C_h  host inputs, layouts as in focus_attn_fwd (r and C
  *                            are required: routing runs inside, per group)
  *   o_h [B, N, H, d] bf16, lse_h [B, H, N] fp32 or NULL: host outputs
- *   n_groups   number of groups, 0 = automatic (4, 2 or 1: the largest that divides
- *              H_kv and, when R > 1, R)
+ *   n_groups   > 0: that many equal groups (it must divide H_kv and, when R > 1,
+ *              R); 0 = automatic: the first group's inputs and the last group's
+ *              outputs cannot overlap any compute, so those two groups are small
+ *              (about an eighth of the KV heads each) and the others about a
+ *              quarter each (focus_host_groups lists the sizes)
  *   ws         device workspace of focus_host_workspace_size(p, n_groups) bytes
  *   compute_stream, copy_stream  two different streams (NULL = legacy default)
  * Host memory should be page-locked (cudaHostAlloc / cudaHostRegister), else the
@@ -221,13 +241,18 @@ int focus_route_static(const focus_params* p, const float* r, const float* C,
  * complete once copy_stream has been synchronised.
  */
 size_t focus_host_workspace_size(const focus_params* p, int n_groups);
+/* The groups focus_attn_fwd_host uses for (p, n_groups): writes the KV heads of
+ * each group, in order, to kv_heads[0 .. min(count, max_groups)) (kv_heads may be
+ * NULL) and returns the number of groups, or a negative FOCUS_ERR_* code. */
+int focus_host_groups(const focus_params* p, int n_groups, int32_t* kv_heads, int max_groups);
 int focus_attn_fwd_host(const focus_params* p, const uint16_t* q_h, const uint16_t* k_h,
                         const uint16_t* v_h, const float* r_h, const float* C_h, uint16_t* o_h,
                         float* lse_h, int n_groups, void* ws, size_t ws_bytes,
                         void* compute_stream, void* copy_stream);
 
 /* Synchronises `stream` and returns the device status word of the last call
- * that used this workspace (FOCUS_OK, FOCUS_ERR_TIMEOUT, FOCUS_ERR_BOUNDS), or
+ * that used this workspace (FOCUS_OK, FOCUS_ERR_TIMEOUT, FOCUS_ERR_BOUNDS,
+ * FOCUS_ERR_NONFINITE), or
  * FOCUS_ERR_CUDA if the synchronisation itself failed. */
 int focus_get_status(const void* ws, void* stream);
 

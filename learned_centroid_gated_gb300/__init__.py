@@ -36,6 +36,7 @@ FOCUS_OK = 0
 ERRORS = {
     -1: "FOCUS_ERR_INVALID_ARG", -2: "FOCUS_ERR_UNSUPPORTED", -3: "FOCUS_ERR_WORKSPACE",
     -4: "FOCUS_ERR_CUDA", -5: "FOCUS_ERR_TIMEOUT", -6: "FOCUS_ERR_BOUNDS", -7: "FOCUS_ERR_ALIGNMENT",
+    -8: "FOCUS_ERR_NONFINITE",
 }
 
 
@@ -118,6 +119,8 @@ N_STAGE_EVENTS = 6
 STAGES = ("route", "bucket", "permute", "attn_window", "attn_long")
 _lib.focus_route_static.argtypes = [_PP, _P, _P, _P, _P, _P]
 _lib.focus_route_static.restype = ctypes.c_int
+_lib.focus_route_static_limit.argtypes = []
+_lib.focus_route_static_limit.restype = ctypes.c_size_t
 _lib.focus_bwd_workspace_size.argtypes = [_PP]
 _lib.focus_bwd_workspace_size.restype = ctypes.c_size_t
 _lib.focus_attn_bwd.argtypes = [_PP, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]
@@ -219,12 +222,18 @@ def route(p: Params, r: torch.Tensor, C: torch.Tensor, *, margin: bool = False, 
     return mask, marg
 
 
+def route_static_limit() -> int:
+    """Bytes of the fixed device scratch that route_static uses for Sinkhorn."""
+    return int(_lib.focus_route_static_limit())
+
+
 def route_static(p: Params, r: torch.Tensor, C: torch.Tensor, *, margin: bool = False,
                  stream=None):
-    """route() without a workspace: the library's fixed 4 MiB device scratch is used
-    instead, for callers that must not allocate device memory when they call in.
-    The outputs here are still torch tensors; pass preallocated ones through the C
-    ABI (focus_route_static) to allocate nothing at all."""
+    """route() without a workspace: the library's fixed device scratch
+    (route_static_limit() bytes, used by the Sinkhorn step only) is used instead,
+    for callers that must not allocate device memory when they call in.  The
+    outputs here are still torch tensors; pass preallocated ones through the C ABI
+    (focus_route_static) to allocate nothing at all."""
     assert r.dtype == torch.float32 and C.dtype == torch.float32 and r.is_cuda and C.is_cuda
     mask = torch.empty(p.B, p.R, p.N, dtype=torch.int32, device=r.device)
     marg = torch.empty(p.B, p.R, p.N, dtype=torch.float32, device=r.device) if margin else None
@@ -278,6 +287,16 @@ _lib.focus_host_workspace_size.restype = ctypes.c_size_t
 _lib.focus_attn_fwd_host.argtypes = [_PP, _P, _P, _P, _P, _P, _P, _P, ctypes.c_int, _P, ctypes.c_size_t,
                                      _P, _P]
 _lib.focus_attn_fwd_host.restype = ctypes.c_int
+_lib.focus_host_groups.argtypes = [_PP, ctypes.c_int, ctypes.POINTER(ctypes.c_int32), ctypes.c_int]
+_lib.focus_host_groups.restype = ctypes.c_int
+
+
+def host_groups(p: Params, n_groups: int = 0) -> list[int]:
+    """KV heads of each head group focus_attn_fwd_host uses (in order)."""
+    buf = (ctypes.c_int32 * 64)()
+    n = _lib.focus_host_groups(ctypes.byref(p.c()), n_groups, buf, 64)
+    _check(n if n < 0 else 0, "focus_host_groups")
+    return list(buf[:n])
 
 
 def host_workspace_size(p: Params, n_groups: int = 0) -> int:
@@ -303,6 +322,10 @@ class HostSession:
         self.copy = torch.cuda.Stream(self.device)
         self.o_host = torch.empty(p.B, p.N, p.H, p.d_head, dtype=torch.bfloat16, pin_memory=True)
         self.lse_host = torch.empty(p.B, p.H, p.N, dtype=torch.float32, pin_memory=True)
+
+    def group_sizes(self) -> list[int]:
+        """KV heads of each head group, in processing order."""
+        return host_groups(self.p, self.n_groups)
 
     def h2d_bytes(self, *tensors) -> int:
         return sum(t.numel() * t.element_size() for t in tensors)

@@ -83,8 +83,12 @@ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // ------------------------------------------------------------ kernel launchers --
 // route.cu
+// status: device status word for FOCUS_ERR_NONFINITE, or nullptr
 cudaError_t launch_route(const focus_params& p, const WsLayout& L, const float* r, const float* C,
-                         char* ws, uint32_t* mask_out, float* margin_out, cudaStream_t s);
+                         char* ws, uint32_t* mask_out, float* margin_out, int* status,
+                         cudaStream_t s);
+// focus_api.cu: shape checks shared by every entry point (host only)
+int check_params(const focus_params* p);
 // bucket.cu
 cudaError_t launch_bucket(const focus_params& p, const WsLayout& L, const uint32_t* mask, char* ws,
                           cudaStream_t s);

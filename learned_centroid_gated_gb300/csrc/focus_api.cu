@@ -30,6 +30,8 @@ bool use_groups(const focus_params& p) {
   return grp < seg;
 }
 
+}  // namespace
+
 // Shape checks shared by every entry point (host only, nothing launched).
 int check_params(const focus_params* p) {
   if (!p) return FOCUS_ERR_INVALID_ARG;
@@ -49,6 +51,8 @@ int check_params(const focus_params* p) {
   if (rows >= (int64_t)INT32_MAX) return FOCUS_ERR_UNSUPPORTED;
   return FOCUS_OK;
 }
+
+namespace {
 
 WsLayout layout(const focus_params& p) {
   WsLayout L{};
@@ -189,7 +193,8 @@ int focus_route(const focus_params* p, const float* r, const float* C, uint32_t*
   cudaStream_t s = (cudaStream_t)stream;
   char* w = (char*)ws;
   if ((rc = cuda_rc(reset_header(w, s)))) return rc;
-  return cuda_rc(launch_route(*p, L, r, C, w, mask_out, margin_out, s));
+  return cuda_rc(launch_route(*p, L, r, C, w, mask_out, margin_out,
+                              &reinterpret_cast<WsHeader*>(w)->status, s));
 }
 
 int focus_bucket(const focus_params* p, const uint32_t* mask, int32_t* perm_out,
@@ -246,7 +251,9 @@ int focus_attn_fwd_ev(const focus_params* p, const uint16_t* q, const uint16_t* 
   const uint32_t* mask = mask_in;
   if (!mask) {
     uint32_t* m = reinterpret_cast<uint32_t*>(w + L.mask);
-    if ((rc = cuda_rc(launch_route(*p, L, r, C, w, m, nullptr, s)))) return rc;
+    if ((rc = cuda_rc(launch_route(*p, L, r, C, w, m, nullptr,
+                                   &reinterpret_cast<WsHeader*>(w)->status, s))))
+      return rc;
     mask = m;
   }
   if ((rc = mark(1))) return rc;
@@ -275,30 +282,76 @@ int focus_attn_fwd(const focus_params* p, const uint16_t* q, const uint16_t* k,
 // ------------------------------------------------------------ host buffers --
 namespace {
 
-int host_groups(const focus_params& p, int n_groups) {
-  auto ok = [&](int g) {
-    return g >= 1 && p.H_kv % g == 0 && (p.R == 1 || p.R % g == 0);
+// Head groups of the host-buffer entry: runs of consecutive KV heads (with their
+// query heads and, when R > 1, their routing heads), as (first KV head, KV heads).
+// A group must hold whole routing heads when R > 1, so sizes are multiples of
+// unit = H_kv / R (1 when R = 1).
+struct HostGroups {
+  int n = 0;
+  int off[64], cnt[64];
+  int max_cnt = 0;
+};
+
+// n_groups > 0: that many equal groups (it must divide H_kv and, when R > 1, R).
+// n_groups == 0: automatic.  The first group's inputs and the last group's outputs
+// cannot overlap any compute, so those two groups are small (about an eighth of
+// the heads each) and the rest is split into groups of about a quarter; problems
+// with fewer than four units use equal groups of one unit.
+bool host_groups(const focus_params& p, int n_groups, HostGroups* G) {
+  const int unit = p.R == 1 ? 1 : p.H_kv / p.R;
+  const int U = p.H_kv / unit;  // units of whole routing heads
+  G->n = 0;
+  auto add = [&](int units) {
+    G->off[G->n] = (G->n ? G->off[G->n - 1] + G->cnt[G->n - 1] : 0);
+    G->cnt[G->n] = units * unit;
+    if (G->cnt[G->n] > G->max_cnt) G->max_cnt = G->cnt[G->n];
+    ++G->n;
   };
-  if (n_groups > 0) return ok(n_groups) ? n_groups : -1;
-  for (int g : {4, 2, 1})
-    if (ok(g)) return g;
-  return 1;
+  if (n_groups > 0) {
+    if (n_groups > 64 || p.H_kv % n_groups != 0 || (p.R != 1 && p.R % n_groups != 0)) return false;
+    const int per = p.H_kv / n_groups;
+    for (int g = 0; g < n_groups; ++g) {
+      G->off[g] = g * per;
+      G->cnt[g] = per;
+    }
+    G->n = n_groups;
+    G->max_cnt = per;
+    return true;
+  }
+  if (U < 4) {
+    for (int g = 0; g < U; ++g) add(1);
+    return true;
+  }
+  const int edge = U / 8 > 1 ? U / 8 : 1;
+  const int mid = U - 2 * edge;
+  const int quarter = U / 4 > 1 ? U / 4 : 1;
+  const int n_mid = (mid + quarter - 1) / quarter;
+  if (2 + n_mid > 64) return false;
+  add(edge);
+  for (int g = 0, left = mid; g < n_mid; ++g) {
+    const int take = left / (n_mid - g);  // near-equal middle groups
+    add(take);
+    left -= take;
+  }
+  add(edge);
+  return true;
 }
 
-focus_params group_params(const focus_params& p, int G) {
+focus_params group_params(const focus_params& p, int kv_cnt) {
   focus_params q = p;
-  q.H = p.H / G;
-  q.H_kv = p.H_kv / G;
-  q.R = p.R == 1 ? 1 : p.R / G;
+  const int gq = p.H / p.H_kv;
+  q.H = kv_cnt * gq;
+  q.H_kv = kv_cnt;
+  q.R = p.R == 1 ? 1 : kv_cnt / (p.H_kv / p.R);
   return q;
 }
 
 struct HostLayout {
-  size_t q, k, v, o, lse, r, set_bytes, C, attn, total;
+  size_t q, k, v, o, lse, r, set_bytes, C, attn, attn_bytes, total;
 };
 
-HostLayout host_layout(const focus_params& p, int G) {
-  const focus_params g = group_params(p, G);
+HostLayout host_layout(const focus_params& p, const HostGroups& G) {
+  const focus_params g = group_params(p, G.max_cnt);
   HostLayout H{};
   size_t off = 0;
   auto take = [&](size_t bytes) {
@@ -316,7 +369,8 @@ HostLayout host_layout(const focus_params& p, int G) {
   H.set_bytes = off;
   off = 2 * H.set_bytes;  // two staging sets
   H.C = take((size_t)p.K * FOCUS_D_G * 4);
-  H.attn = take(layout(g).total);
+  H.attn_bytes = layout(g).total;  // the largest group's workspace serves every group
+  H.attn = take(H.attn_bytes);
   H.total = off;
   return H;
 }
@@ -325,9 +379,18 @@ HostLayout host_layout(const focus_params& p, int G) {
 
 size_t focus_host_workspace_size(const focus_params* p, int n_groups) {
   if (check_params(p) != FOCUS_OK) return 0;
-  const int G = host_groups(*p, n_groups);
-  if (G < 1) return 0;
+  HostGroups G;
+  if (!host_groups(*p, n_groups, &G)) return 0;
   return host_layout(*p, G).total;
+}
+
+int focus_host_groups(const focus_params* p, int n_groups, int32_t* kv_heads, int max_groups) {
+  int rc = check_params(p);
+  if (rc) return rc;
+  HostGroups G;
+  if (!host_groups(*p, n_groups, &G)) return FOCUS_ERR_INVALID_ARG;
+  for (int g = 0; kv_heads && g < G.n && g < max_groups; ++g) kv_heads[g] = G.cnt[g];
+  return G.n;
 }
 
 int focus_attn_fwd_host(const focus_params* p, const uint16_t* q_h, const uint16_t* k_h,
@@ -337,19 +400,19 @@ int focus_attn_fwd_host(const focus_params* p, const uint16_t* q_h, const uint16
   int rc = check_params(p);
   if (rc) return rc;
   if (!q_h || !k_h || !v_h || !r_h || !C_h || !o_h) return FOCUS_ERR_INVALID_ARG;
-  const int G = host_groups(*p, n_groups);
-  if (G < 1) return FOCUS_ERR_INVALID_ARG;
+  HostGroups G;
+  if (!host_groups(*p, n_groups, &G)) return FOCUS_ERR_INVALID_ARG;
   if (compute_stream == copy_stream) return FOCUS_ERR_INVALID_ARG;
   const HostLayout HL = host_layout(*p, G);
   if (!ws) return FOCUS_ERR_INVALID_ARG;
   if (!aligned(ws, 256)) return FOCUS_ERR_ALIGNMENT;
   if (ws_bytes < HL.total) return FOCUS_ERR_WORKSPACE;
-  const focus_params gp = group_params(*p, G);
-  const size_t attn_bytes = layout(gp).total;
   cudaStream_t cs = (cudaStream_t)compute_stream, xs = (cudaStream_t)copy_stream;
   char* w = (char*)ws;
   const size_t d2 = (size_t)p->d_head * 2;
   const size_t BN = (size_t)p->B * p->N;
+  const int gq = p->H / p->H_kv;                   // query heads per KV head
+  const int kv_per_rho = p->H_kv / p->R;           // KV heads per routing head
 
   cudaEvent_t ev_in[2], ev_comp[2];
   for (int i = 0; i < 2; ++i) {
@@ -367,34 +430,38 @@ int focus_attn_fwd_host(const focus_params* p, const uint16_t* q_h, const uint16
   auto set_ptr = [&](int g, size_t off) { return w + (g & 1) * HL.set_bytes + off; };
   // inputs of group g into staging set g % 2 (strided 2-D copies out of the host layout)
   auto copy_in = [&](int g) -> cudaError_t {
+    const focus_params gp = group_params(*p, G.cnt[g]);
+    const size_t kv0 = (size_t)G.off[g], h0 = kv0 * gq;
     cudaError_t e;
     if (g >= 2 && (e = cudaStreamWaitEvent(xs, ev_comp[g & 1], 0)) != cudaSuccess) return e;
-    if ((e = cudaMemcpy2DAsync(set_ptr(g, HL.q), gp.H * d2, q_h + (size_t)g * gp.H * p->d_head,
-                               p->H * d2, gp.H * d2, BN, cudaMemcpyHostToDevice, xs)))
+    if ((e = cudaMemcpy2DAsync(set_ptr(g, HL.q), gp.H * d2, q_h + h0 * p->d_head, p->H * d2,
+                               gp.H * d2, BN, cudaMemcpyHostToDevice, xs)))
       return e;
-    if ((e = cudaMemcpy2DAsync(set_ptr(g, HL.k), gp.H_kv * d2, k_h + (size_t)g * gp.H_kv * p->d_head,
+    if ((e = cudaMemcpy2DAsync(set_ptr(g, HL.k), gp.H_kv * d2, k_h + kv0 * p->d_head,
                                p->H_kv * d2, gp.H_kv * d2, BN, cudaMemcpyHostToDevice, xs)))
       return e;
-    if ((e = cudaMemcpy2DAsync(set_ptr(g, HL.v), gp.H_kv * d2, v_h + (size_t)g * gp.H_kv * p->d_head,
+    if ((e = cudaMemcpy2DAsync(set_ptr(g, HL.v), gp.H_kv * d2, v_h + kv0 * p->d_head,
                                p->H_kv * d2, gp.H_kv * d2, BN, cudaMemcpyHostToDevice, xs)))
       return e;
     const size_t rw = (size_t)gp.R * FOCUS_D_G * 4;
-    const float* rsrc = r_h + (p->R == 1 ? 0 : (size_t)g * gp.R * FOCUS_D_G);
+    const float* rsrc = r_h + (p->R == 1 ? 0 : (kv0 / kv_per_rho) * FOCUS_D_G);
     if ((e = cudaMemcpy2DAsync(set_ptr(g, HL.r), rw, rsrc, (size_t)p->R * FOCUS_D_G * 4, rw, BN,
                                cudaMemcpyHostToDevice, xs)))
       return e;
     return cudaEventRecord(ev_in[g & 1], xs);
   };
   auto copy_out = [&](int g) -> cudaError_t {
+    const focus_params gp = group_params(*p, G.cnt[g]);
+    const size_t h0 = (size_t)G.off[g] * gq;
     cudaError_t e;
     if ((e = cudaStreamWaitEvent(xs, ev_comp[g & 1], 0))) return e;
-    if ((e = cudaMemcpy2DAsync(o_h + (size_t)g * gp.H * p->d_head, p->H * d2, set_ptr(g, HL.o),
-                               gp.H * d2, gp.H * d2, BN, cudaMemcpyDeviceToHost, xs)))
+    if ((e = cudaMemcpy2DAsync(o_h + h0 * p->d_head, p->H * d2, set_ptr(g, HL.o), gp.H * d2,
+                               gp.H * d2, BN, cudaMemcpyDeviceToHost, xs)))
       return e;
     if (lse_h &&
-        (e = cudaMemcpy2DAsync(lse_h + (size_t)g * gp.H * p->N, (size_t)p->H * p->N * 4,
-                               set_ptr(g, HL.lse), (size_t)gp.H * p->N * 4,
-                               (size_t)gp.H * p->N * 4, p->B, cudaMemcpyDeviceToHost, xs)))
+        (e = cudaMemcpy2DAsync(lse_h + h0 * p->N, (size_t)p->H * p->N * 4, set_ptr(g, HL.lse),
+                               (size_t)gp.H * p->N * 4, (size_t)gp.H * p->N * 4, p->B,
+                               cudaMemcpyDeviceToHost, xs)))
       return e;
     return cudaSuccess;
   };
@@ -403,18 +470,20 @@ int focus_attn_fwd_host(const focus_params* p, const uint16_t* q_h, const uint16
                                     cudaMemcpyHostToDevice, xs))))
     return cleanup(rc);
   if ((rc = cuda_rc(copy_in(0)))) return cleanup(rc);
-  for (int g = 0; g < G; ++g) {
-    if (g + 1 < G && (rc = cuda_rc(copy_in(g + 1)))) return cleanup(rc);
+  for (int g = 0; g < G.n; ++g) {
+    if (g + 1 < G.n && (rc = cuda_rc(copy_in(g + 1)))) return cleanup(rc);
     // compute of group g: inputs landed; staging outputs of set g % 2 were copied out
     // (copy_out(g - 2) precedes copy_in(g) on the copy stream, which the event covers)
     if ((rc = cuda_rc(cudaStreamWaitEvent(cs, ev_in[g & 1], 0)))) return cleanup(rc);
+    const focus_params gp = group_params(*p, G.cnt[g]);
     rc = focus_attn_fwd(&gp, reinterpret_cast<const uint16_t*>(set_ptr(g, HL.q)),
                         reinterpret_cast<const uint16_t*>(set_ptr(g, HL.k)),
                         reinterpret_cast<const uint16_t*>(set_ptr(g, HL.v)),
                         reinterpret_cast<const float*>(set_ptr(g, HL.r)),
                         reinterpret_cast<const float*>(w + HL.C), nullptr,
                         reinterpret_cast<uint16_t*>(set_ptr(g, HL.o)),
-                        reinterpret_cast<float*>(set_ptr(g, HL.lse)), w + HL.attn, attn_bytes, cs);
+                        reinterpret_cast<float*>(set_ptr(g, HL.lse)), w + HL.attn, HL.attn_bytes,
+                        cs);
     if (rc) return cleanup(rc);
     if ((rc = cuda_rc(cudaEventRecord(ev_comp[g & 1], cs)))) return cleanup(rc);
     if ((rc = cuda_rc(copy_out(g)))) return cleanup(rc);
@@ -549,6 +618,7 @@ const char* focus_strerror(int code) {
     case FOCUS_ERR_TIMEOUT: return "device wait timed out";
     case FOCUS_ERR_BOUNDS: return "device index check failed (mask with wrong bit count?)";
     case FOCUS_ERR_ALIGNMENT: return "misaligned pointer";
+    case FOCUS_ERR_NONFINITE: return "non-finite routing score (NaN or inf in r or C)";
     default: return "unknown status";
   }
 }

@@ -141,11 +141,14 @@ __global__ void sinkhorn_col_final(int N, int K, int nblk, const float2* __restr
   beta[br * K + g] = (float)log((double)N / (double)K) - lse;
 }
 
-// Top-k membership.  One thread per (b, n, rho) in r's memory order.
+// Top-k membership.  One thread per (b, n, rho) in r's memory order.  A ranking
+// key that is not finite (NaN or +-inf, from non-finite r or C or an overflow)
+// raises FOCUS_ERR_NONFINITE when `status` is given; a NaN key ranks as -inf, so
+// the token's membership is still well defined (ties go to the lower group).
 __global__ void __launch_bounds__(kRouteThreads)
 route_topk(int B, int N, int R, int K, int top_k, int use_beta, float eps,
            const float* __restrict__ r, const float* __restrict__ C, const float* __restrict__ beta,
-           uint32_t* __restrict__ mask, float* __restrict__ margin) {
+           uint32_t* __restrict__ mask, float* __restrict__ margin, int* status) {
   __shared__ float Cs[FOCUS_MAX_K * 16];
   for (int t = threadIdx.x; t < K * 16; t += blockDim.x) Cs[t] = C[t];
   __syncthreads();
@@ -166,6 +169,15 @@ route_topk(int B, int N, int R, int K, int top_k, int use_beta, float eps,
       for (int g = 0; g < FOCUS_MAX_K; ++g)
         if (g < K) key[g] += __ldg(beta + br * K + g);
     }
+    bool finite = true;
+#pragma unroll
+    for (int g = 0; g < FOCUS_MAX_K; ++g) {
+      if (g < K && !isfinite(key[g])) {
+        finite = false;
+        if (isnan(key[g])) key[g] = -INFINITY;
+      }
+    }
+    if (!finite && status) raise_status(status, FOCUS_ERR_NONFINITE);
     uint32_t bits = 0;
     float kth = 0.0f;
     for (int sel = 0; sel < top_k; ++sel) {
@@ -200,7 +212,8 @@ route_topk(int B, int N, int R, int K, int top_k, int use_beta, float eps,
 }  // namespace
 
 cudaError_t launch_route(const focus_params& p, const WsLayout& L, const float* r, const float* C,
-                         char* ws, uint32_t* mask_out, float* margin_out, cudaStream_t s) {
+                         char* ws, uint32_t* mask_out, float* margin_out, int* status,
+                         cudaStream_t s) {
   const int BR = p.B * p.R;
   float* beta = reinterpret_cast<float*>(ws + L.beta);
   float2* part = reinterpret_cast<float2*>(ws + L.skpart);
@@ -215,16 +228,17 @@ cudaError_t launch_route(const focus_params& p, const WsLayout& L, const float* 
   if (blocks > 152 * 64) blocks = 152 * 64;
   route_topk<<<(unsigned)blocks, kRouteThreads, 0, s>>>(p.B, p.N, p.R, p.K, p.top_k,
                                                         p.sinkhorn_iters > 0, p.sinkhorn_eps, r, C,
-                                                        beta, mask_out, margin_out);
+                                                        beta, mask_out, margin_out, status);
   return cudaGetLastError();
 }
 
 }  // namespace focus
 
 // ------------------------------------------------------ allocation-free entry --
-// focus_route_static: focus_route without a caller workspace.  Its scratch (the
-// Sinkhorn column partials and potentials) lives in the file-scope device array
-// below, which every GPU that loads this library holds until the process exits.
+// focus_route_static: focus_route without a caller workspace.  Its only scratch
+// (the Sinkhorn column partials and potentials) lives in the file-scope device
+// array below, which every GPU that loads this library holds until the process
+// exits.  Without Sinkhorn iterations the routing needs no scratch at all.
 #include <mutex>
 
 namespace focus {
@@ -235,60 +249,91 @@ constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_route_scratch[kStaticScratchBytes];
 
+using CtxGetCurrent = int (*)(void**);  // cuCtxGetCurrent(CUcontext*)
+
+CtxGetCurrent ctx_get_current() {
+  static CtxGetCurrent fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<CtxGetCurrent>(p);
+  });
+  return fn;
+}
+
 std::mutex g_scratch_mu;
 void* g_scratch_ptr[kMaxDevices] = {};
+void* g_scratch_ctx[kMaxDevices] = {};
 
-// Device address of g_route_scratch on the current device, looked up once per
-// device (host code cannot use the symbol itself as a device pointer).
+// Device address of g_route_scratch on the current device.  Host code cannot use
+// the symbol itself as a device pointer, so the address is looked up with
+// cudaGetSymbolAddress once per device and kept with the CUDA context it belongs
+// to; a call under another context of that device (after cudaDeviceReset, say)
+// looks it up again.
 cudaError_t static_scratch(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  CtxGetCurrent get = ctx_get_current();
+  if (!get) return cudaErrorNotSupported;
   std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (!g_scratch_ptr[dev]) {
+  void* ctx = nullptr;
+  if (get(&ctx) != 0) return cudaErrorDeviceUninitialized;
+  if (!ctx || !g_scratch_ptr[dev] || g_scratch_ctx[dev] != ctx) {
+    // cudaGetSymbolAddress also makes the device's primary context current on a
+    // thread that has none yet; the context is read after it
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_route_scratch);
     if (e != cudaSuccess) return e;
+    if (get(&ctx) != 0 || !ctx) return cudaErrorDeviceUninitialized;
     g_scratch_ptr[dev] = p;
+    g_scratch_ctx[dev] = ctx;
   }
   *out = g_scratch_ptr[dev];
   return cudaSuccess;
 }
 
+// Scratch bytes of a Sinkhorn routing problem: beta [B*R, K] fp32, 256-byte
+// aligned, then the column partials [B*R, ceil(N/256), K] (max, sum) pairs.
+size_t static_scratch_need(const focus_params& p, size_t* skpart_off, int* nblk) {
+  const size_t BR = (size_t)p.B * p.R;
+  *nblk = (p.N + kSinkBlock - 1) / kSinkBlock;
+  *skpart_off = align_up(sizeof(float) * BR * p.K, 256);
+  return *skpart_off + sizeof(float2) * BR * (size_t)*nblk * p.K;
+}
+
 }  // namespace
 }  // namespace focus
+
+extern "C" size_t focus_route_static_limit(void) { return focus::kStaticScratchBytes; }
 
 extern "C" int focus_route_static(const focus_params* p, const float* r, const float* C,
                                   uint32_t* mask_out, float* margin_out, void* stream) {
   using namespace focus;
-  if (!p) return FOCUS_ERR_INVALID_ARG;
-  if (focus_workspace_size(p) == 0) {  // the shape checks of every other entry point
-    const bool shape_ok = p->B >= 1 && p->N >= 1 && p->H >= 1 && p->H_kv >= 1 && p->R >= 1 &&
-                          p->K >= 1 && p->top_k >= 1 && p->w >= 1 && p->sinkhorn_iters >= 0 &&
-                          p->H % p->H_kv == 0 && p->H_kv % p->R == 0 && p->K <= FOCUS_MAX_K &&
-                          p->top_k <= p->K &&
-                          (p->sinkhorn_iters == 0 || p->sinkhorn_eps > 0.0f);
-    return shape_ok ? FOCUS_ERR_UNSUPPORTED : FOCUS_ERR_INVALID_ARG;
-  }
+  int rc = check_params(p);  // the same shape checks and codes as focus_route
+  if (rc) return rc;
+  // The size limit comes before anything else about the call, so that an
+  // oversized problem is rejected whatever its pointers are.
+  WsLayout L{};
+  L.beta = 0;
+  if (p->sinkhorn_iters > 0 &&
+      static_scratch_need(*p, &L.skpart, &L.nblk_sk) > kStaticScratchBytes)
+    return FOCUS_ERR_WORKSPACE;
   if (!r || !C || !mask_out) return FOCUS_ERR_INVALID_ARG;
   if ((uintptr_t)r % 16 || (uintptr_t)C % 4 || (uintptr_t)mask_out % 4 ||
       (uintptr_t)margin_out % 4)
     return FOCUS_ERR_ALIGNMENT;
-  // Scratch layout inside the static array: beta [B*R, K] fp32, then the column
-  // partials [B*R, ceil(N/256), K] (max, sum) pairs.  Every partial is written
-  // before it is read and beta is not read before the first column step writes
-  // it, so nothing has to be cleared between calls.
-  WsLayout L{};
-  const size_t BR = (size_t)p->B * p->R;
-  L.nblk_sk = (p->N + kSinkBlock - 1) / kSinkBlock;
-  L.beta = 0;
-  L.skpart = align_up(sizeof(float) * BR * p->K, 256);
-  const size_t need = L.skpart + sizeof(float2) * BR * (size_t)L.nblk_sk * p->K;
-  if (need > kStaticScratchBytes) return FOCUS_ERR_WORKSPACE;
+  // Every partial is written before it is read and beta is not read before the
+  // first column step writes it, so nothing in the array needs clearing between
+  // calls.  Without Sinkhorn no kernel touches the array.
   void* scratch = nullptr;
-  if (static_scratch(&scratch) != cudaSuccess) return FOCUS_ERR_CUDA;
+  if (p->sinkhorn_iters > 0 && static_scratch(&scratch) != cudaSuccess) return FOCUS_ERR_CUDA;
   const cudaError_t e = launch_route(*p, L, r, C, static_cast<char*>(scratch), mask_out,
-                                     margin_out, (cudaStream_t)stream);
+                                     margin_out, nullptr, (cudaStream_t)stream);
   return e == cudaSuccess ? FOCUS_OK : FOCUS_ERR_CUDA;
 }

@@ -13,6 +13,13 @@ import oracle
 from learned_centroid_gated_gb300 import pairs
 
 
+# Tests that hand made-up device addresses to entry points that must reject the
+# call on the host run only where no GPU is present: a regression in a check would
+# then fail the test instead of launching a kernel on a bad address.
+host_only = pytest.mark.skipif(torch.cuda.is_available(),
+                               reason="passes made-up device addresses; host-only check")
+
+
 def _params(**kw):
     base = dict(B=1, N=512, H=2, H_kv=2, d_head=64, R=1, K=4, top_k=2, w=64)
     base.update(kw)
@@ -31,7 +38,7 @@ def test_every_declared_symbol_is_exported():
 def test_version_and_strerror():
     assert focus.version() >> 16 == 1
     assert focus.strerror(0) == "ok"
-    for code in range(-7, 0):
+    for code in range(-8, 0):
         assert focus.strerror(code) not in ("", "unknown status")
     assert focus.strerror(-99) == "unknown status"
 
@@ -57,6 +64,7 @@ def _call_attn(p, q=1 << 12, k=1 << 12, v=1 << 12, r=1 << 12, C=1 << 12, mask=No
                                      P(o), P(lse), P(ws), nb, None)
 
 
+@host_only
 def test_argument_errors_are_caught_on_the_host():
     p = _params()
     E = {v: k for k, v in focus.ERRORS.items()}
@@ -116,6 +124,7 @@ def test_schedule_resolution_and_bucket_shape():
     assert focus.workspace_size(_params(**big)) == 0                   # 2^24 * 64 * 4 rows
 
 
+@host_only
 def test_host_entry_sizes_and_argument_errors():
     p = _params(H=8, H_kv=4, R=2)
     assert focus.host_workspace_size(p) > focus.workspace_size(focus.Params(**{**p.__dict__, "H": 4, "H_kv": 2, "R": 1}))
@@ -135,6 +144,7 @@ def test_host_entry_sizes_and_argument_errors():
     assert rc == E["FOCUS_ERR_WORKSPACE"]
 
 
+@host_only
 def test_backward_sizes_and_argument_errors():
     p = _params()
     n = focus.bwd_workspace_size(p)
@@ -157,3 +167,54 @@ def test_backward_sizes_and_argument_errors():
     bad[0] = P((1 << 12) + 8)                                          # misaligned q
     assert focus._lib.focus_attn_bwd(ctypes.byref(p.c()), *bad, h, n, None) == E["FOCUS_ERR_ALIGNMENT"]
     assert focus._lib.focus_attn_bwd(ctypes.byref(p.c()), *args, h, n - 1, None) == E["FOCUS_ERR_WORKSPACE"]
+
+
+def test_static_route_checks_come_before_any_launch():
+    """focus_route_static (no workspace): the same parameter codes as focus_route,
+    and the Sinkhorn size limit before the pointer checks, so every call below is
+    rejected on the host with NULL pointers and nothing can be launched."""
+    E = {v: k for k, v in focus.ERRORS.items()}
+    limit = focus.route_static_limit()
+    assert limit == 4 << 20
+
+    def static(p):
+        return focus._lib.focus_route_static(ctypes.byref(p.c()), None, None, None, None, None)
+
+    def ws_route(p):
+        return focus._lib.focus_route(ctypes.byref(p.c()), None, None, None, None, None, 0, None)
+
+    # Sinkhorn partials of this problem exceed the array: rejected by size first
+    big = _params(N=1 << 20, H=8, H_kv=8, R=8, K=32, top_k=1, sinkhorn_iters=1)
+    need = 256 * -(-8 * 32 * 4 // 256) + 8 * (big.N // 256) * 32 * 8
+    assert need > limit
+    assert static(big) == E["FOCUS_ERR_WORKSPACE"]
+    # the same shape without Sinkhorn needs no scratch: it gets to the pointer check
+    assert static(_params(N=1 << 20, H=8, H_kv=8, R=8, K=32, top_k=1)) == E["FOCUS_ERR_INVALID_ARG"]
+    # parameter errors: identical codes from both routing entry points
+    for bad in (dict(schedule=3), dict(N=0), dict(top_k=5), dict(d_head=96),
+                dict(K=16, top_k=8, schedule=focus.SCHEDULE_SEGMENTS),
+                dict(sinkhorn_iters=1, sinkhorn_eps=0.0)):
+        p = _params(**bad)
+        assert static(p) == ws_route(p) != 0, bad
+    assert focus._lib.focus_route_static(None, None, None, None, None, None) == E["FOCUS_ERR_INVALID_ARG"]
+
+
+@pytest.mark.parametrize("H_kv,R,n_groups", [(32, 1, 0), (8, 1, 0), (8, 8, 0), (16, 8, 0), (12, 1, 0),
+                                              (2, 2, 0), (1, 1, 0), (16, 4, 0), (32, 1, 4), (8, 8, 2)])
+def test_host_groups_cover_every_kv_head_once(H_kv, R, n_groups):
+    """Groups of the host-buffer entry: consecutive, covering every KV head once,
+    whole routing heads each; automatic grouping puts the smallest groups first and
+    last (their copies cannot overlap compute)."""
+    p = _params(H=2 * H_kv, H_kv=H_kv, R=R)
+    sizes = focus.host_groups(p, n_groups)
+    assert sum(sizes) == H_kv and all(s > 0 for s in sizes)
+    unit = 1 if R == 1 else H_kv // R
+    assert all(s % unit == 0 for s in sizes)
+    if n_groups:
+        assert sizes == [H_kv // n_groups] * n_groups
+    elif len(sizes) >= 3:
+        assert sizes[0] == sizes[-1] == min(sizes)
+        if H_kv // unit >= 8:  # enough units for the edges to be smaller than the rest
+            assert max(sizes) > sizes[0]
+    # the workspace is sized for the largest group
+    assert focus.host_workspace_size(p, n_groups) > 0

@@ -83,12 +83,19 @@ def test_deterministic_across_calls(schedule):
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
 
-@pytest.mark.parametrize("name,n_groups", [("tiny", 0), ("gpt2_layer", 4), ("gpt2_layer", 3),
-                                           ("gqa4_R8_small", 0), ("gqa4_R8_small", 2)])
+HOST_CASES = {"routing_pairs_16kv": synth.WORKLOADS["tiny"].replace(
+    N=700, H=16, H_kv=16, R=8, K=5, top_k=2, w=50)}
+
+
+@pytest.mark.parametrize("name,n_groups", [("tiny", 0), ("gpt2_layer", 0), ("gpt2_layer", 4),
+                                           ("gpt2_layer", 3), ("gqa4_R8_small", 0),
+                                           ("gqa4_R8_small", 2), ("routing_pairs_16kv", 0)])
 def test_host_buffer_entry_matches_device_entry(name, n_groups):
     """Grouped, copy-overlapped host entry = device entry, bit for bit (heads are
-    independent problems and each head's arithmetic is the same)."""
-    wl = SMALL[name] if name in SMALL else synth.WORKLOADS[name]
+    independent problems and each head's arithmetic is the same), with equal groups
+    and with the automatic unequal ones (small first and last group; groups of two
+    KV heads sharing one routing head in the last case)."""
+    wl = SMALL.get(name) or HOST_CASES.get(name) or synth.WORKLOADS[name]
     x = {k: v.pin_memory() for k, v in synth.make_inputs(wl, seed=4, device="cpu").items()}
     p = focus.Params.from_workload(wl)
     o_h, l_h = focus.attn_fwd_host(p, x["q"], x["k"], x["v"], x["r"], x["C"], n_groups=n_groups)
@@ -97,18 +104,24 @@ def test_host_buffer_entry_matches_device_entry(name, n_groups):
     assert torch.equal(o_h, o_d.cpu()) and torch.equal(l_h, l_d.cpu())
 
 
-# Full-size workloads: sampled query rows and, for the 1M-token case, two query
-# heads on different KV heads (the oracle's cost grows with N).
-# FOCUS_TEST_SAMPLES overrides the row count.
-FULL = {"mha7b_32k": (512, None), "gqa_128k": (256, None), "extreme_1m": (4096, [0, 31])}
+# Full-size workloads in the benchmark's launch configuration, every head: the 32K
+# layer on all of its rows, the 128K GQA layer on a seeded sample of 8192 query
+# rows, the 1M-token layer on a seeded sample of 4096 (always including 0, w-1, w
+# and N-1).  Membership is compared for all N tokens.  FOCUS_TEST_SAMPLES
+# overrides the row count of the sampled ones.
+FULL = {"mha7b_32k": None, "gqa_128k": 8192, "extreme_1m": 4096}
 
 
 @pytest.mark.parametrize("name", list(FULL))
-def test_full_size_sampled_rows(name):
+def test_full_size_rows_all_heads(name):
     wl = synth.WORKLOADS[name]
-    n = int(os.environ.get("FOCUS_TEST_SAMPLES", FULL[name][0]))
-    rows = synth.sample_queries(wl.N, n, wl.w, seed=5)
-    x, m, errs = _run(wl, seed=0, rows=rows, heads=FULL[name][1])
+    n = FULL[name]
+    rows = None
+    if n is not None:
+        n = int(os.environ.get("FOCUS_TEST_SAMPLES", n))
+        rows = synth.sample_queries(wl.N, n, wl.w, seed=5)
+    x, m, errs = _run(wl, seed=0, rows=rows)
     n_diff, n_near = compare_membership(wl, m, x["r"], x["C"])
-    print(f"{name}: {n} rows, max|dO|={errs[0]:.2e} max rel dLSE={errs[1]:.2e}, "
-          f"membership differences {n_diff} (near-ties {n_near})")
+    print(f"{name}: {wl.N if rows is None else len(rows)} rows x {wl.H} heads, "
+          f"max|dO|={errs[0]:.2e} max rel dLSE={errs[1]:.2e}, "
+          f"membership differences {n_diff} (near-ties {n_near}) over {wl.N} tokens")

@@ -75,3 +75,55 @@ def test_bad_mask_raises_bounds_status_without_fault():
     assert focus.get_status(ws) == -6
     good, _ = focus.route(p, *synth.make_routing(wl, device="cuda"), ws=ws)
     assert focus.get_status(ws) == 0
+
+
+def test_nonfinite_routing_inputs_raise_status_without_fault():
+    """A NaN routing vector and an infinite component: the kernel raises
+    FOCUS_ERR_NONFINITE, every token still gets exactly top_k groups (a NaN key ranks
+    below every number, ties to the lower group), the finite tokens match the oracle,
+    and the forward pass that routes internally completes with finite outputs."""
+    wl = synth.WORKLOADS["tiny"].replace(N=700, K=6, top_k=2, R=2, H=4, H_kv=2)
+    r, C = synth.make_routing(wl, seed=7, device="cuda")
+    r[0, 5, 0, :] = float("nan")      # every score of token 5 (routing head 0) is NaN
+    r[0, 9, 1, 3] = float("inf")      # token 9 (routing head 1): scores are +-inf
+    p = focus.Params.from_workload(wl)
+    ws = focus.Workspace("cuda").get(p)
+    mask, _ = focus.route(p, r, C, ws=ws)
+    assert focus.get_status(ws) == -8
+    m = mask_np(mask)
+    assert m[0, 0, 5] == (1 << wl.top_k) - 1
+    c3 = C[:, 3].cpu().numpy()
+    key = np.where(c3 > 0, np.inf, -np.inf)
+    want = np.argsort(-key, kind="stable")[:wl.top_k]
+    assert m[0, 1, 9] == sum(1 << int(g) for g in want)
+    bits = np.vectorize(lambda v: bin(int(v)).count("1"))(m)
+    assert (bits == wl.top_k).all()
+    finite = torch.isfinite(r).all(dim=-1).cpu().numpy()  # [B, N, R]
+    m64, marg64, _, _ = route_oracle(wl, torch.nan_to_num(r, nan=0.0, posinf=0.0), C)
+    ok = finite.transpose(0, 2, 1) & (marg64 >= NEAR_TIE)
+    np.testing.assert_array_equal(m[ok], m64[ok])
+    x = synth.make_inputs(wl, seed=7, device="cuda")
+    o, lse = focus.attn_fwd(p, x["q"], x["k"], x["v"], r, C, ws=ws)
+    assert focus.get_status(ws) == -8
+    assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()
+    # the next call on clean inputs clears the status
+    focus.route(p, *synth.make_routing(wl, seed=7, device="cuda"), ws=ws)
+    assert focus.get_status(ws) == 0
+
+
+def test_nonfinite_routing_with_sinkhorn_is_well_defined():
+    """With Sinkhorn, a NaN vector spreads through the column potentials of its
+    (b, routing head): every token of that routing head ranks all-NaN keys and gets
+    groups 0..top_k-1; the other routing head is untouched and matches the oracle."""
+    wl = synth.WORKLOADS["tiny"].replace(N=900, K=5, top_k=2, R=2, H=4, H_kv=2, sinkhorn_iters=2)
+    r, C = synth.make_routing(wl, seed=8, device="cuda")
+    r[0, 17, 0, 2] = float("nan")
+    p = focus.Params.from_workload(wl)
+    ws = focus.Workspace("cuda").get(p)
+    mask, _ = focus.route(p, r, C, ws=ws)
+    assert focus.get_status(ws) == -8
+    m = mask_np(mask)
+    assert (m[0, 0] == (1 << wl.top_k) - 1).all()
+    wl1 = wl.replace(R=1, H=2, H_kv=1)
+    r1 = r[:, :, 1:2].contiguous()
+    compare_membership(wl1, m[:, 1:2], r1, C)
