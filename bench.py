@@ -411,11 +411,13 @@ def run_focus(args):
     barrier()
     ke = max(3, min(K, 10))
     e_times = []
-    for _ in range(ke):  # each call returns after its outputs are on the host
-        e0 = time.perf_counter()
-        sess(host["q"], host["k"], host["v"], host["r"], host["C"])
-        e_times.append(time.perf_counter() - e0)
-    barrier()
+    with ClockSampler(local) as eclk:
+        for _ in range(ke):  # each call returns after its outputs are on the host
+            e0 = time.perf_counter()
+            sess(host["q"], host["k"], host["v"], host["r"], host["C"])
+            e_times.append(time.perf_counter() - e0)
+        barrier()
+    e_clocks = eclk.summary()
     # median of the calls' wall times (a single slow call of the host process would
     # otherwise dominate a mean of a few calls); the mean is reported beside it
     e_s = reduce_max(statistics.median(e_times), dist, dev)
@@ -424,7 +426,7 @@ def run_focus(args):
            "d2h_bytes_per_step": sess.d2h_bytes(), "ms_per_step": 1e3 * e_s,
            "ms_per_step_mean": 1e3 * statistics.mean(e_times), "calls": ke,
            "over_device_ms": e_s * 1e3 / ms_step,
-           "head_groups": sess.group_sizes()}
+           "head_groups": sess.group_sizes(), "clocks": e_clocks}
     del host, sess
 
     peaks, peak_src = load_peaks()

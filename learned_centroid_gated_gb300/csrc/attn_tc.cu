@@ -63,7 +63,7 @@ using namespace ptx;
 constexpr int QT = 128;        // rows per query tile (MMA M)
 constexpr int BMQ = 2 * QT;    // query rows per work item
 constexpr int BNK = kKeyTile;  // keys per tile (MMA N of S, K of P V)
-constexpr int NSTAGE = 3;      // K/V ring slots
+constexpr int NSTAGE = 4;      // K/V ring slots
 constexpr int NRING = 4;       // work items handed from the producer to the other roles
 constexpr int RING_CONSUMERS = 9;  // MMA issuer + the 8 softmax warps
 constexpr int NTHREADS = 384;
@@ -73,6 +73,7 @@ constexpr uint32_t TMEM_COLS = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescale = 8.0f;  // log2 units: rescale O only when the max grows by > 2^8
+constexpr float kSumCap = 1.8446744e19f;  // 2^64: a tile's exponentials above this retake the max
 // Register split after launch (384 threads x 168): warpgroup 2 (producer, MMA,
 // idle) drops to 104, the two softmax warpgroups rise to 192:
 // 128 * 104 + 256 * 192 = 62464 <= 384 * 168 = 64512.
@@ -238,7 +239,7 @@ attn_tc(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensor
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(b_s + 8 * t, 1);
-      mbar_init(b_p + 8 * t, 128);
+      mbar_init(b_p + 8 * t, 4);  // one arrival per softmax warp
       mbar_init(b_o + 8 * t, 1);
     }
     mbar_init(b_drain, 1);
@@ -340,20 +341,25 @@ attn_tc(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensor
       auto ring_wait = [&](int item) {
         return mbar_wait(b_full + 8 * (item % NSTAGE), (item / NSTAGE) & 1, abort_flag, status, tlim);
       };
+      // Descriptors are built once per tile; a K step only moves the start address
+      // (bits 0-13, in 16-byte units, no carry out of the field inside shared
+      // memory), so each MMA costs the issuing thread one add.
       auto issue_S = [&](int qt, uint32_t kaddr) {
+        const uint64_t da = sw128_desc(q_base + qt * L::TILE, 16, 1024);
+        const uint64_t db = sw128_desc(kaddr, 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk / 4) * L::BOX + (kk % 4) * 32;
-          umma_ss(tmem + qt * BNK, sw128_desc(q_base + qt * L::TILE + off, 16, 1024),
-                  sw128_desc(kaddr + off, 16, 1024), IS, kk > 0);
+          const uint32_t off = ((kk / 4) * L::BOX + (kk % 4) * 32) >> 4;
+          umma_ss(tmem + qt * BNK, da + off, db + off, IS, kk > 0);
         }
       };
       auto issue_PV = [&](int qt, uint32_t vaddr, bool acc) {
         // A = P in TMEM (written over the first 64 columns of S_qt), 8 columns per K step
+        const uint64_t dv = sw128_desc(vaddr, L::BOX, 1024);
 #pragma unroll
         for (int kk = 0; kk < BNK / 16; ++kk)
-          umma_ts(tmem + 2 * BNK + qt * D, tmem + qt * BNK + 8 * kk,
-                  sw128_desc(vaddr + kk * 2048, L::BOX, 1024), IPV, (acc || kk > 0) ? 1u : 0u);
+          umma_ts(tmem + 2 * BNK + qt * D, tmem + qt * BNK + 8 * kk, dv + ((kk * 2048) >> 4), IPV,
+                  (acc || kk > 0) ? 1u : 0u);
       };
       int ri = 0, gt = 0, qcnt = 0;
       bool ok = true;
@@ -375,14 +381,20 @@ attn_tc(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensor
         umma_commit(b_s + 8);
         umma_commit(b_empty + 8 * (ri % NSTAGE));
         if (n == 1) umma_commit(b_qe);
+        // A commit makes the tensor core finish everything issued before it, so
+        // the commits are gathered at two points per key step (after S_A and
+        // after S_B; measured: six commits at four points cost ~10% of the
+        // tensor core's rate).  O is signalled once per item, after its last P V;
+        // V(t) is released together with K(t+1), after S_B(t+1).
         for (int t = 0; t < n; ++t) {
           const int iv = ri + 2 * t + 1, ik = ri + 2 * t + 2;
           const uint32_t par = (uint32_t)((gt + t) & 1);
+          const bool last = t + 1 == n;
           if (!(ok = ring_wait(iv) && mbar_wait(b_p, par, abort_flag, status, tlim))) break;
           tc_fence_after();
           issue_PV(0, slot(iv), t > 0);
-          umma_commit(b_o);
-          if (t + 1 < n) {
+          if (last) umma_commit(b_o);
+          if (!last) {
             if (!(ok = ring_wait(ik))) break;
             tc_fence_after();
             issue_S(0, slot(ik));
@@ -391,14 +403,14 @@ attn_tc(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensor
           if (!(ok = mbar_wait(b_p + 8, par, abort_flag, status, tlim))) break;
           tc_fence_after();
           issue_PV(1, slot(iv), t > 0);
-          umma_commit(b_o + 8);
-          umma_commit(b_empty + 8 * (iv % NSTAGE));
-          if (t + 1 < n) {
+          if (last) umma_commit(b_o + 8);
+          if (!last) {
             issue_S(1, slot(ik));
             umma_commit(b_s + 8);
             umma_commit(b_empty + 8 * (ik % NSTAGE));
             if (t + 2 == n) umma_commit(b_qe);  // last S of this item issued
           }
+          umma_commit(b_empty + 8 * (iv % NSTAGE));
         }
         ri += 2 * n;
         gt += n;
@@ -418,6 +430,7 @@ attn_tc(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensor
     const uint32_t tO = tmem + lane_off + 2 * BNK + qt * D;
     const float sl2 = a.sl2;
     int gt = 0;
+    int o_items = 0;  // items with key tiles so far: b_o completes once per such item
     int ks_cnt = 0;  // key-set barrier uses (group lists)
     bool ok = true;
     for (int kr = 0;; ++kr) {
@@ -551,46 +564,64 @@ attn_tc(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensor
             drop32(x3, dk3);
           }
         }
-        float ma = -INFINITY, mb = -INFINITY;
-        auto max32 = [&](uint32_t(&xx)[32]) {
+        // Row max, taken lazily: the exponentials use the running estimate m_use and
+        // the tile's max is computed only while a row has none yet (m_use = -inf) or
+        // when the tile's exponentials sum past kSumCap (then the tile is redone with
+        // its max).  P keeps its relative precision at any magnitude (bf16 has fp32's
+        // exponent range) and O and l have headroom far above kSumCap * keys * |v|,
+        // so this equals the exact online softmax up to rounding, without 64 max
+        // operations per row on every tile.
+        float f = 1.0f;
+        bool rescale = false;
+        auto take_max = [&]() {
+          float mm[8];
 #pragma unroll
-          for (int i = 0; i < 32; i += 4) {
-            ma = max3(ma, __uint_as_float(xx[i]), __uint_as_float(xx[i + 1]));
-            mb = max3(mb, __uint_as_float(xx[i + 2]), __uint_as_float(xx[i + 3]));
+          for (int j = 0; j < 8; ++j) mm[j] = -INFINITY;
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            mm[i & 7] = max3(mm[i & 7], __uint_as_float(x0[i]), __uint_as_float(x1[i]));
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            mm[i & 7] = max3(mm[i & 7], __uint_as_float(x2[i]), __uint_as_float(x3[i]));
+          const float mx = max3(max3(mm[0], mm[1], mm[2]), max3(mm[3], mm[4], mm[5]),
+                                fmaxf(mm[6], mm[7])) * sl2;
+          rescale = mx > m_use + kRescale;
+          if (rescale) {
+            f = ex2(m_use - mx);  // 0 when m_use is -inf
+            l *= f;
+            m_use = mx;
           }
         };
-        max32(x0);
-        max32(x1);
-        max32(x2);
-        max32(x3);
-        const float mx = fmaxf(ma, mb) * sl2;
-        float f = 1.0f;
-        const bool rescale = mx > m_use + kRescale;
-        if (rescale) {
-          f = ex2(m_use - mx);  // 0 when m_use is -inf
-          l *= f;
-          m_use = mx;
-        }
-        const float nms = (m_use == -INFINITY) ? 0.0f : -m_use;
-        float la = 0.0f, lb = 0.0f;
+        if (__any_sync(0xffffffffu, m_use == -INFINITY)) take_max();
+        float la, lb;
         // P (bf16 pairs) goes over the first 64 TMEM columns of this tile's S, which
         // are already in registers: column 16k + i holds keys 32k + 2i and 32k + 2i + 1.
-        auto emit = [&](uint32_t(&xx)[32], int k) {
-          uint32_t pk[16];
+        auto emit_all = [&]() {
+          const float nms = (m_use == -INFINITY) ? 0.0f : -m_use;
+          la = 0.0f;
+          lb = 0.0f;
+          auto emit = [&](uint32_t(&xx)[32], int k) {
+            uint32_t pk[16];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            float y0, y1;
-            ffma2(y0, y1, __uint_as_float(xx[2 * i]), __uint_as_float(xx[2 * i + 1]), sl2, sl2, nms, nms);
-            const float p0 = ex2(y0), p1 = ex2(y1);
-            fadd2(la, lb, la, lb, p0, p1);
-            pk[i] = pack_bf16(p0, p1);
-          }
-          tmem_st16(tS + 16 * k, pk);
+            for (int i = 0; i < 16; ++i) {
+              float y0, y1;
+              ffma2(y0, y1, __uint_as_float(xx[2 * i]), __uint_as_float(xx[2 * i + 1]), sl2, sl2, nms, nms);
+              const float p0 = ex2(y0), p1 = ex2(y1);
+              fadd2(la, lb, la, lb, p0, p1);
+              pk[i] = pack_bf16(p0, p1);
+            }
+            tmem_st16(tS + 16 * k, pk);
+          };
+          emit(x0, 0);
+          emit(x1, 1);
+          emit(x2, 2);
+          emit(x3, 3);
         };
-        emit(x0, 0);
-        emit(x1, 1);
-        emit(x2, 2);
-        emit(x3, 3);
+        emit_all();
+        if (__any_sync(0xffffffffu, !(la + lb <= kSumCap))) {  // rare: the max grew a lot
+          take_max();
+          emit_all();
+        }
         l += la + lb;
         // O (from P V of earlier tiles, all complete once S of this tile is) follows
         // the new maximum; skipped while this row has seen no key (O is still zero).
@@ -608,12 +639,14 @@ attn_tc(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensor
         }
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(b_p + 8 * qt);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(b_p + 8 * qt);
       }
       if (!ok) break;
       // ---- epilogue of this item ----
       if (n > 0) {
-        ok = mbar_wait(b_o + 8 * qt, (uint32_t)((gt + n - 1) & 1), abort_flag, status, tlim);
+        ok = mbar_wait(b_o + 8 * qt, (uint32_t)(o_items & 1), abort_flag, status, tlim);
+        ++o_items;
         if (!__all_sync(0xffffffffu, ok)) {
           ok = false;
           break;

@@ -37,9 +37,25 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// As mbar_try_wait, but a thread whose phase is not complete is suspended in
+// hardware until it completes or `ns` nanoseconds pass, instead of returning at
+// once: a polling warp then takes no issue slots from the warps that share its
+// scheduler (the MMA issuer shares one with two softmax warps).
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+      "selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
+
 // About two seconds at the GB300's clocks; no legitimate wait inside one CTA comes
 // near it (the longest is one DRAM round trip behind a few MMAs).
 constexpr long long kTimeoutCycles = 4000000000LL;
+constexpr uint32_t kWaitSleepNs = 1000;  // longest single hardware suspension of a wait
 
 // Bounded wait for the phase with the given parity.  Returns false if the CTA is
 // aborting (abort flag set by any thread) or if this wait ran out after `limit`
@@ -50,7 +66,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   for (;;) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_sleep(bar, parity, kWaitSleepNs)) return true;
     if (*abort_flag) return false;
     if (clock64() - t0 > limit) {
       *abort_flag = 1;

@@ -67,6 +67,29 @@ def test_attention_all_rows(name, schedule):
 
 
 @pytest.mark.parametrize("schedule", list(SCHEDULES))
+def test_scores_growing_along_the_sequence(schedule):
+    """Scores that grow by ~100 (log2 units) from the first keys to the last, so the
+    kernels' running max lags far behind and has to be retaken mid-row (the path a
+    tile whose exponentials sum past the cap takes), in the window and long-range
+    passes; compared with the oracle on every row."""
+    wl = synth.WORKLOADS["tiny"].replace(N=1500, w=100, K=4, top_k=2)
+    x = synth.make_inputs(wl, seed=6, device="cuda")
+    g = torch.Generator(device="cuda").manual_seed(6)
+    pos = torch.arange(wl.N, device="cuda", dtype=torch.float32).view(1, wl.N, 1, 1)
+    q = (torch.rand(x["q"].shape, generator=g, device="cuda") + 0.5).to(torch.bfloat16)
+    k = ((torch.rand(x["k"].shape, generator=g, device="cuda") + 0.5) * (1 + 5 * pos / wl.N)).to(torch.bfloat16)
+    p = focus.Params.from_workload(wl, schedule=SCHEDULES[schedule])
+    mask, _ = focus.route(p, x["r"], x["C"])
+    o, lse = focus.attn_fwd(p, q, k, x["v"], mask=mask)
+    ws = focus._default_ws[str(q.device)].buf
+    assert focus.get_status(ws) == 0
+    o_ref, lse_ref = oracle.attn(q, k, x["v"], mask_np(mask), w=wl.w, scale=p.scale)
+    assert lse_ref.max() - lse_ref.min() > 40.0  # natural-log units: a wide range of maxima
+    errs = compare_outputs(o, lse, o_ref, lse_ref)
+    print(f"growing scores ({schedule}): max|dO|={errs[0]:.2e} max rel dLSE={errs[1]:.2e}")
+
+
+@pytest.mark.parametrize("schedule", list(SCHEDULES))
 def test_precomputed_mask_and_explicit_scale(schedule):
     wl = synth.WORKLOADS["tiny"].replace(N=777, w=33)
     _run(wl, seed=2, scale=0.05, use_mask_in=True, schedule=SCHEDULES[schedule])

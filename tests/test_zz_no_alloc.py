@@ -60,7 +60,7 @@ def test_static_scratch_route_matches_workspace_route(name):
 def test_static_route_without_sinkhorn_has_no_size_limit():
     """Plain top-k needs no scratch: a problem whose Sinkhorn partials would not fit
     the array runs when sinkhorn_iters = 0 and matches focus_route."""
-    wl = synth.WORKLOADS["tiny"].replace(N=300_000, R=8, H=8, H_kv=8, K=8, top_k=2)
+    wl = synth.WORKLOADS["tiny"].replace(N=1 << 20, R=8, H=8, H_kv=8, K=32, top_k=2)
     p = focus.Params.from_workload(wl)
     need = 256 * -(-p.B * p.R * p.K * 4 // 256) + p.B * p.R * -(-p.N // 256) * p.K * 8
     assert need > focus.route_static_limit()
