@@ -331,6 +331,10 @@ int focus_selftest_timeout(void* ws, size_t ws_bytes, void* stream);
 /* Static, human-readable text for a status code. */
 const char* focus_strerror(int code);
 
+/* Text of the last CUDA error behind a FOCUS_ERR_CUDA returned to this host thread
+ * (cudaGetErrorString), or "no CUDA error". */
+const char* focus_cuda_error_string(void);
+
 /* ABI version, (major << 16) | minor. */
 int focus_version(void);
 

@@ -43,7 +43,10 @@ ERRORS = {
 class FocusError(RuntimeError):
     def __init__(self, code: int, what: str):
         self.code = code
-        super().__init__(f"{what}: {ERRORS.get(code, code)} ({strerror(code)})")
+        detail = strerror(code)
+        if code == -4:  # FOCUS_ERR_CUDA: name the CUDA error behind it
+            detail += ": " + _lib.focus_cuda_error_string().decode()
+        super().__init__(f"{what}: {ERRORS.get(code, code)} ({detail})")
 
 
 class _Params(ctypes.Structure):
@@ -142,6 +145,8 @@ _lib.focus_strerror.argtypes = [ctypes.c_int]
 _lib.focus_strerror.restype = ctypes.c_char_p
 _lib.focus_version.argtypes = []
 _lib.focus_version.restype = ctypes.c_int
+_lib.focus_cuda_error_string.argtypes = []
+_lib.focus_cuda_error_string.restype = ctypes.c_char_p
 
 
 def declared_symbols() -> list[str]:

@@ -153,7 +153,14 @@ int check_ws(const WsLayout& L, const void* ws, size_t ws_bytes) {
   return FOCUS_OK;
 }
 
-int cuda_rc(cudaError_t e) { return e == cudaSuccess ? FOCUS_OK : FOCUS_ERR_CUDA; }
+// The last CUDA error an entry point met on this host thread (focus_cuda_error_string).
+thread_local cudaError_t g_last_cuda_error = cudaSuccess;
+
+int cuda_rc(cudaError_t e) {
+  if (e == cudaSuccess) return FOCUS_OK;
+  g_last_cuda_error = e;
+  return FOCUS_ERR_CUDA;
+}
 
 // Clears the status word and the schedule counter at the start of a call.
 cudaError_t reset_header(char* ws, cudaStream_t s) {
@@ -624,5 +631,9 @@ const char* focus_strerror(int code) {
 }
 
 int focus_version(void) { return (1 << 16) | 0; }
+
+const char* focus_cuda_error_string(void) {
+  return g_last_cuda_error == cudaSuccess ? "no CUDA error" : cudaGetErrorString(g_last_cuda_error);
+}
 
 }  // extern "C"
