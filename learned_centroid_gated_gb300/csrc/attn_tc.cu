@@ -160,6 +160,7 @@ struct Item {
   int br;                     // long: b * R + rho
   int seg;                    // long: segment (group list g)
   int j_lo, j_hi;             // window key range
+  int skew;                   // window: tile B's key tiles start one tile after tile A's
 };
 
 template <bool LONG>
@@ -198,6 +199,11 @@ __device__ __forceinline__ Item decode(const TcArgs& a, int x) {
     it.j_lo = max(0, it.row0 - a.w + 1);
     it.j_hi = it.row0 + it.rows;
     it.n = (it.j_hi - it.j_lo + BNK - 1) / BNK;
+    // A full block past the first w - 1 tokens: query tile A (rows row0 ..
+    // row0 + 127) needs key tiles 0 .. n - 2 and tile B (row0 + 128 .. row0 + 255)
+    // needs 1 .. n - 1 (the band of tile A ends w - 1 + 127 keys after j_lo, tile
+    // B's starts 128 keys after it), so each runs n - 1 tiles.
+    it.skew = (it.row0 >= a.w - 1 && it.rows == BMQ && it.n >= 2) ? 1 : 0;
   }
   return it;
 }
@@ -371,49 +377,64 @@ attn_tc(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensor
         if (x >= n_items) break;
         const Item it = decode<LONG>(a, x);
         if (!it.valid || it.n == 0) continue;
-        const int n = it.n;
+        // sk: the window pass's skew (0 in the long-range passes, at compile time, so
+        // their issue stream carries no extra waits: every instruction of this thread
+        // between MMA groups delays the tensor core)
+        const int n = it.n, sk = LONG ? 0 : it.skew, ns = n - sk;  // ns key steps of each tile
         if (!(ok = mbar_wait(b_q, qcnt & 1, abort_flag, status, tlim) && ring_wait(ri))) break;
+        if (sk && !(ok = ring_wait(ri + 2))) break;
         ++qcnt;
         tc_fence_after();
         issue_S(0, slot(ri));
         umma_commit(b_s);
-        issue_S(1, slot(ri));
+        issue_S(1, slot(ri + 2 * sk));
         umma_commit(b_s + 8);
         umma_commit(b_empty + 8 * (ri % NSTAGE));
-        if (n == 1) umma_commit(b_qe);
+        if (ns == 1) umma_commit(b_qe);
         // A commit makes the tensor core finish everything issued before it, so
         // the commits are gathered at two points per key step (after S_A and
         // after S_B; measured: six commits at four points cost ~10% of the
         // tensor core's rate).  O is signalled once per item, after its last P V;
         // V(t) is released together with K(t+1), after S_B(t+1).
-        for (int t = 0; t < n; ++t) {
-          const int iv = ri + 2 * t + 1, ik = ri + 2 * t + 2;
+        // Tile A's step t uses V(t) and K(t + 1), tile B's V(t + sk) and K(t + 1 + sk)
+        // (ring items V(u) = ri + 2u + 1, K(u) = ri + 2u).  At the end of step t,
+        // V(t) and K(t + 1) have had their last use; with the skew V(n - 1) too.
+        for (int t = 0; t < ns; ++t) {
+          const int iva = ri + 2 * t + 1, ika = ri + 2 * t + 2;
+          const int ivb = iva + 2 * sk, ikb = ika + 2 * sk;
           const uint32_t par = (uint32_t)((gt + t) & 1);
-          const bool last = t + 1 == n;
-          if (!(ok = ring_wait(iv) && mbar_wait(b_p, par, abort_flag, status, tlim))) break;
+          const bool last = t + 1 == ns;
+          if (!(ok = ring_wait(iva) && mbar_wait(b_p, par, abort_flag, status, tlim))) break;
           tc_fence_after();
-          issue_PV(0, slot(iv), t > 0);
+          issue_PV(0, slot(iva), t > 0);
           if (last) umma_commit(b_o);
           if (!last) {
-            if (!(ok = ring_wait(ik))) break;
+            if (!(ok = ring_wait(ika))) break;
             tc_fence_after();
-            issue_S(0, slot(ik));
+            issue_S(0, slot(ika));
             umma_commit(b_s);
           }
+          if (sk && !(ok = ring_wait(ivb))) break;
           if (!(ok = mbar_wait(b_p + 8, par, abort_flag, status, tlim))) break;
           tc_fence_after();
-          issue_PV(1, slot(iv), t > 0);
+          issue_PV(1, slot(ivb), t > 0);
           if (last) umma_commit(b_o + 8);
           if (!last) {
-            issue_S(1, slot(ik));
+            if (sk) {
+              if (!(ok = ring_wait(ikb))) break;
+              tc_fence_after();
+            }
+            issue_S(1, slot(ikb));
             umma_commit(b_s + 8);
-            umma_commit(b_empty + 8 * (ik % NSTAGE));
-            if (t + 2 == n) umma_commit(b_qe);  // last S of this item issued
+            if (t + 2 == ns) umma_commit(b_qe);  // last S of this item issued
           }
-          umma_commit(b_empty + 8 * (iv % NSTAGE));
+          if (!last) umma_commit(b_empty + 8 * (ika % NSTAGE));  // t + 1 < n
+          else if (sk) umma_commit(b_empty + 8 * (ika % NSTAGE));
+          umma_commit(b_empty + 8 * (iva % NSTAGE));
+          if (sk && last) umma_commit(b_empty + 8 * (ivb % NSTAGE));
         }
         ri += 2 * n;
-        gt += n;
+        gt += ns;
         if (!ok) break;
       }
       umma_commit(b_drain);  // every MMA issued above completes before TMEM is released
@@ -446,7 +467,7 @@ attn_tc(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensor
       if (x >= n_items) break;
       const Item it = decode<LONG>(a, x);
       if (!it.valid) continue;
-      const int n = it.n;
+      const int n = it.n - it.skew;  // key steps of this tile
       const int rg = qt * QT + r;  // row in the item
       const bool row_ok = rg < it.rows;
       const int* P = LONG ? a.perm + (int64_t)it.br * a.NR : nullptr;
@@ -489,7 +510,7 @@ attn_tc(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensor
             }
           }
         } else {
-          const int j0 = it.j_lo + t * BNK;
+          const int j0 = it.j_lo + (t + (qt ? it.skew : 0)) * BNK;
           c_lo = max(0, qp - a.w + 1 - j0);
           c_hi = min(min(BNK, it.j_hi - j0), qp - j0 + 1);
           need_mask = c_lo > 0 || c_hi < BNK;
