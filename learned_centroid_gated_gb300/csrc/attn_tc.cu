@@ -50,6 +50,8 @@
 //                      popc(mask_i & (2^g - 1)); a separate pass merges the slots.
 #include <math.h>
 
+#include <cstdlib>
+#include <cstring>
 #include <mutex>
 
 #include "common.cuh"
@@ -906,8 +908,17 @@ cudaError_t launch_timeout_selftest(char* ws, size_t ws_bytes, cudaStream_t s) {
   return launch_tc<64, kWin>(mq, mk, mv, a, 1, s);
 }
 
+// FOCUS_LONG_ENGINE=pair runs the long-range pass on CTA pairs where that engine
+// applies (d = 128, exact-set segments); otherwise this kernel runs it.  Both give
+// the same result up to rounding order.
+bool use_pair_engine(const focus_params& p, const WsLayout& L) {
+  const char* e = std::getenv("FOCUS_LONG_ENGINE");
+  return e && std::strcmp(e, "pair") == 0 && pair_engine_supported(p, L);
+}
+
 cudaError_t launch_attn_long_tc(const focus_params& p, const WsLayout& L, char* ws, bf16* o,
                                 float* lse, float scale, cudaStream_t s) {
+  if (use_pair_engine(p, L)) return launch_attn_long_pair(p, L, ws, o, lse, scale, s);
   TcArgs a = make_args(p, L, ws, scale);
   a.o = o;
   a.lse = lse;

@@ -125,6 +125,10 @@ int tc_block_rows();
 cudaError_t launch_timeout_selftest(char* ws, size_t ws_bytes, cudaStream_t s);
 cudaError_t launch_attn_long_tc(const focus_params& p, const WsLayout& L, char* ws, bf16* o,
                                 float* lse, float scale, cudaStream_t s);
+// attn_pair.cu (long-range pass on CTA pairs: d = 128, exact-set segments)
+bool pair_engine_supported(const focus_params& p, const WsLayout& L);
+cudaError_t launch_attn_long_pair(const focus_params& p, const WsLayout& L, char* ws, bf16* o,
+                                  float* lse, float scale, cudaStream_t s);
 cudaError_t launch_attn_window_tc(const focus_params& p, const WsLayout& L, const bf16* q,
                                   const bf16* k, const bf16* v, char* ws, float scale,
                                   cudaStream_t s);

@@ -42,6 +42,9 @@ SMALL = {
     "gpt2_layer": synth.WORKLOADS["gpt2_layer"],
     "single_token": synth.WORKLOADS["tiny"].replace(N=1),
     "ragged_gqa3": synth.WORKLOADS["tiny"].replace(N=300, H=3, H_kv=1, K=5, top_k=2, w=37),
+    "ragged_gqa3_d128": synth.WORKLOADS["tiny"].replace(N=300, H=3, H_kv=1, K=5, top_k=2, w=37,
+                                                        d_head=128),
+    "single_token_d128": synth.WORKLOADS["tiny"].replace(N=1, d_head=128),
     "routing_per_kv_group_d128_b2": synth.WORKLOADS["tiny"].replace(
         B=2, N=1000, H=4, H_kv=2, R=2, d_head=128, K=6, top_k=3, w=100),
     "window_covers_all": synth.WORKLOADS["tiny"].replace(N=700, w=900, d_head=128),
@@ -66,13 +69,14 @@ def test_attention_all_rows(name, schedule):
     print(f"{name} ({schedule}): max|dO|={errs[0]:.2e} max rel dLSE={errs[1]:.2e}")
 
 
+@pytest.mark.parametrize("d_head", [64, 128])
 @pytest.mark.parametrize("schedule", list(SCHEDULES))
-def test_scores_growing_along_the_sequence(schedule):
+def test_scores_growing_along_the_sequence(schedule, d_head):
     """Scores that grow by ~100 (log2 units) from the first keys to the last, so the
     kernels' running max lags far behind and has to be retaken mid-row (the path a
     tile whose exponentials sum past the cap takes), in the window and long-range
     passes; compared with the oracle on every row."""
-    wl = synth.WORKLOADS["tiny"].replace(N=1500, w=100, K=4, top_k=2)
+    wl = synth.WORKLOADS["tiny"].replace(N=1500, w=100, K=4, top_k=2, d_head=d_head)
     x = synth.make_inputs(wl, seed=6, device="cuda")
     g = torch.Generator(device="cuda").manual_seed(6)
     pos = torch.arange(wl.N, device="cuda", dtype=torch.float32).view(1, wl.N, 1, 1)
@@ -87,6 +91,26 @@ def test_scores_growing_along_the_sequence(schedule):
     assert lse_ref.max() - lse_ref.min() > 40.0  # natural-log units: a wide range of maxima
     errs = compare_outputs(o, lse, o_ref, lse_ref)
     print(f"growing scores ({schedule}): max|dO|={errs[0]:.2e} max rel dLSE={errs[1]:.2e}")
+
+
+ENGINE_CASES = {
+    "extreme_small": SMALL["extreme_small"],
+    "ragged_gqa3_d128": SMALL["ragged_gqa3_d128"],
+    "routing_per_kv_group_d128_b2": SMALL["routing_per_kv_group_d128_b2"],
+}
+
+
+@pytest.mark.parametrize("engine", ["pair", "single"])
+@pytest.mark.parametrize("name", list(ENGINE_CASES))
+def test_both_long_range_engines(name, engine, monkeypatch):
+    """FOCUS_LONG_ENGINE=pair runs the long-range pass (d = 128, exact-set segments)
+    on CTA pairs; by default the one-CTA kernel runs it.  Both against the oracle."""
+    if engine == "pair":
+        monkeypatch.setenv("FOCUS_LONG_ENGINE", "pair")
+    else:
+        monkeypatch.delenv("FOCUS_LONG_ENGINE", raising=False)
+    _, _, errs = _run(ENGINE_CASES[name], seed=4, schedule=focus.SCHEDULE_SEGMENTS)
+    print(f"{name} ({engine}): max|dO|={errs[0]:.2e} max rel dLSE={errs[1]:.2e}")
 
 
 @pytest.mark.parametrize("schedule", list(SCHEDULES))
