@@ -85,7 +85,7 @@ constexpr int kRegsHigh = 192;
 // Kernel modes: window part, long-range part over exact-set segments, over group lists.
 enum : int { kWin = 0, kSeg = 1, kGrp = 2 };
 
-template <int D>
+template <int D, int MODE>
 struct Layout {
   static constexpr int BOX = QT * 128;        // one TMA box: 128 rows x 128 bytes
   static constexpr int BOXES = D / 64;        // boxes per 128 x D tile
@@ -105,8 +105,12 @@ struct Layout {
   static_assert(RING_X + 4 * NRING <= BAR_BYTES, "barrier block overflow");
   // group lists: per query tile, two buffers of [32 group bits][4 words] key sets
   static constexpr int KSET = BAR + BAR_BYTES;
-  static constexpr int KSET_BYTES = 2 * 2 * 32 * 4 * 4;
-  static constexpr int SMEM = KSET + KSET_BYTES + 1024;  // + 1 KB alignment slack
+  static constexpr int KSET_BYTES = MODE == kGrp ? 2 * 2 * 32 * 4 * 4 : 0;
+  // window pass: per softmax warp a 32 x 32 fp32 block that turns its rows of O_w
+  // into coalesced stores
+  static constexpr int STAGE = KSET + KSET_BYTES;
+  static constexpr int STAGE_BYTES = MODE == kWin ? 8 * 32 * 32 * 4 : 0;
+  static constexpr int SMEM = STAGE + STAGE_BYTES + 1024;  // + 1 KB alignment slack
   static_assert(SMEM <= 232448, "shared memory budget");
 };
 
@@ -216,7 +220,7 @@ attn_tc(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensor
         const __grid_constant__ CUtensorMap mv, const TcArgs a, const int n_items) {
   constexpr bool LONG = MODE != kWin;
   constexpr bool GROUP = MODE == kGrp;
-  using L = Layout<D>;
+  using L = Layout<D, MODE>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -680,21 +684,30 @@ attn_tc(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensor
       const int64_t orow = (((int64_t)it.b * a.N + qp) * a.H + it.h) * D;
       const int64_t lrow = ((int64_t)it.b * a.H + it.h) * a.N + qp;
       if constexpr (!LONG) {
-        // window pass (runs first): normalised partial output and its LSE
+        // window pass (runs first): normalised partial output and its LSE.  A thread
+        // holds its row; rows are stored 32 columns at a time through this warp's
+        // 32 x 32 block in shared memory (XOR-swizzled: both the row writes and the
+        // column reads are free of bank conflicts), one 128-byte row segment per
+        // store instead of 32 scattered 16-byte pieces.  A warp's 32 rows are
+        // consecutive tokens, so row j is `H * D` floats after row 0.
         const float inv = 1.0f / l;  // the diagonal key is always in the window
         const float lse = (m_use + log2f(l)) * kLn2;
+        float* st = reinterpret_cast<float*>(sm + L::STAGE) + (warp & 7) * 32 * 32;
+        const int rg0 = qt * QT + (warp & 3) * 32;  // the warp's first row in the item
+        const int64_t orow0 = (((int64_t)it.b * a.N + it.row0 + rg0) * a.H + it.h) * D;
+        const int64_t rstride = (int64_t)a.H * D;
+        const int nrows = min(32, it.rows - rg0);  // rows of this warp inside the item
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t y[32];
           tmem_ld32(tO + 32 * c, y);
           tmem_ld_wait(y);
-          if (row_ok) {
-            float4* dst = reinterpret_cast<float4*>(a.o_part + orow + 32 * c);
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-              dst[i] = make_float4(__uint_as_float(y[4 * i]) * inv, __uint_as_float(y[4 * i + 1]) * inv,
-                                   __uint_as_float(y[4 * i + 2]) * inv, __uint_as_float(y[4 * i + 3]) * inv);
-          }
+          for (int i = 0; i < 32; ++i) st[lane * 32 + (i ^ lane)] = __uint_as_float(y[i]) * inv;
+          __syncwarp();
+          for (int j = 0; j < nrows; ++j)
+            a.o_part[orow0 + j * rstride + 32 * c + lane] = st[j * 32 + (lane ^ j)];
+          __syncwarp();
         }
         if (row_ok) a.lse_part[lrow] = lse;
       } else if constexpr (GROUP) {
@@ -866,7 +879,7 @@ TcArgs make_args(const focus_params& p, const WsLayout& L, char* ws, float scale
 template <int D, int MODE>
 cudaError_t launch_tc(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                       const TcArgs& a, int n_items, cudaStream_t s) {
-  const int smem = Layout<D>::SMEM;
+  const int smem = Layout<D, MODE>::SMEM;
   cudaError_t e = cudaFuncSetAttribute(attn_tc<D, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int sms = num_sms();
