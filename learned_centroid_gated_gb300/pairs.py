@@ -56,7 +56,10 @@ def executed_tiles(mask, w: int, block_rows: int = 256, key_tile: int = 128,
     compatible mask value's keys with pos <= (last row's pos) - w (with group_lists:
     blocks of each group's list against that list's keys); window = for every block
     of `block_rows` consecutive tokens, ceil(span / key_tile) with span the keys
-    (first row - w, last row].  Returns (long_tiles [B, R], window_tiles)."""
+    (first row - w, last row], one fewer for a full block past the first w - 1 tokens
+    with two or more key tiles (its two halves skip the band's last and first key tile
+    respectively).  Counts are in block_rows x key_tile tiles.  Returns
+    (long_tiles [B, R], window_tiles)."""
     m = np.asarray(mask).astype(np.int64) & 0xFFFFFFFF
     B, R, N = m.shape
     long_t = np.zeros((B, R), np.int64)
@@ -85,5 +88,7 @@ def executed_tiles(mask, w: int, block_rows: int = 256, key_tile: int = 128,
     starts = np.arange(0, N, block_rows)
     ends = np.minimum(starts + block_rows, N)
     span = ends - np.maximum(0, starts - w + 1)
-    win_t = int(((span + key_tile - 1) // key_tile).sum())
+    n_win = (span + key_tile - 1) // key_tile
+    skew = (starts >= w - 1) & (ends - starts == block_rows) & (n_win >= 2)
+    win_t = int((n_win - skew).sum())
     return long_t, win_t

@@ -218,3 +218,19 @@ def test_host_groups_cover_every_kv_head_once(H_kv, R, n_groups):
             assert max(sizes) > sizes[0]
     # the workspace is sized for the largest group
     assert focus.host_workspace_size(p, n_groups) > 0
+
+
+def test_window_tile_count_follows_the_skew():
+    """The window pass's executed 256 x 128 tiles: ceil(span / 128) per 256-row block,
+    one fewer for full blocks past the first w - 1 tokens (the two 128-row halves
+    each skip one end of the band), restated per block."""
+    from learned_centroid_gated_gb300 import pairs
+    for N, w in ((4096, 512), (1000, 100), (300, 37), (256, 1), (777, 1024)):
+        mask = np.ones((1, 1, N), np.uint32)
+        _, wt = pairs.executed_tiles(mask, w)
+        want = 0
+        for s0 in range(0, N, 256):
+            e0 = min(s0 + 256, N)
+            n = -(-(e0 - max(0, s0 - w + 1)) // 128)
+            want += n - (1 if (s0 >= w - 1 and e0 - s0 == 256 and n >= 2) else 0)
+        assert wt == want, (N, w, wt, want)

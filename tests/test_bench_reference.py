@@ -36,3 +36,17 @@ def test_reference_arm_prints_one_contract_line():
 
 def test_reference_arm_other_ranks_stay_silent():
     assert _run({"RANK": "1"}) == []
+
+
+def test_cpu_binding_never_raises_without_nvml_or_gpu():
+    """bench.bind_to_gpu_cpus asks NVML for the GPU-local cores; where NVML or the GPU is
+    missing it must leave the affinity alone and return None, not fail the bench."""
+    sys.path.insert(0, ROOT)
+    import bench
+    before = os.sched_getaffinity(0)
+    res = bench.bind_to_gpu_cpus(0)
+    assert res is None or (isinstance(res, list) and res)
+    if res is None:
+        assert os.sched_getaffinity(0) == before
+    else:
+        os.sched_setaffinity(0, before)
