@@ -24,6 +24,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -297,6 +298,15 @@ def group_diagnostics(mask_np: np.ndarray, K: int, top_k: int, margin_np: np.nda
     return out
 
 
+def code_hash(path: str) -> str:
+    """sha256 of a C/CUDA source with its comments and whitespace removed: a traffic
+    capture stays valid across comment edits, not across code changes."""
+    src = open(path, encoding="utf-8").read()
+    src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", " ", src)
+    return hashlib.sha256("".join(src.split()).encode()).hexdigest()
+
+
 def traffic_of(kernel_src: str, workload: str):
     """Per-launch DRAM bytes of the dominant kernel from the committed ncu summary,
     if it was taken on the current kernel source and covers this workload (else
@@ -308,8 +318,7 @@ def traffic_of(kernel_src: str, workload: str):
         return None
     try:
         d = json.load(open(path))
-        h = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()
-        if d.get("source_sha256") != h:
+        if d.get("code_sha256") != code_hash(kernel_src):
             return None
         e = d.get("entries", {}).get(workload)
         return None if e is None else e.get("traffic_bytes_per_launch")

@@ -17,7 +17,7 @@
 // most loaded one finished.  Each item is two 128-row query tiles A and B that
 // ping-pong on the tensor core:
 //   warp 8      TMA producer: Q tiles of each item, then K and V tiles through a
-//               3-slot ring; runs ahead across item boundaries
+//               4-slot ring; runs ahead across item boundaries
 //   warp 9      MMA issuer (one thread): S = Q K^T into TMEM, O += P V into TMEM
 //   warps 0-3   softmax of tile A (thread = row = TMEM lane), warps 4-7 of tile B;
 //               each warpgroup also writes its tile's output rows
