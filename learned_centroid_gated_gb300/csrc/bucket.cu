@@ -451,17 +451,37 @@ permute_qkv(int N, int NR, int H, int H_kv, int R, int d, const int* __restrict_
   const int n = perm[row];
   const int hq = H / R, hkv = H_kv / R;
   const int vec = d / 8;  // uint4 per head row
-  const int nq = hq * vec, nk = hkv * vec;
-  for (int i = threadIdx.x; i < nq + 2 * nk; i += blockDim.x) {
-    if (i < nq) {
-      const int hh = rho * hq + i / vec, c = i % vec;
-      qp[(((int64_t)b * H + hh) * NR + np) * vec + c] = q[(((int64_t)b * N + n) * H + hh) * vec + c];
-    } else {
-      const int j = (i - nq) % nk;
-      const int hh = rho * hkv + j / vec, c = j % vec;
-      const int64_t src = (((int64_t)b * N + n) * H_kv + hh) * vec + c;
-      const int64_t dst = (((int64_t)b * H_kv + hh) * NR + np) * vec + c;
-      if (i < nq + nk) kp[dst] = k[src]; else vp[dst] = v[src];
+  const int nq = hq * vec, nk = hkv * vec, total = nq + 2 * nk;
+  // Up to four 16-byte loads in flight per thread before their stores.
+  constexpr int U = 4;
+  for (int base = threadIdx.x; base < total; base += U * blockDim.x) {
+    uint4 val[U];
+    int64_t dst[U];
+    int which[U];  // 0 = Q, 1 = K, 2 = V, -1 = past the end
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int i = base + u * blockDim.x;
+      which[u] = -1;
+      if (i >= total) continue;
+      if (i < nq) {
+        const int hh = rho * hq + i / vec, c = i % vec;
+        which[u] = 0;
+        dst[u] = (((int64_t)b * H + hh) * NR + np) * vec + c;
+        val[u] = q[(((int64_t)b * N + n) * H + hh) * vec + c];
+      } else {
+        const int j = (i - nq) % nk;
+        const int hh = rho * hkv + j / vec, c = j % vec;
+        const int64_t src = (((int64_t)b * N + n) * H_kv + hh) * vec + c;
+        which[u] = i < nq + nk ? 1 : 2;
+        dst[u] = (((int64_t)b * H_kv + hh) * NR + np) * vec + c;
+        val[u] = which[u] == 1 ? k[src] : v[src];
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      if (which[u] == 0) qp[dst[u]] = val[u];
+      else if (which[u] == 1) kp[dst[u]] = val[u];
+      else if (which[u] == 2) vp[dst[u]] = val[u];
     }
   }
 }
