@@ -219,25 +219,22 @@ int focus_route_static(const focus_params* p, const float* r, const float* C,
 size_t focus_route_static_limit(void);
 
 /*
- * Forward pass on HOST buffers, with the output copies overlapped with compute.
- * The inputs are copied to the device whole (one transfer per tensor: strided reads
- * of host memory, a million rows of a few hundred bytes per head group, ran several
- * times slower than flat ones on some hosts). The heads are then processed in groups
- * of consecutive KV heads (with their query heads and, when R > 1, their routing
- * heads: a group holds whole routing heads), each group split off on the device;
- * group g's outputs are copied out while group g+1 computes.
+ * Forward pass on HOST buffers, with host-device copies overlapped with compute.
+ * The heads are split into groups of consecutive KV heads (with their query heads
+ * and, when R > 1, their routing heads: a group holds whole routing heads); group
+ * g+1's inputs are copied in while group g computes, and group g's outputs are
+ * copied out meanwhile.
  * Each group is an independent problem (attention never mixes heads), so the
  * result equals focus_attn_fwd on the whole problem.
  *   q_h, k_h, v_h, r_h, C_h  host inputs, layouts as in focus_attn_fwd (r and C
  *                            are required: routing runs inside, per group)
  *   o_h [B, N, H, d] bf16, lse_h [B, H, N] fp32 or NULL: host outputs
  *   n_groups   > 0: that many equal groups (it must divide H_kv and, when R > 1,
- *              R); 0 = automatic: the last group's outputs cannot overlap any
- *              compute, so the first and last groups are small (about an eighth of
- *              the KV heads each) and the others about a quarter each
- *              (focus_host_groups lists the sizes)
- *   ws         device workspace of focus_host_workspace_size(p, n_groups) bytes (the
- *              whole inputs, two staging sets of one group, one group's workspace)
+ *              R); 0 = automatic: the first group's inputs and the last group's
+ *              outputs cannot overlap any compute, so those two groups are small
+ *              (about an eighth of the KV heads each) and the others about a
+ *              quarter each (focus_host_groups lists the sizes)
+ *   ws         device workspace of focus_host_workspace_size(p, n_groups) bytes
  *   compute_stream, copy_stream  two different streams (NULL = legacy default)
  * Host memory should be page-locked (cudaHostAlloc / cudaHostRegister), else the
  * copies are staged synchronously by CUDA. Returns after enqueuing: the outputs are

@@ -286,35 +286,6 @@ int focus_attn_fwd(const focus_params* p, const uint16_t* q, const uint16_t* k,
   return focus_attn_fwd_ev(p, q, k, v, r, C, mask_in, o, lse, ws, ws_bytes, stream, nullptr);
 }
 
-namespace focus {
-namespace hostcopy {
-
-// dst row i = 16-byte units [off16, off16 + dst16) of src row i: a head group's slice of
-// token-major rows (rows of all heads) into rows of the group's heads.
-__global__ void gather_cols(const uint4* __restrict__ src, uint4* __restrict__ dst, int64_t rows,
-                            int src16, int dst16, int off16) {
-  const int64_t total = rows * dst16;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
-       i += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t r = i / dst16;
-    dst[i] = src[r * src16 + off16 + (int)(i - r * dst16)];
-  }
-}
-
-cudaError_t launch_gather_cols(const char* src, char* dst, int64_t rows, size_t src_row_bytes,
-                               size_t dst_row_bytes, size_t off_bytes, cudaStream_t s) {
-  int dev = 0, sms = 148;
-  if (cudaGetDevice(&dev) == cudaSuccess)
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  gather_cols<<<(unsigned)(sms * 8), 256, 0, s>>>(
-      reinterpret_cast<const uint4*>(src), reinterpret_cast<uint4*>(dst), rows,
-      (int)(src_row_bytes / 16), (int)(dst_row_bytes / 16), (int)(off_bytes / 16));
-  return cudaGetLastError();
-}
-
-}  // namespace hostcopy
-}  // namespace focus
-
 // ------------------------------------------------------------ host buffers --
 namespace {
 
@@ -382,12 +353,8 @@ focus_params group_params(const focus_params& p, int kv_cnt) {
   return q;
 }
 
-// Host-entry workspace: the whole problem's inputs (copied in flat), two staging sets
-// for one group's inputs and outputs, and the attention workspace of the largest group.
 struct HostLayout {
-  size_t fq, fk, fv, fr, C;                // whole inputs
-  size_t sets, q, k, v, o, lse, r, set_bytes;  // staging set s at sets + s * set_bytes, offsets within
-  size_t attn, attn_bytes, total;
+  size_t q, k, v, o, lse, r, set_bytes, C, attn, attn_bytes, total;
 };
 
 HostLayout host_layout(const focus_params& p, const HostGroups& G) {
@@ -400,33 +367,20 @@ HostLayout host_layout(const focus_params& p, const HostGroups& G) {
     return at;
   };
   const size_t BN = (size_t)p.B * p.N;
-  H.fq = take(BN * p.H * p.d_head * 2);
-  H.fk = take(BN * p.H_kv * p.d_head * 2);
-  H.fv = take(BN * p.H_kv * p.d_head * 2);
-  H.fr = take(BN * p.R * FOCUS_D_G * 4);
+  H.q = take(BN * g.H * p.d_head * 2);
+  H.k = take(BN * g.H_kv * p.d_head * 2);
+  H.v = take(BN * g.H_kv * p.d_head * 2);
+  H.o = take(BN * g.H * p.d_head * 2);
+  H.lse = take((size_t)p.B * g.H * p.N * 4);
+  H.r = take(BN * g.R * FOCUS_D_G * 4);
+  H.set_bytes = off;
+  off = 2 * H.set_bytes;  // two staging sets
   H.C = take((size_t)p.K * FOCUS_D_G * 4);
-  H.sets = off;
-  size_t so = 0;
-  auto take_s = [&](size_t bytes) {
-    const size_t at = so;
-    so = align_up(so + bytes, 256);
-    return at;
-  };
-  H.q = take_s(BN * g.H * p.d_head * 2);
-  H.k = take_s(BN * g.H_kv * p.d_head * 2);
-  H.v = take_s(BN * g.H_kv * p.d_head * 2);
-  H.o = take_s(BN * g.H * p.d_head * 2);
-  H.lse = take_s((size_t)p.B * g.H * p.N * 4);
-  H.r = take_s(BN * g.R * FOCUS_D_G * 4);
-  H.set_bytes = so;
-  off = H.sets + 2 * H.set_bytes;  // two staging sets
   H.attn_bytes = layout(g).total;  // the largest group's workspace serves every group
   H.attn = take(H.attn_bytes);
   H.total = off;
   return H;
 }
-
-
 
 }  // namespace
 
@@ -464,84 +418,82 @@ int focus_attn_fwd_host(const focus_params* p, const uint16_t* q_h, const uint16
   char* w = (char*)ws;
   const size_t d2 = (size_t)p->d_head * 2;
   const size_t BN = (size_t)p->B * p->N;
-  const int gq = p->H / p->H_kv;          // query heads per KV head
-  const int kv_per_rho = p->H_kv / p->R;  // KV heads per routing head
-  const size_t rrow = (size_t)FOCUS_D_G * 4;  // bytes of one routing head's vector
+  const int gq = p->H / p->H_kv;                   // query heads per KV head
+  const int kv_per_rho = p->H_kv / p->R;           // KV heads per routing head
 
-  cudaEvent_t ev_in, ev_comp[2], ev_out[2];
-  if (cudaEventCreateWithFlags(&ev_in, cudaEventDisableTiming) != cudaSuccess) return FOCUS_ERR_CUDA;
-  int made = 0;
-  for (; made < 2; ++made) {
-    if (cudaEventCreateWithFlags(&ev_comp[made], cudaEventDisableTiming) != cudaSuccess) break;
-    if (cudaEventCreateWithFlags(&ev_out[made], cudaEventDisableTiming) != cudaSuccess) {
-      cudaEventDestroy(ev_comp[made]);
-      break;
-    }
+  cudaEvent_t ev_in[2], ev_comp[2];
+  for (int i = 0; i < 2; ++i) {
+    if (cudaEventCreateWithFlags(&ev_in[i], cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&ev_comp[i], cudaEventDisableTiming) != cudaSuccess)
+      return FOCUS_ERR_CUDA;
   }
   auto cleanup = [&](int code) {
-    cudaEventDestroy(ev_in);
-    for (int i = 0; i < made; ++i) {
+    for (int i = 0; i < 2; ++i) {
+      cudaEventDestroy(ev_in[i]);
       cudaEventDestroy(ev_comp[i]);
-      cudaEventDestroy(ev_out[i]);
     }
     return code;
   };
-  if (made < 2) return cleanup(FOCUS_ERR_CUDA);
-  auto set_ptr = [&](int g, size_t off) { return w + HL.sets + (g & 1) * HL.set_bytes + off; };
-
-  // Inputs go in whole, one transfer per tensor: strided host reads (a million rows
-  // of a few hundred bytes per head group) ran several times slower than flat ones on
-  // some hosts, while strided writes back to host memory kept their speed.
-  struct Copy { char* dst; const void* src; size_t bytes; };
-  const Copy ins[5] = {{w + HL.fq, q_h, BN * p->H * d2}, {w + HL.fk, k_h, BN * p->H_kv * d2},
-                       {w + HL.fv, v_h, BN * p->H_kv * d2}, {w + HL.fr, r_h, BN * p->R * rrow},
-                       {w + HL.C, C_h, (size_t)p->K * rrow}};
-  for (const Copy& c : ins)
-    if ((rc = cuda_rc(cudaMemcpyAsync(c.dst, c.src, c.bytes, cudaMemcpyHostToDevice, xs))))
-      return cleanup(rc);
-  if ((rc = cuda_rc(cudaEventRecord(ev_in, xs)))) return cleanup(rc);
-  if ((rc = cuda_rc(cudaStreamWaitEvent(cs, ev_in, 0)))) return cleanup(rc);
-
-  for (int g = 0; g < G.n; ++g) {
+  auto set_ptr = [&](int g, size_t off) { return w + (g & 1) * HL.set_bytes + off; };
+  // inputs of group g into staging set g % 2 (strided 2-D copies out of the host layout)
+  auto copy_in = [&](int g) -> cudaError_t {
     const focus_params gp = group_params(*p, G.cnt[g]);
-    const size_t kv0 = (size_t)G.off[g], h0 = kv0 * gq, rho0 = p->R == 1 ? 0 : kv0 / kv_per_rho;
-    // staging set g % 2: its outputs from group g - 2 have been copied out
-    if (g >= 2 && (rc = cuda_rc(cudaStreamWaitEvent(cs, ev_out[g & 1], 0)))) return cleanup(rc);
-    // this group's heads split off the whole inputs on the device
-    if ((rc = cuda_rc(hostcopy::launch_gather_cols(w + HL.fq, set_ptr(g, HL.q), (int64_t)BN, p->H * d2,
-                                         gp.H * d2, h0 * d2, cs))) ||
-        (rc = cuda_rc(hostcopy::launch_gather_cols(w + HL.fk, set_ptr(g, HL.k), (int64_t)BN, p->H_kv * d2,
-                                         gp.H_kv * d2, kv0 * d2, cs))) ||
-        (rc = cuda_rc(hostcopy::launch_gather_cols(w + HL.fv, set_ptr(g, HL.v), (int64_t)BN, p->H_kv * d2,
-                                         gp.H_kv * d2, kv0 * d2, cs))))
-      return cleanup(rc);
-    const float* r_g = reinterpret_cast<const float*>(w + HL.fr);  // R = 1: every group shares it
-    if (p->R > 1) {
-      if ((rc = cuda_rc(hostcopy::launch_gather_cols(w + HL.fr, set_ptr(g, HL.r), (int64_t)BN, p->R * rrow,
-                                           gp.R * rrow, rho0 * rrow, cs))))
-        return cleanup(rc);
-      r_g = reinterpret_cast<const float*>(set_ptr(g, HL.r));
-    }
+    const size_t kv0 = (size_t)G.off[g], h0 = kv0 * gq;
+    cudaError_t e;
+    if (g >= 2 && (e = cudaStreamWaitEvent(xs, ev_comp[g & 1], 0)) != cudaSuccess) return e;
+    if ((e = cudaMemcpy2DAsync(set_ptr(g, HL.q), gp.H * d2, q_h + h0 * p->d_head, p->H * d2,
+                               gp.H * d2, BN, cudaMemcpyHostToDevice, xs)))
+      return e;
+    if ((e = cudaMemcpy2DAsync(set_ptr(g, HL.k), gp.H_kv * d2, k_h + kv0 * p->d_head,
+                               p->H_kv * d2, gp.H_kv * d2, BN, cudaMemcpyHostToDevice, xs)))
+      return e;
+    if ((e = cudaMemcpy2DAsync(set_ptr(g, HL.v), gp.H_kv * d2, v_h + kv0 * p->d_head,
+                               p->H_kv * d2, gp.H_kv * d2, BN, cudaMemcpyHostToDevice, xs)))
+      return e;
+    const size_t rw = (size_t)gp.R * FOCUS_D_G * 4;
+    const float* rsrc = r_h + (p->R == 1 ? 0 : (kv0 / kv_per_rho) * FOCUS_D_G);
+    if ((e = cudaMemcpy2DAsync(set_ptr(g, HL.r), rw, rsrc, (size_t)p->R * FOCUS_D_G * 4, rw, BN,
+                               cudaMemcpyHostToDevice, xs)))
+      return e;
+    return cudaEventRecord(ev_in[g & 1], xs);
+  };
+  auto copy_out = [&](int g) -> cudaError_t {
+    const focus_params gp = group_params(*p, G.cnt[g]);
+    const size_t h0 = (size_t)G.off[g] * gq;
+    cudaError_t e;
+    if ((e = cudaStreamWaitEvent(xs, ev_comp[g & 1], 0))) return e;
+    if ((e = cudaMemcpy2DAsync(o_h + h0 * p->d_head, p->H * d2, set_ptr(g, HL.o), gp.H * d2,
+                               gp.H * d2, BN, cudaMemcpyDeviceToHost, xs)))
+      return e;
+    if (lse_h &&
+        (e = cudaMemcpy2DAsync(lse_h + h0 * p->N, (size_t)p->H * p->N * 4, set_ptr(g, HL.lse),
+                               (size_t)gp.H * p->N * 4, (size_t)gp.H * p->N * 4, p->B,
+                               cudaMemcpyDeviceToHost, xs)))
+      return e;
+    return cudaSuccess;
+  };
+
+  if ((rc = cuda_rc(cudaMemcpyAsync(w + HL.C, C_h, (size_t)p->K * FOCUS_D_G * 4,
+                                    cudaMemcpyHostToDevice, xs))))
+    return cleanup(rc);
+  if ((rc = cuda_rc(copy_in(0)))) return cleanup(rc);
+  for (int g = 0; g < G.n; ++g) {
+    if (g + 1 < G.n && (rc = cuda_rc(copy_in(g + 1)))) return cleanup(rc);
+    // compute of group g: inputs landed; staging outputs of set g % 2 were copied out
+    // (copy_out(g - 2) precedes copy_in(g) on the copy stream, which the event covers)
+    if ((rc = cuda_rc(cudaStreamWaitEvent(cs, ev_in[g & 1], 0)))) return cleanup(rc);
+    const focus_params gp = group_params(*p, G.cnt[g]);
     rc = focus_attn_fwd(&gp, reinterpret_cast<const uint16_t*>(set_ptr(g, HL.q)),
                         reinterpret_cast<const uint16_t*>(set_ptr(g, HL.k)),
-                        reinterpret_cast<const uint16_t*>(set_ptr(g, HL.v)), r_g,
+                        reinterpret_cast<const uint16_t*>(set_ptr(g, HL.v)),
+                        reinterpret_cast<const float*>(set_ptr(g, HL.r)),
                         reinterpret_cast<const float*>(w + HL.C), nullptr,
                         reinterpret_cast<uint16_t*>(set_ptr(g, HL.o)),
                         reinterpret_cast<float*>(set_ptr(g, HL.lse)), w + HL.attn, HL.attn_bytes,
                         cs);
     if (rc) return cleanup(rc);
     if ((rc = cuda_rc(cudaEventRecord(ev_comp[g & 1], cs)))) return cleanup(rc);
-    // outputs of group g copied out (strided) while group g + 1 computes
-    if ((rc = cuda_rc(cudaStreamWaitEvent(xs, ev_comp[g & 1], 0)))) return cleanup(rc);
-    if ((rc = cuda_rc(cudaMemcpy2DAsync(o_h + h0 * p->d_head, p->H * d2, set_ptr(g, HL.o),
-                                        gp.H * d2, gp.H * d2, BN, cudaMemcpyDeviceToHost, xs))))
-      return cleanup(rc);
-    if (lse_h &&
-        (rc = cuda_rc(cudaMemcpy2DAsync(lse_h + h0 * p->N, (size_t)p->H * p->N * 4, set_ptr(g, HL.lse),
-                                        (size_t)gp.H * p->N * 4, (size_t)gp.H * p->N * 4, p->B,
-                                        cudaMemcpyDeviceToHost, xs))))
-      return cleanup(rc);
-    if ((rc = cuda_rc(cudaEventRecord(ev_out[g & 1], xs)))) return cleanup(rc);
+    if ((rc = cuda_rc(copy_out(g)))) return cleanup(rc);
   }
   return cleanup(FOCUS_OK);
 }
