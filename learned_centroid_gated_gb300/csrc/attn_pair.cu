@@ -6,7 +6,10 @@
 // (pos_j <= pos_i - w) and the window keys are disjoint, so this pass merges with the
 // window pass's normalised partial (O_w, LSE_w) by log-sum-exp.  Same work items,
 // plans, tile order and result as attn_tc<128, kSeg> (exact-set segments), on an
-// engine that keeps the tensor core busier:
+// engine built to take the next S off the softmax's critical path.  On the workloads
+// measured it is slower than attn_tc (7.1 against 5.5 ms at 32K tokens: a thread's
+// fixed costs per tile, not the tensor core, bound it), so it runs only when
+// FOCUS_LONG_ENGINE=pair asks for it:
 //
 // A cluster of two CTAs (the two SMs of a TPC) runs each 256-row query block; CTA r
 // holds rows 128 r .. 128 r + 127.  One thread of CTA 0 issues every MMA with
