@@ -50,3 +50,18 @@ def test_cpu_binding_never_raises_without_nvml_or_gpu():
         assert os.sched_getaffinity(0) == before
     else:
         os.sched_setaffinity(0, before)
+
+
+def test_code_hash_ignores_comments_not_code(tmp_path):
+    """The traffic capture stays valid across comment and whitespace edits of the
+    kernel source and is voided by a code change."""
+    sys.path.insert(0, ROOT)
+    import bench
+    a = tmp_path / "a.cu"
+    a.write_text("int f(int x) {  // one\n  return x + 1; /* two */\n}\n")
+    b = tmp_path / "b.cu"
+    b.write_text("// header\nint f(int x)\n{\n  return x + 1;\n}\n")
+    c = tmp_path / "c.cu"
+    c.write_text("int f(int x) { return x + 2; }\n")
+    assert bench.code_hash(str(a)) == bench.code_hash(str(b))
+    assert bench.code_hash(str(a)) != bench.code_hash(str(c))
