@@ -3,6 +3,8 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "common.cuh"
 
 namespace focus {
@@ -53,6 +55,26 @@ int check_params(const focus_params* p) {
 }
 
 namespace {
+
+// NVTX ranges that name the stages of a call for a profiler (a no-op unless one is
+// attached): at(i) closes the previous stage's range and opens stage i's.
+class StageRanges {
+ public:
+  explicit StageRanges(const char* const* names, int count) : names_(names), count_(count) {}
+  void at(int i) {
+    if (open_) nvtxRangePop();
+    open_ = i < count_;
+    if (open_) nvtxRangePushA(names_[i]);
+  }
+  ~StageRanges() {
+    if (open_) nvtxRangePop();
+  }
+
+ private:
+  const char* const* names_;
+  int count_;
+  bool open_ = false;
+};
 
 WsLayout layout(const focus_params& p) {
   WsLayout L{};
@@ -248,7 +270,12 @@ int focus_attn_fwd_ev(const focus_params* p, const uint16_t* q, const uint16_t* 
   const bf16* qb = reinterpret_cast<const bf16*>(q);
   const bf16* kb = reinterpret_cast<const bf16*>(k);
   const bf16* vb = reinterpret_cast<const bf16*>(v);
+  static const char* const kStageNames[] = {"focus fwd: routing", "focus fwd: bucketing",
+                                            "focus fwd: permuted copies", "focus fwd: window",
+                                            "focus fwd: long-range"};
+  StageRanges ranges(kStageNames, 5);
   auto mark = [&](int i) -> int {
+    ranges.at(i);
     if (!stage_events) return FOCUS_OK;
     return cuda_rc(cudaEventRecord((cudaEvent_t)stage_events[i], s));
   };
@@ -528,7 +555,11 @@ int focus_attn_bwd_ev(const focus_params* p, const uint16_t* q, const uint16_t* 
   bf16* dqb = reinterpret_cast<bf16*>(dq);
   bf16* dkb = reinterpret_cast<bf16*>(dk);
   bf16* dvb = reinterpret_cast<bf16*>(dv);
+  static const char* const kStageNames[] = {"focus bwd: prepare", "focus bwd: window",
+                                            "focus bwd: long-range dq", "focus bwd: long-range dk dv"};
+  StageRanges ranges(kStageNames, 4);
   auto mark = [&](int i) -> int {
+    ranges.at(i);
     if (!stage_events) return FOCUS_OK;
     return cuda_rc(cudaEventRecord((cudaEvent_t)stage_events[i], s));
   };
