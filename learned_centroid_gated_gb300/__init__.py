@@ -22,7 +22,10 @@ import re
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libfocus.so")
+# FOCUS_DEBUG_BOUNDS=1: the debug build (index checks raise FOCUS_ERR_BOUNDS; build it
+# with the same variable set), else the default build
+LIB_PATH = os.path.join(_HERE, "libfocus_debug.so" if os.environ.get("FOCUS_DEBUG_BOUNDS", "")
+                        not in ("", "0") else "libfocus.so")
 HEADER = os.path.join(os.path.dirname(_HERE), "include", "focus.h")
 
 if not os.path.exists(LIB_PATH):

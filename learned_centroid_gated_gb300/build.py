@@ -15,11 +15,15 @@ import sys
 HERE = os.path.dirname(os.path.abspath(__file__))
 SRC = os.path.join(HERE, "csrc")
 ROOT = os.path.dirname(HERE)
-BUILD = os.path.join(ROOT, "_build")
-LIB = os.path.join(HERE, "libfocus.so")
+# FOCUS_DEBUG_BOUNDS=1 builds the debug variant (index checks that raise
+# FOCUS_ERR_BOUNDS on the status word) into its own objects and libfocus_debug.so; the
+# binding loads it when the same variable is set at import.
+DEBUG = os.environ.get("FOCUS_DEBUG_BOUNDS", "") not in ("", "0")
+BUILD = os.path.join(ROOT, "_build_debug" if DEBUG else "_build")
+LIB = os.path.join(HERE, "libfocus_debug.so" if DEBUG else "libfocus.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
-              "-Xptxas", "-warn-spills"] + ARCH
+              "-Xptxas", "-warn-spills"] + ARCH + (["-DFOCUS_DEBUG_BOUNDS"] if DEBUG else [])
 
 
 def _nvcc() -> str:

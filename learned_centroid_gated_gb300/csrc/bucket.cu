@@ -115,7 +115,7 @@ bucket_scan(int nseg, int nchunk, const int* __restrict__ hist, int* __restrict_
 // Stable scatter: perm[seg_base + rank] = n. Same chunking as bucket_hist.
 __global__ void __launch_bounds__(32)
 bucket_scatter(int N, int K, int top_k, int nseg, const uint32_t* __restrict__ mask,
-               const int* __restrict__ cbase, int* __restrict__ perm) {
+               const int* __restrict__ cbase, int* __restrict__ perm, int* status) {
   extern __shared__ int cur[];
   const int br = blockIdx.y, chunk = blockIdx.x, lane = threadIdx.x;
   const int* cb = cbase + ((int64_t)br * gridDim.x + chunk) * nseg;
@@ -134,7 +134,7 @@ bucket_scatter(int N, int K, int top_k, int nseg, const uint32_t* __restrict__ m
     const unsigned peers = __match_any_sync(0xffffffffu, sg);
     if (sg >= 0) {
       const int dst = cur[sg] + __popc(peers & lanemask_lt());
-      P[dst] = n;
+      if (FOCUS_IN_BOUNDS(dst >= 0 && dst < N, status)) P[dst] = n;
     }
     __syncwarp();
     if (sg >= 0 && (peers & lanemask_lt()) == 0u) cur[sg] += __popc(peers);
@@ -444,11 +444,12 @@ build_plan_bwd(int N, int NR, int w, int nseg, int group, const int* __restrict_
 __global__ void __launch_bounds__(256)
 permute_qkv(int N, int NR, int H, int H_kv, int R, int d, const int* __restrict__ perm,
             const uint4* __restrict__ q, const uint4* __restrict__ k, const uint4* __restrict__ v,
-            uint4* __restrict__ qp, uint4* __restrict__ kp, uint4* __restrict__ vp) {
+            uint4* __restrict__ qp, uint4* __restrict__ kp, uint4* __restrict__ vp, int* status) {
   const int64_t row = blockIdx.x;  // (b * R + rho) * NR + n'
   const int br = (int)(row / NR), np = (int)(row % NR);
   const int b = br / R, rho = br % R;
   const int n = perm[row];
+  if (!FOCUS_IN_BOUNDS(n >= 0 && n < N, status)) return;
   const int hq = H / R, hkv = H_kv / R;
   const int vec = d / 8;  // uint4 per head row
   const int nq = hq * vec, nk = hkv * vec, total = nq + 2 * nk;
@@ -507,7 +508,7 @@ cudaError_t launch_bucket(const focus_params& p, const WsLayout& L, const uint32
   const size_t shm = sizeof(int) * L.nseg;
   bucket_hist<<<grid, 32, shm, s>>>(p.N, p.K, p.top_k, L.nseg, mask, hist, status);
   bucket_scan<<<BR, 1024, 0, s>>>(L.nseg, L.nchunk, hist, segoff, cbase);
-  bucket_scatter<<<grid, 32, shm, s>>>(p.N, p.K, p.top_k, L.nseg, mask, cbase, perm);
+  bucket_scatter<<<grid, 32, shm, s>>>(p.N, p.K, p.top_k, L.nseg, mask, cbase, perm, status);
   return cudaGetLastError();
 }
 
@@ -542,7 +543,8 @@ cudaError_t launch_permute(const focus_params& p, const WsLayout& L, const bf16*
       p.N, L.NR, p.H, p.H_kv, p.R, p.d_head, reinterpret_cast<const int*>(ws + L.perm),
       reinterpret_cast<const uint4*>(q), reinterpret_cast<const uint4*>(k),
       reinterpret_cast<const uint4*>(v), reinterpret_cast<uint4*>(ws + L.qp),
-      reinterpret_cast<uint4*>(ws + L.kp), reinterpret_cast<uint4*>(ws + L.vp));
+      reinterpret_cast<uint4*>(ws + L.kp), reinterpret_cast<uint4*>(ws + L.vp),
+      &reinterpret_cast<WsHeader*>(ws)->status);
   return cudaGetLastError();
 }
 

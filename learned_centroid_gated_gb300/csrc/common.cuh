@@ -79,6 +79,20 @@ __host__ __device__ inline uint32_t binom(int n, int r) {
 // Raise a device status code (the first one raised wins).
 __device__ inline void raise_status(int* status, int code) { atomicCAS(status, 0, code); }
 
+// Index checks of the debug build (compiled with FOCUS_DEBUG_BOUNDS, see build.py): an
+// index read from device data that falls outside its array raises FOCUS_ERR_BOUNDS on
+// the status word and the access is skipped.  In the default build the check is
+// `true` and costs nothing.
+#ifdef FOCUS_DEBUG_BOUNDS
+__device__ inline bool in_bounds(bool ok, int* status) {
+  if (!ok && status) raise_status(status, FOCUS_ERR_BOUNDS);
+  return ok;
+}
+#define FOCUS_IN_BOUNDS(cond, status) ::focus::in_bounds((cond), (status))
+#else
+#define FOCUS_IN_BOUNDS(cond, status) true
+#endif
+
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // ------------------------------------------------------------ kernel launchers --
